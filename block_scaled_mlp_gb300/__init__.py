@@ -1,0 +1,297 @@
+"""MXFP8 training MLP for Blackwell sm_103a: a thin ctypes binding of the C-ABI
+library ``libmxmlp.so`` (declared in ``include/mxmlp.h``).
+
+Every function here only marshals arguments: it checks tensor devices and
+dtypes, allocates output tensors with PyTorch (device memory and streams are
+all PyTorch is used for), and calls the C entry point of the same name on the
+current CUDA stream.  There is no other code path: if the library is missing
+the calls raise ``MxError``.
+
+Tensors:
+  bf16 activations/weights     torch.bfloat16, contiguous, on a CUDA device
+  MXFP8 codes                  torch.uint8 (E4M3 bit patterns)
+  scales                       torch.uint8 (E8M0 bytes, MMA or linear layout)
+  group offsets                torch.int32 on the device (cumulative ends)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MxError", "lib", "library_path", "ROW", "COL", "BOTH", "SCALE_LINEAR", "SCALE_MMA",
+    "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "GROUP_M", "GROUP_K", "mma_scale_bytes",
+    "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
+    "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "MlpContext", "ErrorWord",
+]
+
+ROW, COL, BOTH = 1, 2, 3
+SCALE_LINEAR, SCALE_MMA = 0, 1
+RECIPE_RCEIL, RECIPE_RCEIL_WGRAD_HP = 0, 1
+GROUP_M, GROUP_K = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmxmlp.so")
+_lib = None
+
+_V, _I64, _I32, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+_SIGS = {
+    "mx_version": ([], _I),
+    "mx_status_string": ([_I], ctypes.c_char_p),
+    "mx_last_error": ([], ctypes.c_char_p),
+    "mx_quantize": ([_V, _I64, _I64, _I, _I, _V, _V, _V, _V, _V], _I),
+    "mx_swiglu_quant": ([_V, _I64, _I64, _I, _I, _V, _V, _V, _V, _V], _I),
+    "mx_swiglu_quant_bwd": ([_V, _V, _I64, _I64, _I, _I, _V, _V, _V, _V, _V, _V, _V], _I),
+    "mx_scaled_mm": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _V, _V], _I),
+    "mx_grouped_mm": ([_I, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _V, _V, _V], _I),
+    "mx_bf16_wgrad": ([_V, _V, _I64, _I64, _I64, _V, _I32, _I32, _V, _V, _V], _I),
+    "mx_mlp_workspace_size": ([_I64, _I64, _I64, _I32, _I, ctypes.POINTER(ctypes.c_size_t),
+                               ctypes.POINTER(ctypes.c_size_t)], _I),
+    "mx_mlp_fwd": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V], _I),
+    "mx_mlp_bwd": ([_V, _V, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V,
+                    _V, _V], _I),
+}
+
+
+class MxError(RuntimeError):
+    """A libmxmlp call failed (status code and message from the library)."""
+
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def lib():
+    """Load libmxmlp.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise MxError(-1, f"{library_path} is not built; run __graft_entry__.build()")
+        L = ctypes.CDLL(library_path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        L = lib()
+        raise MxError(rc, f"{L.mx_status_string(rc).decode()}: {L.mx_last_error().decode()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise MxError(1, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MxError(1, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MxError(1, f"{name} must be contiguous")
+
+
+def mma_scale_bytes(rows: int, cols: int) -> int:
+    """Bytes of the MMA-layout scales of a [rows, cols] matrix (cols/32 scales per row)."""
+    s = cols // 32
+    return ((rows + 127) // 128) * ((s + 3) // 4) * 512
+
+
+def _scales(rows, cols, layout, device, batch=None):
+    n = mma_scale_bytes(rows, cols) if layout == SCALE_MMA else rows * (cols // 32)
+    shape = (n,) if batch is None else (batch, n)
+    return torch.empty(shape, dtype=torch.uint8, device=device)
+
+
+class ErrorWord:
+    """Device int32 that kernels OR their fault bits into."""
+
+    def __init__(self, device=None):
+        self.t = torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+    def ptr(self):
+        return ctypes.c_void_p(self.t.data_ptr())
+
+    def value(self) -> int:
+        return int(self.t.item())
+
+    def check(self):
+        v = self.value()
+        if v:
+            raise MxError(v, f"device fault bits 0x{v:x} ({lib().mx_status_string(v).decode()})")
+
+
+# ---------------------------------------------------------------- per-op calls
+
+
+def quantize(x, axis=BOTH, layout=SCALE_MMA):
+    """MXFP8 cast of a bf16 [rows, cols] matrix.  Returns a dict with
+    q_row [rows, cols], s_row, q_col [cols, rows], s_col (absent axes None)."""
+    _need(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    dev = x.device
+    out = dict(q_row=None, s_row=None, q_col=None, s_col=None)
+    if axis & ROW:
+        out["q_row"] = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        out["s_row"] = _scales(rows, cols, layout, dev)
+    if axis & COL:
+        out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        out["s_col"] = _scales(cols, rows, layout, dev)
+    _check(lib().mx_quantize(_ptr(x), rows, cols, axis, layout, _ptr(out["q_row"]), _ptr(out["s_row"]),
+                             _ptr(out["q_col"]), _ptr(out["s_col"]), _stream()))
+    return out
+
+
+def swiglu_quant(h13, axis=BOTH, layout=SCALE_MMA):
+    """Fused SwiGLU of h13 [M, 2h] = [g | u] with dual MXFP8 quantization of
+    y [M, h].  Returns dict(q_row [M,h], s_row, q_col [h,M], s_col)."""
+    _need(h13, torch.bfloat16, "h13")
+    M, h2 = h13.shape
+    h = h2 // 2
+    dev = h13.device
+    out = dict(q_row=torch.empty((M, h), dtype=torch.uint8, device=dev), s_row=_scales(M, h, layout, dev),
+               q_col=None, s_col=None)
+    if axis & COL:
+        out["q_col"] = torch.empty((h, M), dtype=torch.uint8, device=dev)
+        out["s_col"] = _scales(h, M, layout, dev)
+    _check(lib().mx_swiglu_quant(_ptr(h13), M, h, axis, layout, _ptr(out["q_row"]), _ptr(out["s_row"]),
+                                 _ptr(out["q_col"]), _ptr(out["s_col"]), _stream()))
+    return out
+
+
+def swiglu_quant_bwd(dy, h13, axis=BOTH, layout=SCALE_MMA, bf16_transposed=False):
+    """Fused SwiGLU backward: dh13 = [dg | du] quantized rowwise (and
+    columnwise with axis=BOTH).  With bf16_transposed=True (rowwise only) it
+    also returns dh13_t [2h, M] and y_t [h, M] in bf16."""
+    _need(dy, torch.bfloat16, "dy")
+    _need(h13, torch.bfloat16, "h13")
+    M, h = dy.shape
+    dev = dy.device
+    out = dict(q_row=torch.empty((M, 2 * h), dtype=torch.uint8, device=dev),
+               s_row=_scales(M, 2 * h, layout, dev), q_col=None, s_col=None, dh13_t=None, y_t=None)
+    if axis & COL:
+        out["q_col"] = torch.empty((2 * h, M), dtype=torch.uint8, device=dev)
+        out["s_col"] = _scales(2 * h, M, layout, dev)
+    if bf16_transposed:
+        out["dh13_t"] = torch.empty((2 * h, M), dtype=torch.bfloat16, device=dev)
+        out["y_t"] = torch.empty((h, M), dtype=torch.bfloat16, device=dev)
+    _check(lib().mx_swiglu_quant_bwd(_ptr(dy), _ptr(h13), M, h, axis, layout, _ptr(out["q_row"]),
+                                     _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]),
+                                     _ptr(out["dh13_t"]), _ptr(out["y_t"]), _stream()))
+    return out
+
+
+def scaled_mm(aq, as_, bq, bs, err: ErrorWord | None = None):
+    """C[M, N] = deq(A) deq(B)^T in bf16 (MMA-layout scales)."""
+    _need(aq, torch.uint8, "aq")
+    _need(bq, torch.uint8, "bq")
+    M, K = aq.shape
+    N = bq.shape[0]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    _check(lib().mx_scaled_mm(_ptr(aq), _ptr(as_), _ptr(bq), _ptr(bs), M, N, K, _ptr(c),
+                              err.ptr() if err else None, _stream()))
+    return c
+
+
+def grouped_mm(mode, aq, as_, bq, bs, offs, pad_multiple=128, err: ErrorWord | None = None):
+    """Grouped MXFP8 GEMM.  GROUP_M: aq [M_total, K], bq [E, N, K] -> [M_total, N].
+    GROUP_K: aq [N, M_total], bq [K, M_total] -> [E, N, K]."""
+    _need(offs, torch.int32, "offs")
+    E = offs.numel()
+    if mode == GROUP_M:
+        M_total, K = aq.shape
+        N = bq.shape[1]
+        c = torch.empty((M_total, N), dtype=torch.bfloat16, device=aq.device)
+    else:
+        N, M_total = aq.shape
+        K = bq.shape[0]
+        c = torch.empty((E, N, K), dtype=torch.bfloat16, device=aq.device)
+    _check(lib().mx_grouped_mm(mode, _ptr(aq), _ptr(as_), _ptr(bq), _ptr(bs), M_total, N, K, _ptr(offs), E,
+                               pad_multiple, _ptr(c), err.ptr() if err else None, _stream()))
+    return c
+
+
+def bf16_wgrad(a, b, offs=None, pad_multiple=128, err: ErrorWord | None = None):
+    """bf16 weight gradient: a [N, M_total], b [K, M_total] -> [E, N, K]
+    (or [N, K] with offs=None)."""
+    _need(a, torch.bfloat16, "a")
+    _need(b, torch.bfloat16, "b")
+    N, M_total = a.shape
+    K = b.shape[0]
+    E = 1 if offs is None else offs.numel()
+    shape = (N, K) if offs is None else (E, N, K)
+    c = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
+    _check(lib().mx_bf16_wgrad(_ptr(a), _ptr(b), M_total, N, K, _ptr(offs), E, pad_multiple, _ptr(c),
+                               err.ptr() if err else None, _stream()))
+    return c
+
+
+# ---------------------------------------------------------------- MLP
+
+
+def mlp_workspace_size(M_total, d, h, E=0, recipe=RECIPE_RCEIL):
+    c = ctypes.c_size_t()
+    s = ctypes.c_size_t()
+    _check(lib().mx_mlp_workspace_size(M_total, d, h, E, recipe, ctypes.byref(c), ctypes.byref(s)))
+    return c.value, s.value
+
+
+class MlpContext:
+    """What mlp_fwd saves for mlp_bwd (a caller-owned device buffer plus the
+    call's arguments)."""
+
+    def __init__(self, buf, args):
+        self.buf = buf
+        self.args = args
+
+
+def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL, pad_multiple=128, scratch=None,
+            err: ErrorWord | None = None, out=None):
+    """MXFP8 SwiGLU MLP forward.  Dense: w1/w3 [h, d], w2 [d, h].  Grouped
+    (offs given): w1/w3 [E, h, d], w2 [E, d, h].  Returns (out, ctx)."""
+    for n, t in (("x", x), ("w1", w1), ("w3", w3), ("w2", w2)):
+        _need(t, torch.bfloat16, n)
+    M, d = x.shape
+    h = w1.shape[-2]
+    E = 0 if offs is None else offs.numel()
+    cb, sb = mlp_workspace_size(M, d, h, E, recipe)
+    ctx = torch.empty(cb, dtype=torch.uint8, device=x.device)
+    if scratch is None or scratch.numel() < sb:
+        scratch = torch.empty(sb, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mx_mlp_fwd(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), M, d, h, _ptr(offs), max(E, 1), pad_multiple,
+                            recipe, _ptr(ctx), _ptr(scratch), _ptr(out), err.ptr() if err else None, _stream()))
+    return out, MlpContext(ctx, dict(x=x, w1=w1, w3=w3, w2=w2, offs=offs, recipe=recipe, M=M, d=d, h=h, E=E,
+                                     pad=pad_multiple))
+
+
+def mlp_bwd(ctx: MlpContext, dout, scratch=None, err: ErrorWord | None = None, grads=None):
+    """MXFP8 SwiGLU MLP backward from mlp_fwd's context.  Returns (dx, dw1, dw3, dw2)."""
+    a = ctx.args
+    _need(dout, torch.bfloat16, "dout")
+    M, d, h, E = a["M"], a["d"], a["h"], a["E"]
+    _, sb = mlp_workspace_size(M, d, h, E, a["recipe"])
+    if scratch is None or scratch.numel() < sb:
+        scratch = torch.empty(sb, dtype=torch.uint8, device=dout.device)
+    if grads is None:
+        dx = torch.empty((M, d), dtype=torch.bfloat16, device=dout.device)
+        dw1 = torch.empty_like(a["w1"])
+        dw3 = torch.empty_like(a["w3"])
+        dw2 = torch.empty_like(a["w2"])
+    else:
+        dx, dw1, dw3, dw2 = grads
+    _check(lib().mx_mlp_bwd(_ptr(ctx.buf), _ptr(dout), _ptr(a["x"]), _ptr(a["w1"]), _ptr(a["w3"]), _ptr(a["w2"]),
+                            M, d, h, _ptr(a["offs"]), max(E, 1), a["pad"], a["recipe"], _ptr(scratch), _ptr(dx),
+                            _ptr(dw1), _ptr(dw3), _ptr(dw2), err.ptr() if err else None, _stream()))
+    return dx, dw1, dw3, dw2

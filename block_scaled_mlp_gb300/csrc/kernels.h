@@ -1,0 +1,85 @@
+// kernels.h - internal host interface between the C-ABI layer (api.cu) and
+// the kernel launchers (quant.cu, swiglu.cu, gemm.cu).  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/mxmlp.h"
+
+namespace mx {
+
+// ---------------------------------------------------------------- host utils
+int num_sms();
+// Records a thread-local message; returns `code`.
+int fail(int code, const char* fmt, ...);
+int cuda_status(cudaError_t e, const char* what);
+int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
+
+// ---------------------------------------------------------------- quantize
+struct QuantLaunch {
+  const void* x;
+  int64_t rows, cols;
+  int32_t batch;
+  int layout;
+  // rowwise MX: codes [rows, cols] per batch item; batch strides qr_bs
+  // (codes) and sr_bs (scale bytes), 0 = densely packed
+  void* q_row;
+  void* s_row;
+  int64_t qr_bs, sr_bs;
+  // columnwise MX: codes of column c at q_col + c*qc_ld + qc_off (+ b*qc_bs)
+  void* q_col;
+  void* s_col;
+  int64_t qc_ld, qc_off, qc_bs, sc_bs;
+  // columnwise bf16 transpose (instead of q_col): element (r, c) at
+  // t_col[c*tc_ld + tc_off + r] (+ b*tc_bs)
+  void* t_col;
+  int64_t tc_ld, tc_off, tc_bs;
+  int32_t* err;
+};
+int launch_quant(const QuantLaunch& q, cudaStream_t stream);
+
+// ---------------------------------------------------------------- SwiGLU
+struct SwigluLaunch {
+  const void* h13;   // [M, 2h]
+  const void* dy;    // [M, h] (backward only)
+  int64_t M, h;
+  int layout;
+  void* q_row; void* s_row;   // fwd: y rows [M,h]; bwd: dh13 rows [M,2h]
+  void* q_col; void* s_col;   // fwd: y cols [h,M]; bwd: dh13 cols [2h,M]
+  void* dh13_t;               // bwd, optional: [2h, M] bf16
+  void* y_t;                  // bwd, optional: [h, M] bf16
+  int32_t* err;
+};
+int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream);
+int launch_swiglu_bwd(const SwigluLaunch& s, cudaStream_t stream);
+
+// ---------------------------------------------------------------- GEMM
+enum GemmMode { GEMM_DENSE = 0, GEMM_GROUP_M = 1, GEMM_GROUP_K = 2 };
+
+struct GemmLaunch {
+  int mx;                 // 1: MXFP8 block-scaled, 0: bf16
+  int mode;               // GemmMode
+  // C[m, n] = sum_k A[m, k] B[n, k]
+  const void* a;          // [M, K] (DENSE/GROUP_M) or [M, Ktot] (GROUP_K)
+  const void* sfa;        // MMA-layout scales of A
+  const void* b;          // [N, K], [E, N, K] (GROUP_M) or [N, Ktot] (GROUP_K)
+  const void* sfb;
+  int64_t M, N, K;        // GROUP_K: K = total tokens
+  const int32_t* offs;    // group ends (GROUP_M: over M, GROUP_K: over K)
+  int32_t E;
+  // output: row m of C goes to c0 (m < split) or c1 (m - split) when split>0;
+  // GROUP_K: output [E, M, N], expert e row m at (e*Msub + m) of c0/c1 where
+  // Msub = split ? split : M.
+  void* c0;
+  void* c1;
+  int64_t split;
+  int32_t* err;
+};
+int launch_gemm(const GemmLaunch& g, cudaStream_t stream);
+
+}  // namespace mx

@@ -1,0 +1,227 @@
+// quant.cu - standalone MXFP8 cast of bf16 matrices (rowwise, columnwise or
+// both from one read), plus a bf16 transposed copy used by the bf16
+// weight-gradient recipe.
+//
+// Design: a persistent kernel streams 128x128 bf16 tiles through a 3-stage
+// TMA ring in shared memory (one producer warp, eight consumer warps).  The
+// rowwise path reads 16-byte row segments from the tile (4 lanes per
+// 32-element block, warp-shuffle amax); the columnwise path reads 4-byte
+// column pairs down 32 rows (one thread per block) - the transpose happens
+// in shared memory, so every global load and store stays coalesced.
+#include "tile_quant.cuh"
+#include "kernels.h"
+
+namespace mx {
+
+namespace {
+
+constexpr int QT_R = 128;          // tile rows
+constexpr int QT_C = 128;          // tile cols (two 64-column TMA boxes)
+constexpr int QT_STAGES = 3;
+constexpr int QT_BOX_BYTES = QT_R * 64 * 2;        // 16 KB
+constexpr int QT_TILE_BYTES = 2 * QT_BOX_BYTES;    // 32 KB
+constexpr int QT_CONSUMER_WARPS = 8;
+constexpr int QT_THREADS = (QT_CONSUMER_WARPS + 1) * 32;
+constexpr size_t QT_SMEM = QT_STAGES * QT_TILE_BYTES + 1024 + 64;
+
+struct QuantKParams {
+  int64_t rows, cols;
+  int32_t batch;
+  int64_t row_tiles, col_tiles;
+  // rowwise MX
+  uint8_t* q_row; int64_t qr_ld; int64_t qr_bs;
+  ScaleDst s_row; int64_t sr_bs;
+  // columnwise MX: dest [cols, *] codes, row c at q_col + c*qc_ld + qc_off
+  uint8_t* q_col; int64_t qc_ld; int64_t qc_off; int64_t qc_bs;
+  ScaleDst s_col; int64_t sc_off; int64_t sc_bs;
+  // columnwise bf16 transpose: dest [cols, *] bf16
+  uint16_t* t_col; int64_t tc_ld; int64_t tc_off; int64_t tc_bs;
+  int32_t* err;
+};
+
+// COLK: 0 no columnwise output, 1 MXFP8 columnwise, 2 bf16 transpose.
+template <bool ROW, int COLK>
+__global__ void __launch_bounds__(QT_THREADS, 2)
+    quant_kernel(const __grid_constant__ CUtensorMap tmx, QuantKParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + QT_STAGES * QT_TILE_BYTES);
+  uint64_t* empty = full + QT_STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t tiles_per_b = p.row_tiles * p.col_tiles;
+  const int64_t n_tiles = tiles_per_b * p.batch;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QT_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], QT_CONSUMER_WARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == QT_CONSUMER_WARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmx);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t b = t / tiles_per_b;
+        const int64_t rem = t - b * tiles_per_b;
+        const int64_t rt = rem / p.col_tiles, ct = rem - rt * p.col_tiles;
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.err)) break;
+        mbar_arrive_expect_tx(&full[stage], QT_TILE_BYTES);
+        uint8_t* dst = smem + stage * QT_TILE_BYTES;
+        tma_load_3d(dst, &tmx, (int32_t)(ct * QT_C), (int32_t)(rt * QT_R), (int32_t)b, &full[stage]);
+        tma_load_3d(dst + QT_BOX_BYTES, &tmx, (int32_t)(ct * QT_C + 64), (int32_t)(rt * QT_R),
+                    (int32_t)b, &full[stage]);
+        if (++stage == QT_STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t b = t / tiles_per_b;
+    const int64_t rem = t - b * tiles_per_b;
+    const int64_t rt = rem / p.col_tiles, ct = rem - rt * p.col_tiles;
+    const int64_t r0 = rt * QT_R, c0 = ct * QT_C;
+    if (!mbar_wait(&full[stage], phase, p.err)) break;
+    const uint8_t* tile = smem + stage * QT_TILE_BYTES;
+
+    if (ROW) {
+      // 16 lanes per 128-column row, 8 elements per lane; 2 rows per warp step.
+      const int seg = lane & 15;
+      const int box = seg >> 3, chunk = seg & 7;
+      uint8_t* qrow = p.q_row + b * p.qr_bs;
+      ScaleDst sd = p.s_row;
+      sd.base += b * p.sr_bs;
+#pragma unroll 2
+      for (int it = 0; it < QT_R / (2 * QT_CONSUMER_WARPS); ++it) {
+        const int rr = it * (2 * QT_CONSUMER_WARPS) + warp * 2 + (lane >> 4);
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + box * QT_BOX_BYTES + rr * 128 + chunk * 16);
+        const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
+        uint32_t s;
+        const uint2 codes = quant_row8(pk, s);
+        const int64_t r = r0 + rr;
+        const int64_t c = c0 + box * 64 + chunk * 8;
+        if (r < p.rows && c < p.cols) {
+          *reinterpret_cast<uint2*>(qrow + r * p.qr_ld + c) = codes;
+          if ((chunk & 3) == 0) sd.put(r, c >> 5, s);
+        }
+      }
+    }
+
+    if (COLK != 0) {
+      // one thread per (column pair, 32-row block)
+      const int rb = warp & 3;
+      const int pair = (warp >> 2) * 32 + lane;     // 0..63
+      const int box = pair >> 5, pc = pair & 31;
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        v[i] = *reinterpret_cast<const uint32_t*>(tile + box * QT_BOX_BYTES + (rb * 32 + i) * 128 + pc * 4);
+      const int64_t rg = r0 + rb * 32;
+      const int64_t cg = c0 + box * 64 + pc * 2;
+      if (rg < p.rows && cg < p.cols) {
+        if (COLK == 1) {
+          uint8_t* qcol = p.q_col + b * p.qc_bs;
+          ScaleDst sd = p.s_col;
+          sd.base += b * p.sc_bs;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t col[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) col[i] = half ? (v[i] >> 16) : (v[i] & 0xFFFFu);
+            uint32_t codes[8];
+            const uint32_t s = quant_col32(col, codes);
+            uint8_t* dst = qcol + (cg + half) * p.qc_ld + p.qc_off + rg;
+            store16(dst, codes[0], codes[1], codes[2], codes[3]);
+            store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
+            sd.put(cg + half, p.sc_off + (rg >> 5), s);
+          }
+        } else {
+          uint16_t* tcol = p.t_col + b * p.tc_bs;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t a0 = half ? (v[2 * i] >> 16) : (v[2 * i] & 0xFFFFu);
+              const uint32_t a1 = half ? (v[2 * i + 1] >> 16) : (v[2 * i + 1] & 0xFFFFu);
+              w[i] = a0 | (a1 << 16);
+            }
+            uint16_t* dst = tcol + (cg + half) * p.tc_ld + p.tc_off + rg;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) store16(dst + q * 8, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+        }
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == QT_STAGES) { stage = 0; phase ^= 1; }
+  }
+}
+
+}  // namespace
+
+int launch_quant(const QuantLaunch& q, cudaStream_t stream) {
+  const bool row = q.q_row != nullptr;
+  const int colk = q.q_col ? 1 : (q.t_col ? 2 : 0);
+  CUtensorMap tm;
+  {
+    uint64_t dims[3] = {(uint64_t)q.cols, (uint64_t)q.rows, (uint64_t)q.batch};
+    uint64_t strides[2] = {(uint64_t)q.cols * 2, (uint64_t)q.cols * q.rows * 2};
+    uint32_t box[3] = {64, QT_R, 1};
+    int rc = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q.x), dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  QuantKParams p{};
+  p.rows = q.rows; p.cols = q.cols; p.batch = q.batch;
+  p.row_tiles = (q.rows + QT_R - 1) / QT_R;
+  p.col_tiles = (q.cols + QT_C - 1) / QT_C;
+  p.q_row = (uint8_t*)q.q_row; p.qr_ld = q.cols; p.qr_bs = q.qr_bs ? q.qr_bs : q.rows * q.cols;
+  const int64_t S_row = q.cols / 32;
+  p.s_row = ScaleDst{(uint8_t*)q.s_row, (S_row + 3) / 4, S_row, q.layout == MX_SCALE_MMA};
+  p.sr_bs = q.sr_bs ? q.sr_bs
+                    : (q.layout == MX_SCALE_MMA ? ((q.rows + 127) / 128) * ((S_row + 3) / 4) * 512 : q.rows * S_row);
+  p.q_col = (uint8_t*)q.q_col; p.qc_ld = q.qc_ld; p.qc_off = q.qc_off; p.qc_bs = q.qc_bs;
+  const int64_t S_col = q.qc_ld / 32;
+  p.s_col = ScaleDst{(uint8_t*)q.s_col, (S_col + 3) / 4, S_col, q.layout == MX_SCALE_MMA};
+  p.sc_off = q.qc_off / 32; p.sc_bs = q.sc_bs;
+  p.t_col = (uint16_t*)q.t_col; p.tc_ld = q.tc_ld; p.tc_off = q.tc_off; p.tc_bs = q.tc_bs;
+  p.err = q.err;
+
+  const int64_t n_tiles = p.row_tiles * p.col_tiles * q.batch;
+  if (n_tiles == 0) return MX_OK;
+  int grid = (int)std::min<int64_t>(n_tiles, (int64_t)num_sms() * 2);
+  cudaError_t e;
+#define MX_LAUNCH_Q(R, C)                                                                      \
+  do {                                                                                         \
+    auto k = quant_kernel<R, C>;                                                               \
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QT_SMEM);    \
+    if (e == cudaSuccess) {                                                                    \
+      k<<<grid, QT_THREADS, QT_SMEM, stream>>>(tm, p);                                         \
+      e = cudaGetLastError();                                                                  \
+    }                                                                                          \
+  } while (0)
+  if (row && colk == 0) MX_LAUNCH_Q(true, 0);
+  else if (row && colk == 1) MX_LAUNCH_Q(true, 1);
+  else if (row && colk == 2) MX_LAUNCH_Q(true, 2);
+  else if (!row && colk == 1) MX_LAUNCH_Q(false, 1);
+  else if (!row && colk == 2) MX_LAUNCH_Q(false, 2);
+  else return MX_ERR_INVALID_ARG;
+#undef MX_LAUNCH_Q
+  return cuda_status(e, "quant_kernel launch");
+}
+
+}  // namespace mx

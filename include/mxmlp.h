@@ -1,0 +1,243 @@
+/*
+ * mxmlp.h - C ABI of the MXFP8 training-MLP library (libmxmlp.so).
+ *
+ * The library runs the hot path of an MXFP8 SwiGLU MLP on one Blackwell GPU
+ * (sm_103a): w13 GEMM -> SwiGLU with dual MXFP8 quantization -> w2 GEMM, in
+ * dense and grouped-expert form, forward and backward, as described on the
+ * page "Add MXFP8 fused-MLP overrides in torchtitan" (pytorch/torchtitan PR
+ * 4257), Summary section.  The per-op entry points follow the two ops the
+ * page "TrainingWeightWrapperTensor base class; subclasses for FP8/MXFP8 with
+ * grouped_mm and linear overrides" (pytorch/ao PR 3968) overrides: linear
+ * (mx_scaled_mm) and grouped_mm (mx_grouped_mm).
+ *
+ * MXFP8: 32-element blocks of FP8 E4M3 codes sharing one E8M0 power-of-two
+ * scale.  Scale rule (RCEIL): 2^e with e the smallest integer such that
+ * amax <= 448 * 2^e, clamped to [-127,127]; byte e+127.  Codes: v*2^-e
+ * rounded to nearest even, saturated to +-448.  All-zero block: scale 0x00.
+ * A block holding a NaN or an infinity: scale 0xFF, every code 0x7F.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers, row-major, densely packed
+ *   unless a leading dimension is given.  bf16 tensors are passed as
+ *   `const void*` / `void*` holding IEEE bfloat16 values.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *   only enqueues work on `stream` and returns; it never synchronizes.
+ * - The caller owns every buffer.  No entry point allocates device memory
+ *   (mx_mlp_workspace_size tells the caller how much to provide).
+ * - Arguments are validated on the host before anything is enqueued.  On a
+ *   bad argument the call returns a non-zero mx_status and enqueues nothing;
+ *   mx_last_error() then holds a one-line description (thread-local).
+ *   There is no fallback path: unsupported shapes return
+ *   MX_ERR_UNSUPPORTED.
+ * - Faults found on the device (non-monotone or unaligned group offsets, a
+ *   pipeline wait that exceeded its bound) are OR-ed as mx_status bits into
+ *   the caller's `err_word` (int32, device memory; may be NULL where noted)
+ *   and the kernel skips the faulty work instead of trapping.
+ * - Scale layout MX_SCALE_MMA is the block-scaled tensor-core layout: the
+ *   [R, S] scale matrix (R rows, S = cols/32 scale columns) is cut into
+ *   128-row x 4-column tiles of 512 bytes; tile (rb, cb) sits at byte
+ *   (rb * ceil(S/4) + cb) * 512, and inside a tile scale (r, c) sits at
+ *   (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4).  Size:
+ *   ceil(R/128) * ceil(S/4) * 512 bytes; padding bytes are written as 0x00.
+ *   MX_SCALE_LINEAR is the plain [R, S] row-major byte matrix.
+ */
+#ifndef MXMLP_H
+#define MXMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MX_API __attribute__((visibility("default")))
+#else
+#define MX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes are distinct bits so that device-side faults can be OR-ed
+ * into one error word. */
+typedef enum {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1,  /* null pointer, negative or zero size, bad enum */
+  MX_ERR_ALIGNMENT = 2,    /* pointer or leading dimension not 16-byte aligned */
+  MX_ERR_UNSUPPORTED = 4,  /* shape the kernels do not cover (no fallback) */
+  MX_ERR_BAD_OFFSETS = 8,  /* group offsets decreasing, unaligned or past M */
+  MX_ERR_TIMEOUT = 16,     /* a device pipeline wait exceeded its bound */
+  MX_ERR_CUDA = 32         /* a CUDA runtime/driver call failed */
+} mx_status;
+
+typedef enum { MX_ROW = 1, MX_COL = 2, MX_BOTH = 3 } mx_axis;
+typedef enum { MX_SCALE_LINEAR = 0, MX_SCALE_MMA = 1 } mx_scale_layout;
+/* MX_RECIPE_RCEIL: every GEMM in MXFP8.  MX_RECIPE_RCEIL_WGRAD_HP: forward
+ * and input-gradient GEMMs in MXFP8, weight-gradient GEMMs in bf16
+ * ("wgrad_with_hp", pages "TrainingWeightWrapperTensor base class ..." and
+ * "[mxfp8 training] unified MXFP8TrainingConfig ...", Autograd function
+ * changes). */
+typedef enum { MX_RECIPE_RCEIL = 0, MX_RECIPE_RCEIL_WGRAD_HP = 1 } mx_recipe;
+typedef enum { MX_GROUP_M = 0, MX_GROUP_K = 1 } mx_grouped_mode;
+
+/* Library version (major*10000 + minor*100 + patch). */
+MX_API int mx_version(void);
+/* Static string for a status code (bits OR-ed together name the first). */
+MX_API const char* mx_status_string(int status);
+/* Thread-local description of the last failing call on this thread. */
+MX_API const char* mx_last_error(void);
+
+/*
+ * mx_quantize - MXFP8 cast of a bf16 matrix, rowwise and/or columnwise.
+ * The "standalone cast" of the torchtitan page (Numerics and tests).
+ *
+ *   x       [rows, cols] bf16.
+ *   axis    MX_ROW: blocks of 32 along cols  -> q_row [rows, cols] u8,
+ *                                              s_row scales of [rows, cols/32]
+ *           MX_COL: blocks of 32 along rows  -> q_col [cols, rows] u8 (the
+ *                                              transposed matrix, contiguous
+ *                                              along rows), s_col scales of
+ *                                              [cols, rows/32]
+ *           MX_BOTH: both (one read of x).
+ *   layout  scale layout of s_row / s_col (MX_SCALE_LINEAR or MX_SCALE_MMA).
+ * Requirements: cols % 32 == 0; for MX_COL/MX_BOTH rows % 32 == 0; x and
+ * the code buffers 16-byte aligned; cols * 2 bytes a multiple of 16.
+ * Unused outputs may be NULL.
+ */
+MX_API int mx_quantize(const void* x, int64_t rows, int64_t cols, int axis, int layout,
+                void* q_row, void* s_row, void* q_col, void* s_col, void* stream);
+
+/*
+ * mx_swiglu_quant - fused SwiGLU forward with dual MXFP8 quantization; the
+ * bf16 activation y is never written to memory (torchtitan page, Summary:
+ * "fused SwiGLU + dual MXFP8 quantization", "never materializes the BF16
+ * post-activation tensor").
+ *
+ *   h13     [M, 2h] bf16: g = h13[:, :h] (x . w1^T), u = h13[:, h:] (x . w3^T).
+ *   y       = RN_bf16(RN_f32(a * u)), a = RN_bf16(RN_f32(g * sigma)),
+ *             sigma = 1/(1+exp(-g)) correctly rounded to fp32.
+ *   MX_ROW  -> yq_row [M, h] u8 + ys_row scales of [M, h/32]
+ *   MX_COL  -> yq_col [h, M] u8 + ys_col scales of [h, M/32]
+ * Requirements: h % 64 == 0, M % 32 == 0 (M % 128 == 0 with MX_COL).
+ */
+MX_API int mx_swiglu_quant(const void* h13, int64_t M, int64_t h, int axis, int layout,
+                    void* yq_row, void* ys_row, void* yq_col, void* ys_col, void* stream);
+
+/*
+ * mx_swiglu_quant_bwd - fused SwiGLU backward with dual MXFP8 quantization of
+ * dh13 = [dg | du] (torchtitan page, Summary: "1 bwd fused op").
+ *
+ *   dy      [M, h] bf16 (gradient of y);  h13 [M, 2h] bf16 from the forward.
+ *   du      = RN_bf16(RN_f32(dy * a));
+ *   dg      = RN_bf16(dy * u * sigma * (1 + g * (1 - sigma))) rounded once
+ *             from the exact value (NaN for non-finite g).
+ *   MX_ROW  -> dq_row [M, 2h] u8 + ds_row scales of [M, 2h/32]
+ *   MX_COL  -> dq_col [2h, M] u8 + ds_col scales of [2h, M/32]
+ *   dh13_t  optional (may be NULL): dh13 in bf16, TRANSPOSED: [2h, M]
+ *   y_t     optional (may be NULL): the recomputed forward y in bf16,
+ *           TRANSPOSED: [h, M].  The transposed (token-contiguous) layout is
+ *           the one the bf16 weight-gradient GEMM of the wgrad_with_hp recipe
+ *           reads.
+ * Requirements: as mx_swiglu_quant; dh13_t / y_t need M % 128 == 0.
+ */
+MX_API int mx_swiglu_quant_bwd(const void* dy, const void* h13, int64_t M, int64_t h, int axis,
+                        int layout, void* dq_row, void* ds_row, void* dq_col, void* ds_col,
+                        void* dh13_t, void* y_t, void* stream);
+
+/*
+ * mx_scaled_mm - block-scaled MXFP8 GEMM on the tcgen05 tensor cores:
+ *   C[M, N] (bf16, RN) = deq(A)[M, K] . deq(B)[N, K]^T, fp32 accumulation.
+ *   aq [M, K] u8, as scales MX_SCALE_MMA of [M, K/32];
+ *   bq [N, K] u8, bs scales MX_SCALE_MMA of [N, K/32].
+ * Requirements: M % 128 == 0, N % 128 == 0, K % 128 == 0.
+ * err_word may be NULL.
+ */
+MX_API int mx_scaled_mm(const void* aq, const void* as, const void* bq, const void* bs, int64_t M,
+                 int64_t N, int64_t K, void* c, int32_t* err_word, void* stream);
+
+/*
+ * mx_grouped_mm - grouped block-scaled MXFP8 GEMM over expert-major token
+ * groups (grouped_mm override, ao page; padded dispatch with pad_multiple =
+ * 128, torchtitan page, Summary).
+ *
+ *   offs    [E] int32 device array of cumulative group ends: group e owns
+ *           token rows [offs[e-1], offs[e]) (offs[-1] = 0).  Every group size
+ *           must be a multiple of pad_multiple (only 128 is supported), the
+ *           offsets non-decreasing and offs[E-1] <= M_total.  Read on the
+ *           device: no host synchronization.
+ *   MX_GROUP_M (forward / input gradient):
+ *           A = aq [M_total, K] (tokens), B = bq [E, N, K] (per-expert
+ *           weights, scales MX_SCALE_MMA per expert, expert stride
+ *           (N/128)*(K/128)*512 bytes), C = c [M_total, N] bf16.  Rows past
+ *           offs[E-1] are written as zeros.  Empty groups cost nothing.
+ *   MX_GROUP_K (weight gradient):
+ *           A = aq [N, M_total], B = bq [K, M_total] (columnwise copies,
+ *           contiguous along tokens), C = c [E, N, K] bf16 with
+ *           C[e] = A[:, group e] . B[:, group e]^T.  An empty group's C[e]
+ *           is written as exact zeros.
+ * Requirements: M_total, N, K multiples of 128; 1 <= E <= 1024.
+ * err_word (may be NULL) receives MX_ERR_BAD_OFFSETS if offs violates the
+ * rules; the offending groups are then skipped.
+ */
+MX_API int mx_grouped_mm(int mode, const void* aq, const void* as, const void* bq, const void* bs,
+                  int64_t M_total, int64_t N, int64_t K, const int32_t* offs, int32_t E,
+                  int32_t pad_multiple, void* c, int32_t* err_word, void* stream);
+
+/*
+ * mx_bf16_wgrad - bf16 weight-gradient GEMM of the wgrad_with_hp recipe on
+ * the tcgen05 tensor cores (kind::f16), fp32 accumulation, bf16 RN output.
+ *   a [N, M_total] bf16, b [K, M_total] bf16 (token-contiguous, e.g. the
+ *   transposed outputs of mx_swiglu_quant_bwd), c [E, N, K] bf16 with
+ *   C[e] = a[:, group e] . b[:, group e]^T.  offs as in mx_grouped_mm; pass
+ *   offs = NULL and E = 1 for the dense case (one group of M_total tokens).
+ * Requirements: M_total, N, K multiples of 128.
+ */
+MX_API int mx_bf16_wgrad(const void* a, const void* b, int64_t M_total, int64_t N, int64_t K,
+                  const int32_t* offs, int32_t E, int32_t pad_multiple, void* c,
+                  int32_t* err_word, void* stream);
+
+/*
+ * mx_mlp_workspace_size - bytes of the two caller-provided buffers of
+ * mx_mlp_fwd / mx_mlp_bwd for a given problem.
+ *   ctx_bytes      saved-for-backward context (written by mx_mlp_fwd, read
+ *                  by mx_mlp_bwd): h13 in bf16 and the quantized operands.
+ *   scratch_bytes  temporary buffer used inside one call (fwd or bwd).
+ * E = 0 selects the dense MLP (weights without an expert axis).
+ */
+MX_API int mx_mlp_workspace_size(int64_t M_total, int64_t d, int64_t h, int32_t E, int recipe,
+                          size_t* ctx_bytes, size_t* scratch_bytes);
+
+/*
+ * mx_mlp_fwd - forward of the MXFP8 SwiGLU MLP (torchtitan page, Summary):
+ *   out = (silu(x . w1^T) * (x . w3^T)) . w2^T with every GEMM in MXFP8.
+ *   x [M_total, d] bf16; dense: w1, w3 [h, d], w2 [d, h]; grouped (offs not
+ *   NULL): w1, w3 [E, h, d], w2 [E, d, h] and offs/E/pad_multiple as in
+ *   mx_grouped_mm.  w1 and w3 are packed into w13 = [w1; w3] while they are
+ *   quantized; the caller's weights are never modified.
+ *   ctx, scratch: buffers of the sizes mx_mlp_workspace_size returns (16-byte
+ *   aligned).  out [M_total, d] bf16.
+ * Requirements: M_total % 128 == 0, d % 128 == 0, h % 128 == 0.
+ */
+MX_API int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, int64_t M_total,
+               int64_t d, int64_t h, const int32_t* offs, int32_t E, int32_t pad_multiple,
+               int recipe, void* ctx, void* scratch, void* out, int32_t* err_word,
+               void* stream);
+
+/*
+ * mx_mlp_bwd - backward of the MXFP8 SwiGLU MLP from the context mx_mlp_fwd
+ * wrote (same shapes, recipe, offs and weights as that forward call).
+ *   dout [M_total, d] bf16 -> dx [M_total, d], dw1, dw3 ([h, d] or
+ *   [E, h, d]) and dw2 ([d, h] or [E, d, h]), all bf16.  The weight
+ *   gradients are overwritten (not accumulated).  The w13 gradient is
+ *   written straight into dw1 and dw3.
+ */
+MX_API int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const void* w1, const void* w3,
+               const void* w2, int64_t M_total, int64_t d, int64_t h, const int32_t* offs,
+               int32_t E, int32_t pad_multiple, int recipe, void* scratch, void* dx, void* dw1,
+               void* dw3, void* dw2, int32_t* err_word, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXMLP_H */

@@ -1,0 +1,87 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point the header declares, and rejects bad arguments on the host (before
+any CUDA call) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxmlp.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_scaled_mlp_gb300 as mx
+    return mx.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"MX_API\s+(?:const\s+char\*|int)\s+(mx_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ["mx_quantize", "mx_swiglu_quant", "mx_swiglu_quant_bwd", "mx_scaled_mm", "mx_grouped_mm",
+                 "mx_bf16_wgrad", "mx_mlp_workspace_size", "mx_mlp_fwd", "mx_mlp_bwd"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert L.mx_status_string(0) == b"MX_OK"
+    assert L.mx_status_string(8) == b"MX_ERR_BAD_OFFSETS"
+    assert L.mx_status_string(16) == b"MX_ERR_TIMEOUT"
+    assert L.mx_version() >= 100
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_quantize_rejects_bad_arguments(L):
+    p = _fake()
+    assert L.mx_quantize(None, 64, 64, 3, 1, p, p, p, p, None) == 1           # null x
+    assert L.mx_quantize(p, 64, 48, 1, 1, p, p, None, None, None) == 4        # cols % 32
+    assert L.mx_quantize(p, 48, 64, 2, 1, None, None, p, p, None) == 4        # rows % 32 for COL
+    assert L.mx_quantize(p, 64, 64, 5, 1, p, p, p, p, None) == 1              # bad axis
+    assert L.mx_quantize(_fake(0x10001), 64, 64, 1, 1, p, p, None, None, None) == 2  # alignment
+    assert b"aligned" in L.mx_last_error()
+
+
+def test_gemm_rejects_bad_arguments(L):
+    p = _fake()
+    assert L.mx_scaled_mm(p, p, p, p, 100, 128, 128, p, None, None) == 4
+    assert L.mx_grouped_mm(0, p, p, p, p, 256, 128, 128, p, 4, 64, p, None, None) == 4   # pad 64
+    assert L.mx_grouped_mm(0, p, p, p, p, 256, 128, 128, p, 0, 128, p, None, None) == 1  # E = 0
+    assert L.mx_grouped_mm(7, p, p, p, p, 256, 128, 128, p, 4, 128, p, None, None) == 1  # mode
+    assert L.mx_bf16_wgrad(p, p, 256, 128, 128, None, 3, 128, p, None, None) == 1         # dense needs E=1
+
+
+def test_mlp_workspace_and_validation(L):
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.mx_mlp_workspace_size(256, 256, 512, 0, 0, ctypes.byref(c), ctypes.byref(s)) == 0
+    # ctx holds at least h13 (bf16) and the columnwise copies
+    assert c.value >= 256 * 1024 * 2 + 256 * 256 + 512 * 256
+    assert s.value > 0
+    c2, s2 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.mx_mlp_workspace_size(256, 256, 512, 0, 1, ctypes.byref(c2), ctypes.byref(s2)) == 0
+    p = _fake()
+    assert L.mx_mlp_fwd(p, p, p, p, 200, 256, 512, None, 0, 128, 0, p, p, p, None, None) == 4
+    assert L.mx_mlp_fwd(p, p, p, p, 256, 256, 512, p, 4, 128, 9, p, p, p, None, None) == 1
+    assert L.mx_mlp_bwd(p, None, p, p, p, p, 256, 256, 512, None, 0, 128, 0, p, p, p, p, p, None, None) == 1
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    import block_scaled_mlp_gb300 as mx
+    with pytest.raises(mx.MxError):
+        mx.quantize(torch.zeros(64, 64, dtype=torch.bfloat16))

@@ -1,0 +1,132 @@
+"""GPU parity of the fused SwiGLU + dual MXFP8 quantization kernels against
+the oracle (forward: bit-exact codes/scales; backward: du and the codes
+bit-exact, dg reported as the fraction of codes one step away)."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_mlp_gb300 as mx
+import synth
+from oracle import mx_oracle as o
+from tests.util import bits, to_dev, u8
+
+pytestmark = pytest.mark.gpu
+
+
+def _h13(M, h, seed, scale=1.3):
+    return synth.normal_bf16((M, 2 * h), scale, seed)
+
+
+def test_silu_every_bf16_input_exact():
+    """a(g) for all 65536 bf16 g: with u = 1 and dy = 0 the backward's
+    recomputed y equals a(g) exactly, and y_t exposes it in bf16."""
+    g = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 128)
+    M, h = 512, 128
+    h13 = np.concatenate([g, np.full((M, h), 0x3F80, dtype=np.uint16)], axis=1)  # u = 1.0
+    dy = np.zeros((M, h), dtype=np.uint16)
+    res = mx.swiglu_quant_bwd(to_dev(dy), to_dev(h13), axis=mx.ROW, bf16_transposed=True)
+    torch.cuda.synchronize()
+    a_gpu = bits(res["y_t"]).T
+    a_ref = o.swiglu_fwd(g, h13[:, h:])
+    nan = np.isnan(o.bf16_to_f64(a_ref))
+    assert np.array_equal(np.isnan(o.bf16_to_f64(a_gpu)), nan)
+    mism = (a_gpu != a_ref) & ~nan
+    assert not mism.any(), f"{mism.sum()} mismatches, e.g. g bits {g[mism][:8]}"
+
+
+@pytest.mark.parametrize("M,h", [(256, 512), (384, 192), (128, 64)])
+def test_swiglu_fwd_dual_matches_oracle(M, h):
+    h13 = _h13(M, h, seed=M + h)
+    res = mx.swiglu_quant(to_dev(h13), mx.BOTH, mx.SCALE_MMA)
+    torch.cuda.synchronize()
+    g, u = o.split_h13(h13)
+    y = o.swiglu_fwd(g, u)
+    q, s = o.quantize_rows(y)
+    assert np.array_equal(u8(res["q_row"]), q)
+    assert np.array_equal(u8(res["s_row"]), o.scales_to_mma(s))
+    qc, sc = o.quantize_cols(y)
+    assert np.array_equal(u8(res["q_col"]), qc)
+    assert np.array_equal(u8(res["s_col"]), o.scales_to_mma(sc))
+
+
+def test_swiglu_fwd_extreme_inputs():
+    """Large |g| (slow path), zeros, -0, infinities and NaN in g and u."""
+    M, h = 128, 128
+    rng = np.random.default_rng(1)
+    g = rng.standard_normal((M, h)) * np.exp(rng.uniform(-8, 6, (M, h)))
+    u = rng.standard_normal((M, h)) * np.exp(rng.uniform(-8, 6, (M, h)))
+    g[0, :8] = [0.0, -0.0, np.inf, -np.inf, np.nan, 100.0, -100.0, -90.0]
+    u[1, :4] = [np.inf, 0.0, -0.0, np.nan]
+    h13 = np.concatenate([o.round_to_bf16_bits(g), o.round_to_bf16_bits(u)], axis=1)
+    res = mx.swiglu_quant(to_dev(h13), mx.BOTH, mx.SCALE_LINEAR)
+    torch.cuda.synchronize()
+    y = o.swiglu_fwd(*o.split_h13(h13))
+    q, s = o.quantize_rows(y)
+    assert np.array_equal(u8(res["q_row"]), q)
+    assert np.array_equal(u8(res["s_row"]).reshape(s.shape), s)
+    qc, sc = o.quantize_cols(y)
+    assert np.array_equal(u8(res["q_col"]), qc)
+
+
+def _bwd_ref(dy, h13):
+    g, u = o.split_h13(h13)
+    dg, du = o.swiglu_bwd(dy, g, u)
+    return np.concatenate([dg, du], axis=1), o.swiglu_fwd(g, u)
+
+
+@pytest.mark.parametrize("M,h", [(256, 512), (192, 128)])
+def test_swiglu_bwd_dual_matches_oracle(M, h):
+    h13 = _h13(M, h, seed=7 + M)
+    dy = synth.normal_bf16((M, h), 1.0, seed=8 + M)
+    res = mx.swiglu_quant_bwd(to_dev(dy), to_dev(h13), mx.BOTH, mx.SCALE_MMA)
+    torch.cuda.synchronize()
+    dh13, _ = _bwd_ref(dy, h13)
+    q, s = o.quantize_rows(dh13)
+    qc, sc = o.quantize_cols(dh13)
+    got_q, got_qc = u8(res["q_row"]), u8(res["q_col"])
+    # du half bit-exact; dg codes within one E4M3 step, fraction reported
+    assert np.array_equal(got_q[:, h:], q[:, h:])
+    dist = o.e4m3_code_distance(got_q[:, :h], q[:, :h])
+    assert dist.max() <= 1
+    frac = float((dist > 0).mean())
+    print(f"dg one-code fraction (rowwise): {frac:.3e}")
+    assert np.array_equal(u8(res["s_row"]), o.scales_to_mma(s))
+    assert np.array_equal(got_qc, qc)
+    assert np.array_equal(u8(res["s_col"]), o.scales_to_mma(sc))
+
+
+def test_swiglu_bwd_bf16_outputs_exact():
+    """The HP recipe's bf16 outputs: dh13 = [dg | du] and y, transposed."""
+    M, h = 256, 256
+    h13 = _h13(M, h, seed=21, scale=3.0)
+    dy = synth.normal_bf16((M, h), 1.0, seed=22)
+    res = mx.swiglu_quant_bwd(to_dev(dy), to_dev(h13), mx.ROW, mx.SCALE_MMA, bf16_transposed=True)
+    torch.cuda.synchronize()
+    dh13, y = _bwd_ref(dy, h13)
+    got = bits(res["dh13_t"]).T
+    mism = got != dh13
+    print(f"dh13 bf16 mismatch fraction: {mism.mean():.3e}")
+    assert not mism.any()
+    assert np.array_equal(bits(res["y_t"]).T, y)
+    q, s = o.quantize_rows(dh13)
+    assert np.array_equal(u8(res["q_row"]), q)
+
+
+def test_swiglu_bwd_extreme_inputs():
+    M, h = 128, 64
+    rng = np.random.default_rng(2)
+    g = rng.standard_normal((M, h)) * np.exp(rng.uniform(-6, 6, (M, h)))
+    u = rng.standard_normal((M, h)) * np.exp(rng.uniform(-6, 6, (M, h)))
+    dy = rng.standard_normal((M, h)) * np.exp(rng.uniform(-6, 6, (M, h)))
+    g[0, :8] = [0.0, -0.0, np.inf, -np.inf, np.nan, 100.0, -1000.0, -1.2784645]
+    g[1, :] = -1.2784645 + rng.uniform(-0.01, 0.01, h)    # near the root of 1+g(1-sigma)
+    dy[2, :4] = [0.0, -0.0, 1e30, 1e-30]
+    h13 = np.concatenate([o.round_to_bf16_bits(g), o.round_to_bf16_bits(u)], axis=1)
+    dyb = o.round_to_bf16_bits(dy)
+    res = mx.swiglu_quant_bwd(to_dev(dyb), to_dev(h13), mx.ROW, mx.SCALE_LINEAR, bf16_transposed=True)
+    torch.cuda.synchronize()
+    dh13, y = _bwd_ref(dyb, h13)
+    got = bits(res["dh13_t"]).T
+    vnan = np.isnan(o.bf16_to_f64(dh13))
+    assert np.array_equal(np.isnan(o.bf16_to_f64(got)), vnan)
+    assert np.array_equal(got[~vnan], dh13[~vnan])
