@@ -1,0 +1,466 @@
+"""Throughput of the MXFP8 SwiGLU MLP (fwd + bwd) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one forward + backward of the whole MLP (quantize x and the
+weights, w13 GEMM, fused SwiGLU + dual quantization, w2 GEMM; then the
+backward GEMMs, fused SwiGLU backward and both weight gradients) through
+the C ABI, inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+Workloads (seeded synthetic data, shapes of the pages' MXFP8 fused-MLP
+workloads): llama3_8b_ffn (default: dense, M=8192, d=4096, h=14336,
+wgrad_with_hp recipe), moe_16e, moe_64e (grouped, default recipe).
+
+Reported beside the device-timed value:
+  e2e           the same step through the public API with host buffers:
+                x and dout copied in from pinned memory, out and dx copied
+                back, every step.
+  roofline      the dominant kernel (the MXFP8 tcgen05 GEMM): algorithmic
+                FLOPs of its launches / their CUDA-event durations, measured
+                in a per-kernel pass of the same step (the same kernels
+                launched one by one with events between them).
+  cpu_baseline  the CPU oracle on a bounded sample of the workload.
+  --impl reference runs that oracle sample as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+MXFP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = dict(FALLBACK_PEAKS)
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                if k in d and d[k]:
+                    out[k] = float(d[k])
+            out["source"] = "measured"
+            return out
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS)
+
+
+# ------------------------------------------------------------------ workload
+
+
+def make_workload(name):
+    w = dict(synth.WORKLOADS[name])
+    if w["kind"] == "dense":
+        inp = synth.dense_mlp_inputs(w["M"], w["d"], w["h"], w["seed"])
+        inp["offs"] = None
+        w["tokens"] = w["M"]
+        w["M_total"] = w["M"]
+    else:
+        if w["counts"] == "zipf":
+            counts = synth.zipf_group_counts(w["E"], w["tokens"], w["s"], w["seed"], w["n_empty"])
+        else:
+            counts = synth.dirichlet_group_counts(w["E"], w["tokens"], w["alpha"], w["seed"], w["n_empty"])
+        inp = synth.grouped_mlp_inputs(counts, w["d"], w["h"], w["seed"])
+        w["M_total"] = int(inp["offs"][-1])
+    w.setdefault("recipe", "rceil")
+    w["flops"] = 18.0 * w["tokens"] * w["d"] * w["h"]   # real routed rows, padding excluded
+    return w, inp
+
+
+def to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx_, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx_.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx_) if mx_ else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def run_gpu(args, rank, world, dev):
+    import block_scaled_mlp_gb300 as mx
+
+    w, inp = make_workload(args.workload)
+    recipe = mx.RECIPE_RCEIL_WGRAD_HP if w["recipe"] == "wgrad_hp" else mx.RECIPE_RCEIL
+    t = {k: to_dev(inp[k], dev) for k in ("x", "w1", "w3", "w2", "dout")}
+    offs = None if inp["offs"] is None else torch.from_numpy(inp["offs"]).to(dev)
+    M, d, h = w["M_total"], w["d"], w["h"]
+    E = 0 if offs is None else offs.numel()
+    cb, sb = mx.mlp_workspace_size(M, d, h, E, recipe)
+    ctx = torch.empty(cb, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(sb, dtype=torch.uint8, device=dev)
+    out = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    grads = (torch.empty((M, d), dtype=torch.bfloat16, device=dev), torch.empty_like(t["w1"]),
+             torch.empty_like(t["w3"]), torch.empty_like(t["w2"]))
+    err = mx.ErrorWord(dev)
+    stream = torch.cuda.current_stream(dev)
+    L = mx.lib()
+    P = mx._ptr
+
+    def step(x, dout):
+        rc = L.mx_mlp_fwd(P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1), 128, recipe,
+                          P(ctx), P(scratch), P(out), err.ptr(), mx._stream())
+        mx._check(rc)
+        rc = L.mx_mlp_bwd(P(ctx), P(dout), P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1),
+                          128, recipe, P(scratch), P(grads[0]), P(grads[1]), P(grads[2]), P(grads[3]), err.ptr(),
+                          mx._stream())
+        mx._check(rc)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warmup
+    for _ in range(args.warmup):
+        step(t["x"], t["dout"])
+    torch.cuda.synchronize(dev)
+    err.check()
+
+    # ---- device-timed region (inputs resident in HBM; working set > L2)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(t["x"], t["dout"])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    err.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = w["flops"] * world / (ms_max * 1e-3) / 1e12
+    launches_per_step = 13 if E == 0 else 13
+
+    # ---- end to end through the public API with host buffers
+    hx = t["x"].cpu().pin_memory()
+    hd = t["dout"].cpu().pin_memory()
+    ho = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
+    dx_buf, dd_buf = torch.empty_like(t["x"]), torch.empty_like(t["dout"])
+    barrier()
+    torch.cuda.synchronize(dev)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        dx_buf.copy_(hx, non_blocking=True)
+        dd_buf.copy_(hd, non_blocking=True)
+        step(dx_buf, dd_buf)
+        ho.copy_(out, non_blocking=True)
+        hdx.copy_(grads[0], non_blocking=True)
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms_e2e = a0.elapsed_time(a1) / args.steps
+    et = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(et, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = w["flops"] * world / (float(et.item()) * 1e-3) / 1e12
+    h2d = (hx.numel() + hd.numel()) * 2
+    d2h = (ho.numel() + hdx.numel()) * 2
+
+    # ---- per-kernel pass: the same kernels launched one by one with events
+    kern = kernel_breakdown(mx, w, t, offs, recipe, dev, max(1, min(args.steps, 10)))
+    peaks = load_peaks()
+    mx_peak = peaks["bf16_tflops_sustained"] * MXFP8_OVER_BF16
+    g = kern["mx_gemm"]
+    achieved = g["flops"] / (g["ms"] * 1e-3) / 1e12
+    roofline = {"kernel": "gemm_kernel<MXFP8,BN=256> (tcgen05 block-scaled)", "bound": "tensor",
+                "achieved": round(achieved, 1), "peak": round(mx_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / mx_peak, 4), "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained x {MXFP8_OVER_BF16} (nominal fp8/bf16 ratio)"}
+    mem = kern["mem"]
+    mem_gbs = mem["bytes"] / (mem["ms"] * 1e-3) / 1e9
+
+    res = {
+        "metric": "MXFP8 MLP fwd+bwd TFLOP/s",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp8-e4m3 (fp32 accumulate)" + (" + bf16 wgrad" if recipe else ""),
+        "data": "synthetic (seeded; bf16 N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": args.workload, "M_total": M, "tokens": w["tokens"], "d": d, "h": h, "E": E or None,
+                   "recipe": w["recipe"], "flops_per_step": w["flops"],
+                   "l2": f"inputs larger than L2 (weights {3 * d * h * 2 * max(E, 1) / 1e6:.0f} MB bf16)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "quant_swiglu": {"achieved_gbs": round(mem_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
+                         "frac": round(mem_gbs / peaks["hbm_gbs"], 4),
+                         "kernels": "quantize x/dout (row+col) + fused SwiGLU fwd/bwd",
+                         "peak_source": peaks["source"]},
+        "kernels_ms_per_step": {k: round(v["ms"] / kern["steps"], 4) for k, v in kern.items() if isinstance(v, dict)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    return res
+
+
+def kernel_breakdown(mx, w, t, offs, recipe, dev, steps):
+    """Per-kernel CUDA-event timing of the step's kernels, launched one by
+    one through the per-op entry points (bit-identical to the composite)."""
+    hp = recipe == mx.RECIPE_RCEIL_WGRAD_HP
+    d, h, M = w["d"], w["h"], w["M_total"]
+    grouped = offs is not None
+    W1, W3, W2 = (t[k] if grouped else t[k][None] for k in ("w1", "w3", "w2"))
+    E = W1.shape[0]
+    # weights quantized once, packed as the composite packs them (untimed)
+    w13q, w13s, w13qc, w13sc, w2q, w2s, w2qc, w2sc = ([] for _ in range(8))
+    for e in range(E):
+        a, b, c = mx.quantize(W1[e].contiguous()), mx.quantize(W3[e].contiguous()), mx.quantize(W2[e].contiguous())
+        w13q.append(torch.cat([a["q_row"], b["q_row"]]))
+        w13s.append(torch.cat([a["s_row"], b["s_row"]]))
+        w13qc.append(torch.cat([a["q_col"], b["q_col"]], 1))
+        w13sc.append(torch.cat([a["s_col"].view(d // 128, h // 128, 512), b["s_col"].view(d // 128, h // 128, 512)],
+                               1).reshape(-1))
+        w2q.append(c["q_row"]); w2s.append(c["s_row"]); w2qc.append(c["q_col"]); w2sc.append(c["s_col"])
+    pk = [torch.stack(v) if grouped else v[0] for v in (w13q, w13s, w13qc, w13sc, w2q, w2s, w2qc, w2sc)]
+    w13q, w13s, w13qc, w13sc, w2q, w2s, w2qc, w2sc = pk
+    x, dout = t["x"], t["dout"]
+    x_t = x.t().contiguous() if hp else None
+    dout_t = dout.t().contiguous() if hp else None
+    tokens = w["tokens"]
+    f = {"mx_gemm": 0.0, "bf16_gemm": 0.0}
+    acc = {"mx_gemm": [0.0, 0.0], "bf16_gemm": [0.0, 0.0], "mem": [0.0, 0.0]}
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(kind, flops_or_bytes, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        r = fn()
+        b.record(stream)
+        pending.append((kind, flops_or_bytes, a, b))
+        return r
+
+    def mm(aq, as_, bq, bs):
+        return mx.grouped_mm(mx.GROUP_M, aq, as_, bq, bs, offs) if grouped else mx.scaled_mm(aq, as_, bq, bs)
+
+    def wg(aq, as_, bq, bs):
+        return mx.grouped_mm(mx.GROUP_K, aq, as_, bq, bs, offs) if grouped else mx.scaled_mm(aq, as_, bq, bs)
+
+    mdh = 2.0 * tokens * d * h
+    for it in range(steps + 1):
+        pending = []
+        xq = timed("mem", M * d * (2 + 2 * 1.03125), lambda: mx.quantize(x, mx.BOTH))
+        h13 = timed("mx_gemm", 2 * mdh, lambda: mm(xq["q_row"], xq["s_row"], w13q, w13s))
+        y = timed("mem", M * h * (4 + (1.03125 if hp else 2.0625)),
+                  lambda: mx.swiglu_quant(h13, mx.ROW if hp else mx.BOTH))
+        timed("mx_gemm", mdh, lambda: mm(y["q_row"], y["s_row"], w2q, w2s))
+        dq = timed("mem", M * d * (2 + 2 * 1.03125), lambda: mx.quantize(dout, mx.BOTH))
+        dy = timed("mx_gemm", mdh, lambda: mm(dq["q_row"], dq["s_row"], w2qc, w2sc))
+        if hp:
+            dh = timed("mem", M * h * (6 + 2 * 1.03125 + 6), lambda: mx.swiglu_quant_bwd(dy, h13, mx.ROW,
+                                                                                       bf16_transposed=True))
+            timed("bf16_gemm", mdh, lambda: mx.bf16_wgrad(dout_t, dh["y_t"], offs))
+            timed("bf16_gemm", 2 * mdh, lambda: mx.bf16_wgrad(dh["dh13_t"], x_t, offs))
+        else:
+            dh = timed("mem", M * h * (6 + 4 * 1.03125), lambda: mx.swiglu_quant_bwd(dy, h13, mx.BOTH))
+            timed("mx_gemm", mdh, lambda: wg(dq["q_col"], dq["s_col"], y["q_col"], y["s_col"]))
+            timed("mx_gemm", 2 * mdh, lambda: wg(dh["q_col"], dh["s_col"], xq["q_col"], xq["s_col"]))
+        timed("mx_gemm", 2 * mdh, lambda: mm(dh["q_row"], dh["s_row"], w13qc, w13sc))
+        torch.cuda.synchronize(dev)
+        if it == 0:
+            continue  # warm-up pass
+        for kind, work, a, b in pending:
+            acc[kind][0] += work
+            acc[kind][1] += a.elapsed_time(b)
+    out = {"steps": steps}
+    for k, (work, ms) in acc.items():
+        if ms > 0:
+            out[k] = {"flops" if k != "mem" else "bytes": work / steps, "ms": ms / steps}
+    out["mx_gemm"]["flops"] = acc["mx_gemm"][0] / steps
+    out["mem"]["bytes"] = acc["mem"][0] / steps
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample(w, inp, tokens, hidden):
+    """A bounded sample of the workload for the CPU oracle: the first
+    `tokens` routed rows and the first `hidden` hidden units (all of d)."""
+    from oracle import mx_oracle as o
+    x = inp["x"][:tokens]
+    dout = inp["dout"][:tokens]
+    if inp["offs"] is None:
+        w1, w3, w2 = inp["w1"][:hidden], inp["w3"][:hidden], inp["w2"][:, :hidden]
+        offs = None
+    else:
+        # the sample stays inside the first non-empty group
+        first = int(np.nonzero(np.diff(np.concatenate([[0], inp["offs"]])))[0][0])
+        start = 0 if first == 0 else int(inp["offs"][first - 1])
+        x = inp["x"][start:start + tokens]
+        dout = inp["dout"][start:start + tokens]
+        w1, w3 = inp["w1"][first, :hidden], inp["w3"][first, :hidden]
+        w2 = inp["w2"][first][:, :hidden]
+        offs = None
+    rec = "wgrad_hp" if w["recipe"] == "wgrad_hp" else "rceil"
+    t0 = time.perf_counter()
+    f = o.mlp_fwd(x, w1, w3, w2, offs=offs, recipe=rec)
+    o.mlp_bwd(x, w1, w3, w2, dout, offs=offs, recipe=rec, fwd=f)
+    dt = time.perf_counter() - t0
+    flops = 18.0 * tokens * w["d"] * hidden
+    return flops, dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    w, inp = make_workload(args.workload)
+    tokens, hidden = 64, 512
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, tokens, hidden)
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(args.steps):
+        fl, dt = oracle_sample(w, inp, tokens, hidden)
+        tot_f += fl
+        tot_t += dt
+    value = tot_f / tot_t / 1e12
+    sample = f"{tokens} tokens x {hidden} hidden units (all d={w['d']}) of {args.workload}, fwd+bwd"
+    return {
+        "impl": "reference",
+        "metric": "MXFP8 MLP fwd+bwd TFLOP/s",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (exact MXFP8 oracle)",
+        "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline(args):
+    w, inp = make_workload(args.workload)
+    tokens, hidden = (256, 1024) if w["kind"] == "dense" else (256, 512)
+    fl, dt = oracle_sample(w, inp, tokens, hidden)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"{tokens} tokens x {hidden} hidden units (all d={w['d']}) of {args.workload}, fwd+bwd"}
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama3_8b_ffn", choices=sorted(k for k in synth.WORKLOADS if k != "tiny_dense"))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    res = run_gpu(args, rank, world, dev)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

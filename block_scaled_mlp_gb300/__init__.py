@@ -254,6 +254,11 @@ class MlpContext:
         self.buf = buf
         self.args = args
 
+    def h13(self):
+        """The saved w13 GEMM output [M_total, 2h] (bf16), first in the context."""
+        M, h = self.args["M"], self.args["h"]
+        return self.buf[: M * 2 * h * 2].view(torch.bfloat16).view(M, 2 * h)
+
 
 def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL, pad_multiple=128, scratch=None,
             err: ErrorWord | None = None, out=None):

@@ -56,6 +56,21 @@ MX_DEVINL uint32_t bf16_from_f64_rn(double x) {
   return sign | ((uint32_t)(ee + 127) << 7) | (uint32_t)(n - 128);
 }
 
+MX_DEVINL double bf16_bits_to_f64(uint32_t b) { return (double)__uint_as_float(b << 16); }
+
+// The bf16 rounding midpoint nearest to x (x finite, non-zero): halfway
+// between RN_bf16(x) and its neighbour on x's side.
+MX_DEVINL double nearest_bf16_midpoint(double x) {
+  const uint32_t b = bf16_from_f64_rn(x);
+  const double v = bf16_bits_to_f64(b);
+  const uint32_t mag = b & 0x7FFFu;
+  uint32_t nmag;
+  if (fabs(x) >= fabs(v)) nmag = mag + 1;
+  else nmag = mag == 0 ? 0 : mag - 1;
+  const double w = bf16_bits_to_f64((b & 0x8000u) | nmag);
+  return 0.5 * (v + w);
+}
+
 MX_DEVINL float sigmoid_f32_slow(float g) {
   const double s = 1.0 / (1.0 + exp(-(double)g));
   return __double2float_rn(s);
@@ -96,15 +111,25 @@ MX_DEVINL uint32_t dg_bits(float dyf, float g, float u) {
   }
   const double gd = (double)g;
   const double t = exp(-gd);
-  double f;
-  if (t > 1e300) {
-    f = -0.0;  // sigma underflows: f is a tiny negative number
-  } else {
-    const double s = 1.0 / (1.0 + t);
-    const double oms = t * s;
-    f = s * (1.0 + gd * oms);
+  const double dyu64 = (double)dyf * (double)u;  // exact
+  if (t > 1e300) return bf16_from_f64_rn(dyu64 * -0.0);  // sigma underflows: f is a tiny negative
+  const double s = 1.0 / (1.0 + t);
+  const double oms = t * s;
+  double pd = dyu64 * (s * (1.0 + gd * oms));
+  // Exact ties: dy*u (16 significant bits) can sit exactly on a bf16 rounding
+  // midpoint while f is 1 (large g) or 1/2 (tiny |g|) to fp64 precision.
+  // The exact product then lies just off the midpoint on the side given by
+  // the sign of f - 1 (positive for large g) or f - 1/2 (sign of g).
+  if (pd != 0.0 && isfinite(pd)) {
+    const double m = nearest_bf16_midpoint(pd);
+    if (fabs(pd - m) <= fabs(pd) * 0x1p-40) {
+      double dir = 0.0;
+      if (m == dyu64) dir = 1.0;
+      else if (m == 0.5 * dyu64) dir = (gd > 0.0) ? 1.0 : ((gd < 0.0) ? -1.0 : 0.0);
+      if (dir != 0.0) pd = m + copysign(fabs(m) * 0x1p-20, dyu64 * dir);
+      else if (m == 0.5 * dyu64) pd = m;  // g == 0: an exact tie, ties to even
+    }
   }
-  const double pd = ((double)dyf * (double)u) * f;
   return bf16_from_f64_rn(pd);
 }
 

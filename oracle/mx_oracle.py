@@ -284,10 +284,10 @@ def _mp_sigmoid(g: float):
         return 1 / (1 + mpmath.exp(-x))
 
 
-def _mp_round(x, f32: bool) -> float:
+def _mp_round(x, f32: bool, prec: int = _MP_PREC) -> float:
     """Round an mpf to the nearest float32 (f32=True) or bfloat16 value, ties
-    to even, deciding the direction in high precision."""
-    with mpmath.workprec(_MP_PREC):
+    to even, deciding the direction in `prec`-bit precision."""
+    with mpmath.workprec(prec):
         approx = float(x)
         if f32:
             c = np.float32(approx)
@@ -374,12 +374,38 @@ def swiglu_fwd(g_bits, u_bits) -> np.ndarray:
         return round_to_bf16_bits(round_to_f32(a * u))  # a*u exact in float64
 
 
-def _mp_dsilu_factor(g: float):
-    """sigma(g) * (1 + g*(1 - sigma(g))) in 240-bit precision."""
-    with mpmath.workprec(_MP_PREC):
+def _mp_dsilu_factor(g: float, prec: int = _MP_PREC):
+    """sigma(g) * (1 + g*(1 - sigma(g))) in `prec`-bit precision, with 1 - sigma
+    formed as e^-g/(1+e^-g) so that no cancellation occurs for large g."""
+    with mpmath.workprec(prec):
         x = mpmath.mpf(g)
-        s = 1 / (1 + mpmath.exp(-x))
-        return s * (1 + x * (1 - s))
+        t = mpmath.exp(-x)
+        s = 1 / (1 + t)
+        oms = t / (1 + t)
+        return s * (1 + x * oms)
+
+
+def _dg_exact_bf16(dyu: float, g: float) -> int:
+    """RN_bf16 of the exact dyu * f(g) (dyu = dy*u, an exact float64) for the
+    few products the float64 evaluation cannot round with certainty.
+
+    f(g) - 1 ~ g*e^-g for large g and f(g) - 1/2 ~ g/2 for tiny g, so the
+    working precision grows with |g| until the exact value is resolved; for
+    g > 1000 the deviation of f from 1 is below 2^-1400 and only decides
+    exact ties of dyu, always away from zero (f > 1 for g > 1.28)."""
+    if g > 1000.0:
+        b = int(round_to_bf16_bits(dyu))
+        lo = float(bf16_to_f64(_bf16_step(np.uint16(b), -1)))
+        hi = float(bf16_to_f64(_bf16_step(np.uint16(b), +1)))
+        v = float(bf16_to_f64(np.uint16(b)))
+        for w in (lo, hi):
+            if dyu == (v + w) / 2:           # exact tie of dyu: f > 1 breaks it
+                return int(round_to_bf16_bits(max(v, w, key=abs)))
+        return b
+    prec = _MP_PREC + 160 + int(2 * max(0.0, 1.45 * g))
+    with mpmath.workprec(prec):
+        exact = mpmath.mpf(dyu) * _mp_dsilu_factor(g, prec)
+        return int(round_to_bf16_bits(_mp_round(exact, f32=False, prec=prec)))
 
 
 def _dsilu_factor_f64(g):
@@ -431,9 +457,7 @@ def swiglu_bwd(dy_bits, g_bits, u_bits):
                           np.abs(p - (c + bf16_to_f64(hi_b)) / 2))
         amb = np.isfinite(p) & (p != 0) & (dist <= np.abs(p) * (rel + 2.0 ** -50))
     for i in zip(*np.nonzero(amb)):
-        with mpmath.workprec(_MP_PREC):
-            exact = mpmath.mpf(float(dyu[i])) * _mp_dsilu_factor(float(g[i]))
-        dg_bits[i] = round_to_bf16_bits(_mp_round(exact, f32=False))
+        dg_bits[i] = _dg_exact_bf16(float(dyu[i]), float(g[i]))
     dg_bits[~np.isfinite(g)] = 0x7FC0
     return dg_bits, du_bits
 
