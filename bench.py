@@ -261,7 +261,7 @@ def run_gpu(args, rank, world, dev):
                          "frac": round(mem_gbs / peaks["hbm_gbs"], 4),
                          "kernels": "quantize x/dout (row+col) + fused SwiGLU fwd/bwd",
                          "peak_source": peaks["source"]},
-        "kernels_ms_per_step": {k: round(v["ms"] / kern["steps"], 4) for k, v in kern.items() if isinstance(v, dict)},
+        "kernels_ms_per_step": {k: round(v["ms"], 4) for k, v in kern.items() if isinstance(v, dict)},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -426,6 +426,67 @@ def cpu_baseline(args):
             "sample": f"{tokens} tokens x {hidden} hidden units (all d={w['d']}) of {args.workload}, fwd+bwd"}
 
 
+# ------------------------------------------------------------------ profiling cases
+
+
+def run_profile_case(args):
+    """One kernel on a small case (a few hundred MB on the device, larger
+    than L2), launched --iters times: the command the committed ncu
+    summaries were captured with."""
+    import block_scaled_mlp_gb300 as mx
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    c = args.profile_case
+    M = 8192
+
+    def rnd(*shape, std=1.0):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    if c == "quant":
+        x = rnd(M, 8192)
+        fn = lambda: mx.quantize(x, mx.BOTH)
+        work, unit = M * 8192 * (2 + 2 * 1.03125), "B"
+    elif c in ("swiglu_fwd", "swiglu_fwd_row"):
+        h13 = rnd(M, 2 * 8192, std=1.3)
+        ax = mx.ROW if c.endswith("row") else mx.BOTH
+        fn = lambda: mx.swiglu_quant(h13, ax)
+        work, unit = M * 8192 * (4 + (1.03125 if ax == mx.ROW else 2.0625)), "B"
+    elif c in ("swiglu_bwd", "swiglu_bwd_hp"):
+        h13, dy = rnd(M, 2 * 8192, std=1.3), rnd(M, 8192)
+        if c == "swiglu_bwd":
+            fn = lambda: mx.swiglu_quant_bwd(dy, h13, mx.BOTH)
+            work = M * 8192 * (6 + 4 * 1.03125)
+        else:
+            fn = lambda: mx.swiglu_quant_bwd(dy, h13, mx.ROW, bf16_transposed=True)
+            work = M * 8192 * (6 + 2 * 1.03125 + 6)
+        unit = "B"
+    elif c in ("gemm_mx", "gemm_bf16"):
+        N, K = 8192, 4096
+        if c == "gemm_mx":
+            a, b = mx.quantize(rnd(M, K), mx.ROW), mx.quantize(rnd(N, K, std=0.02), mx.ROW)
+            fn = lambda: mx.scaled_mm(a["q_row"], a["s_row"], b["q_row"], b["s_row"])
+        else:
+            at, bt = rnd(N, M), rnd(K, M, std=0.02)   # bf16 wgrad: [N, tokens] x [K, tokens]
+            fn = lambda: mx.bf16_wgrad(at, bt)
+        work, unit = 2.0 * M * N * K, "FLOP"
+    else:
+        raise SystemExit(f"unknown case {c}")
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.iters
+    rate = work / (ms * 1e-3) / (1e9 if unit == "B" else 1e12)
+    print(json.dumps({"case": c, "ms": round(ms, 4), "rate": round(rate, 1),
+                      "unit": "GB/s" if unit == "B" else "TFLOP/s"}))
+
+
 # ------------------------------------------------------------------ main
 
 
@@ -437,7 +498,14 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_ffn", choices=sorted(k for k in synth.WORKLOADS if k != "tiny_dense"))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None,
+                    choices=["quant", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd", "swiglu_bwd_hp", "gemm_mx",
+                             "gemm_bf16"])
+    ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
 
     rank = int(os.environ.get("RANK", "0"))

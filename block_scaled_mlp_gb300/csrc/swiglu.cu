@@ -31,6 +31,21 @@ namespace mx {
 namespace {
 
 // ------------------------------------------------------------------ numerics
+//
+// Three tiers, all giving the exactly defined result:
+//   1. fp32 fast path: t = expf(-g) (at most 2 ulp), s = rcp.approx(1 + t)
+//      (at most 1 ulp); the bf16 result is kept when it lies farther from a
+//      bf16 rounding midpoint than the error bound of the fp32 chain.
+//   2. float-float (pairs of fp32 carrying ~46 bits) for the few elements
+//      near a midpoint: an own exp (Cody-Waite reduction by ln 2 split in
+//      three parts, then the Taylor series of e^r, |r| <= ln2/2, evaluated
+//      by Horner's rule with double-float arithmetic in the style of Dekker
+//      1971 / Knuth TAOCP 4.2.2 error-free transforms) and a Newton-corrected
+//      reciprocal.  Runs on the fp32 pipe.
+//   3. fp64 for |g| > 64, for extreme magnitudes of dy*u and for the
+//      float-float results that are still within their error of a midpoint.
+
+MX_DEVINL double bf16_bits_to_f64(uint32_t b) { return (double)__uint_as_float(b << 16); }
 
 // RN to bf16 from an fp64 value (ties to even, subnormals, overflow to Inf).
 MX_DEVINL uint32_t bf16_from_f64_rn(double x) {
@@ -56,8 +71,6 @@ MX_DEVINL uint32_t bf16_from_f64_rn(double x) {
   return sign | ((uint32_t)(ee + 127) << 7) | (uint32_t)(n - 128);
 }
 
-MX_DEVINL double bf16_bits_to_f64(uint32_t b) { return (double)__uint_as_float(b << 16); }
-
 // The bf16 rounding midpoint nearest to x (x finite, non-zero): halfway
 // between RN_bf16(x) and its neighbour on x's side.
 MX_DEVINL double nearest_bf16_midpoint(double x) {
@@ -71,44 +84,143 @@ MX_DEVINL double nearest_bf16_midpoint(double x) {
   return 0.5 * (v + w);
 }
 
-MX_DEVINL float sigmoid_f32_slow(float g) {
+// |low 16 bits of p - 0x8000| > margin: p's bf16 rounding is decided with
+// room to spare (the bf16 midpoints are the fp32 values whose low half is
+// exactly 0x8000).
+MX_DEVINL bool clear_of_midpoint(float p, uint32_t margin) {
+  const uint32_t low = __float_as_uint(p) & 0xFFFFu;
+  return (low - (0x8000u - margin)) > 2u * margin;
+}
+
+MX_DEVINL float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// ---- float-float
+struct ff {
+  float hi, lo;
+};
+MX_DEVINL ff fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+MX_DEVINL ff two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+MX_DEVINL ff ff_add(ff x, ff y) {
+  ff s = two_sum(x.hi, y.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+MX_DEVINL ff ff_add_f(ff x, float b) {
+  ff s = two_sum(x.hi, b);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, x.lo));
+}
+MX_DEVINL ff ff_mul(ff x, ff y) {
+  const float p = __fmul_rn(x.hi, y.hi);
+  float e = __fmaf_rn(x.hi, y.hi, -p);
+  e = __fmaf_rn(x.hi, y.lo, e);
+  e = __fmaf_rn(x.lo, y.hi, e);
+  return fast_two_sum(p, e);
+}
+MX_DEVINL ff ff_mul_f(ff x, float b) {
+  const float p = __fmul_rn(x.hi, b);
+  float e = __fmaf_rn(x.hi, b, -p);
+  e = __fmaf_rn(x.lo, b, e);
+  return fast_two_sum(p, e);
+}
+MX_DEVINL ff ff_rcp(ff x) {  // one Newton step on a correctly rounded quotient
+  const float q = __fdiv_rn(1.0f, x.hi);
+  float e = __fmaf_rn(-x.hi, q, 1.0f);
+  e = __fmaf_rn(-x.lo, q, e);
+  return fast_two_sum(q, __fmul_rn(q, e));
+}
+
+// e^x as float-float for |x| <= 64 (relative error well below 2^-44).
+MX_DEVINL ff ff_exp(float x) {
+  // ln 2 = L1 + L2 + L3, L1 with 15 significant bits so that n*L1 is exact
+  constexpr float L1 = 0x1.62e4p-1f, L2 = 0x1.7f7d1cp-20f, L3 = 0x1.ef357ap-45f;
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  ff r = two_sum(x, -__fmul_rn(n, L1));  // exact
+  const float p2 = __fmul_rn(n, L2);
+  r = ff_add(r, ff{-p2, -__fmaf_rn(n, L2, -p2)});
+  r = ff_add_f(r, -__fmul_rn(n, L3));
+  // Taylor coefficients 1/k! (k = 7..11 in fp32, k = 0..6 as float-float)
+  float tail = 0x1.ae6456p-26f;
+  tail = __fmaf_rn(tail, r.hi, 0x1.27e4fcp-22f);
+  tail = __fmaf_rn(tail, r.hi, 0x1.71de3ap-19f);
+  tail = __fmaf_rn(tail, r.hi, 0x1.a01a02p-16f);
+  tail = __fmaf_rn(tail, r.hi, 0x1.a01a02p-13f);
+  const ff c[7] = {{1.0f, 0.0f},
+                   {1.0f, 0.0f},
+                   {0.5f, 0.0f},
+                   {0x1.555556p-3f, -0x1.555556p-28f},
+                   {0x1.555556p-5f, -0x1.555556p-30f},
+                   {0x1.111112p-7f, -0x1.dddddep-32f},
+                   {0x1.6c16c2p-10f, -0x1.27d27ep-35f}};
+  ff acc{tail, 0.0f};
+#pragma unroll
+  for (int k = 6; k >= 0; --k) acc = ff_add(ff_mul(acc, r), c[k]);
+  const float two_n = __uint_as_float((uint32_t)((int)n + 127) << 23);
+  return {__fmul_rn(acc.hi, two_n), __fmul_rn(acc.lo, two_n)};
+}
+
+// fp32 ulp of a positive normal float
+MX_DEVINL float ulp_of(float x) { return __uint_as_float(__float_as_uint(x) & 0x7F800000u) * 0x1p-23f; }
+
+MX_DEVINL float sigmoid_f32_fp64(float g) {
   const double s = 1.0 / (1.0 + exp(-(double)g));
   return __double2float_rn(s);
 }
 
-// bf16 SiLU a(g) as bit pattern.
-MX_DEVINL uint32_t silu_bits(float g) {
-  float p = 0.f;
-  bool slow = !(fabsf(g) <= 64.0f);
-  if (!slow) {
-    const float t = expf(-g);
-    const float s = __frcp_rn(__fadd_rn(1.0f, t));
-    p = __fmul_rn(g, s);
-    const int low = (int)(__float_as_uint(p) & 0xFFFFu);
-    slow = (abs(low - 0x8000) <= 64) || (fabsf(p) < 1e-30f);
-  }
-  if (slow) p = __fmul_rn(g, sigmoid_f32_slow(g));
-  return f32_to_bf16_bits(p);
+// Correctly rounded fp32 sigma for |g| <= 64 via float-float; falls back to
+// fp64 if the float-float value is within its error of an fp32 midpoint.
+MX_DEVINL float sigmoid_f32_ff(float g, ff* t_out, ff* s_out) {
+  const ff t = ff_exp(-g);
+  const ff s = ff_rcp(ff_add_f(t, 1.0f));
+  *t_out = t;
+  *s_out = s;
+  const float half_ulp = 0.5f * ulp_of(s.hi);
+  if (fabsf(fabsf(s.lo) - half_ulp) <= s.hi * 0x1p-40f) return sigmoid_f32_fp64(g);
+  return s.hi;
 }
 
-MX_DEVINL uint32_t dg_bits(float dyf, float g, float u) {
-  if (!isfinite(g)) return 0x7FC0u;
-  const float dyu = __fmul_rn(dyf, u);  // exact when in the normal range
-  const float adyu = fabsf(dyu);
-  if (fabsf(g) <= 64.0f && adyu >= 1e-30f && adyu <= 1e30f) {
-    const float t = expf(-g);
-    const float s = __frcp_rn(__fadd_rn(1.0f, t));
-    const float oms = __fmul_rn(t, s);
-    const float go = __fmul_rn(g, oms);
-    const float inner = __fadd_rn(1.0f, go);
-    const float f = __fmul_rn(s, inner);
-    const float p = __fmul_rn(dyu, f);
-    const float ratio = fabsf(go) / fabsf(inner);
-    const int low = (int)(__float_as_uint(p) & 0xFFFFu);
-    const float dist = (float)abs(low - 0x8000);
-    if (dist > 32.0f + 32.0f * ratio && fabsf(p) >= 1e-30f && fabsf(p) <= 1e30f)
-      return f32_to_bf16_bits(p);
+// bf16 SiLU from a correctly rounded fp32 sigma
+MX_DEVINL uint32_t silu_from_sigma(float g, float sig) { return f32_to_bf16_bits(__fmul_rn(g, sig)); }
+
+// Result of the shared fast path for one element.
+struct SigFast {
+  float t, s;   // expf(-g), approx 1/(1+t)
+  bool ok;      // |g| <= 64 (fast path usable at all)
+};
+MX_DEVINL SigFast sig_fast(float g) {
+  SigFast r;
+  r.ok = fabsf(g) <= 64.0f;  // false for NaN / Inf too
+  r.t = expf(-g);
+  r.s = rcp_approx(__fadd_rn(1.0f, r.t));
+  return r;
+}
+
+// a(g): RN_bf16(RN_f32(g * sigma_c)).  Fast-path error of g*s against
+// g*sigma_c is at most 9 fp32 ulps; 16 leaves room.
+MX_DEVINL uint32_t silu_bits_from(float g, const SigFast& f) {
+  if (f.ok) {
+    const float p = __fmul_rn(g, f.s);
+    if (clear_of_midpoint(p, 16)) return f32_to_bf16_bits(p);
+    ff t, s;
+    return silu_from_sigma(g, sigmoid_f32_ff(g, &t, &s));
   }
+  return silu_from_sigma(g, sigmoid_f32_fp64(g));
+}
+
+MX_DEVINL uint32_t silu_bits(float g) { return silu_bits_from(g, sig_fast(g)); }
+
+// dg by fp64 with exact-tie handling (see the comment inside).
+MX_DEVINL uint32_t dg_bits_fp64(float dyf, float g, float u) {
   const double gd = (double)g;
   const double t = exp(-gd);
   const double dyu64 = (double)dyf * (double)u;  // exact
@@ -131,6 +243,41 @@ MX_DEVINL uint32_t dg_bits(float dyf, float g, float u) {
     }
   }
   return bf16_from_f64_rn(pd);
+}
+
+// dg = RN_bf16(dy * u * sigma * (1 + g (1 - sigma))), one rounding.
+MX_DEVINL uint32_t dg_bits_from(float dyf, float g, float u, const SigFast& f) {
+  if (!isfinite(g)) return 0x7FC0u;
+  const float dyu = __fmul_rn(dyf, u);  // exact in the normal range
+  const float adyu = fabsf(dyu);
+  if (f.ok && adyu >= 0x1p-100f && adyu <= 0x1p100f) {
+    // tier 1: relative error of p <= (10 + 12 * ratio) * 2^-24
+    const float oms = __fmul_rn(f.t, f.s);
+    const float go = __fmul_rn(g, oms);
+    const float inner = __fadd_rn(1.0f, go);
+    const float p = __fmul_rn(dyu, __fmul_rn(f.s, inner));
+    const float ratio = fabsf(go) * rcp_approx(fabsf(inner));
+    const float margin = 24.0f + 26.0f * ratio;
+    if (margin < 16384.0f && clear_of_midpoint(p, (uint32_t)margin) && fabsf(p) >= 0x1p-100f)
+      return f32_to_bf16_bits(p);
+    // tier 2: float-float
+    const ff t = ff_exp(-g);
+    const ff s = ff_rcp(ff_add_f(t, 1.0f));
+    const ff omsf = ff_mul(t, s);
+    const ff gof = ff_mul_f(omsf, g);
+    const ff in = ff_add_f(gof, 1.0f);
+    const ff pf = ff_mul_f(ff_mul(s, in), dyu);
+    const float rat2 = fabsf(gof.hi) / fabsf(in.hi);
+    const uint32_t low = __float_as_uint(pf.hi) & 0xFFFFu;
+    if (low != 0x8000u) return f32_to_bf16_bits(pf.hi);
+    if (fabsf(pf.lo) > fabsf(pf.hi) * 0x1p-40f * (1.0f + rat2)) {
+      // pf.hi is a bf16 midpoint; the exact value lies on pf.lo's side
+      const uint32_t b = __float_as_uint(pf.hi);
+      const bool up = (pf.lo > 0.0f) == (pf.hi > 0.0f);  // away from zero
+      return ((up ? (b + 0x8000u) : (b - 0x8000u)) >> 16) & 0xFFFFu;
+    }
+  }
+  return dg_bits_fp64(dyf, g, u);
 }
 
 // ------------------------------------------------------------------ forward
@@ -346,9 +493,10 @@ __global__ void __launch_bounds__(SB_THREADS, 2)
           const float dyf = hh ? bf16_hi(dp[i]) : bf16_lo(dp[i]);
           const float g = hh ? bf16_hi(gp[i]) : bf16_lo(gp[i]);
           const float u = hh ? bf16_hi(up[i]) : bf16_lo(up[i]);
-          const float a = bf16_lo(silu_bits(g));
+          const SigFast sf = sig_fast(g);
+          const float a = bf16_lo(silu_bits_from(g, sf));
           const uint32_t du = f32_to_bf16_bits(__fmul_rn(dyf, a));
-          const uint32_t dg = dg_bits(dyf, g, u);
+          const uint32_t dg = dg_bits_from(dyf, g, u, sf);
           dgw |= dg << (16 * hh);
           duw |= du << (16 * hh);
           if (MODE == 2) yw |= f32_to_bf16_bits(__fmul_rn(a, u)) << (16 * hh);
