@@ -134,18 +134,15 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           uint8_t* qcol = p.q_col + b * p.qc_bs;
           ScaleDst sd = p.s_col;
           sd.base += b * p.sc_bs;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t col[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) col[i] = half ? (v[i] >> 16) : (v[i] & 0xFFFFu);
-            uint32_t codes[8];
-            const uint32_t s = quant_col32(col, codes);
-            uint8_t* dst = qcol + (cg + half) * p.qc_ld + p.qc_off + rg;
-            store16(dst, codes[0], codes[1], codes[2], codes[3]);
-            store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
-            sd.put(cg + half, p.sc_off + (rg >> 5), s);
-          }
+          uint32_t ca[8], cb[8], sa, sb;
+          quant_col32x2(v, ca, cb, sa, sb);
+          uint8_t* dst = qcol + cg * p.qc_ld + p.qc_off + rg;
+          store16(dst, ca[0], ca[1], ca[2], ca[3]);
+          store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
+          store16(dst + p.qc_ld, cb[0], cb[1], cb[2], cb[3]);
+          store16(dst + p.qc_ld + 16, cb[4], cb[5], cb[6], cb[7]);
+          sd.put(cg, p.sc_off + (rg >> 5), sa);
+          sd.put(cg + 1, p.sc_off + (rg >> 5), sb);
         } else {
           uint16_t* tcol = p.t_col + b * p.tc_bs;
 #pragma unroll

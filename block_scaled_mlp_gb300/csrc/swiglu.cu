@@ -172,7 +172,7 @@ MX_DEVINL ff ff_exp(float x) {
 // fp32 ulp of a positive normal float
 MX_DEVINL float ulp_of(float x) { return __uint_as_float(__float_as_uint(x) & 0x7F800000u) * 0x1p-23f; }
 
-MX_DEVINL float sigmoid_f32_fp64(float g) {
+__device__ __noinline__ float sigmoid_f32_fp64(float g) {
   const double s = 1.0 / (1.0 + exp(-(double)g));
   return __double2float_rn(s);
 }
@@ -205,22 +205,29 @@ MX_DEVINL SigFast sig_fast(float g) {
   return r;
 }
 
-// a(g): RN_bf16(RN_f32(g * sigma_c)).  Fast-path error of g*s against
-// g*sigma_c is at most 9 fp32 ulps; 16 leaves room.
-MX_DEVINL uint32_t silu_bits_from(float g, const SigFast& f) {
-  if (f.ok) {
-    const float p = __fmul_rn(g, f.s);
-    if (clear_of_midpoint(p, 16)) return f32_to_bf16_bits(p);
+// Tiers 2 and 3 of a(g), kept out of line: they run for well under 0.1%
+// of the elements and would otherwise bloat every unrolled copy of the fast
+// path (instruction-cache misses).
+__device__ __noinline__ uint32_t silu_bits_slow(float g) {
+  if (fabsf(g) <= 64.0f) {
     ff t, s;
     return silu_from_sigma(g, sigmoid_f32_ff(g, &t, &s));
   }
   return silu_from_sigma(g, sigmoid_f32_fp64(g));
 }
 
+// a(g): RN_bf16(RN_f32(g * sigma_c)).  Fast-path error of g*s against
+// g*sigma_c is at most 9 fp32 ulps; 16 leaves room.
+MX_DEVINL uint32_t silu_bits_from(float g, const SigFast& f) {
+  const float p = __fmul_rn(g, f.s);
+  if (f.ok && clear_of_midpoint(p, 16)) return f32_to_bf16_bits(p);
+  return silu_bits_slow(g);
+}
+
 MX_DEVINL uint32_t silu_bits(float g) { return silu_bits_from(g, sig_fast(g)); }
 
 // dg by fp64 with exact-tie handling (see the comment inside).
-MX_DEVINL uint32_t dg_bits_fp64(float dyf, float g, float u) {
+__device__ __noinline__ uint32_t dg_bits_fp64(float dyf, float g, float u) {
   const double gd = (double)g;
   const double t = exp(-gd);
   const double dyu64 = (double)dyf * (double)u;  // exact
@@ -245,21 +252,12 @@ MX_DEVINL uint32_t dg_bits_fp64(float dyf, float g, float u) {
   return bf16_from_f64_rn(pd);
 }
 
-// dg = RN_bf16(dy * u * sigma * (1 + g (1 - sigma))), one rounding.
-MX_DEVINL uint32_t dg_bits_from(float dyf, float g, float u, const SigFast& f) {
+// Tiers 2 and 3 of dg (out of line, see silu_bits_slow).
+__device__ __noinline__ uint32_t dg_bits_slow(float dyf, float g, float u) {
   if (!isfinite(g)) return 0x7FC0u;
   const float dyu = __fmul_rn(dyf, u);  // exact in the normal range
   const float adyu = fabsf(dyu);
-  if (f.ok && adyu >= 0x1p-100f && adyu <= 0x1p100f) {
-    // tier 1: relative error of p <= (10 + 12 * ratio) * 2^-24
-    const float oms = __fmul_rn(f.t, f.s);
-    const float go = __fmul_rn(g, oms);
-    const float inner = __fadd_rn(1.0f, go);
-    const float p = __fmul_rn(dyu, __fmul_rn(f.s, inner));
-    const float ratio = fabsf(go) * rcp_approx(fabsf(inner));
-    const float margin = 24.0f + 26.0f * ratio;
-    if (margin < 16384.0f && clear_of_midpoint(p, (uint32_t)margin) && fabsf(p) >= 0x1p-100f)
-      return f32_to_bf16_bits(p);
+  if (fabsf(g) <= 64.0f && adyu >= 0x1p-100f && adyu <= 0x1p100f) {
     // tier 2: float-float
     const ff t = ff_exp(-g);
     const ff s = ff_rcp(ff_add_f(t, 1.0f));
@@ -269,8 +267,8 @@ MX_DEVINL uint32_t dg_bits_from(float dyf, float g, float u, const SigFast& f) {
     const ff pf = ff_mul_f(ff_mul(s, in), dyu);
     const float rat2 = fabsf(gof.hi) / fabsf(in.hi);
     const uint32_t low = __float_as_uint(pf.hi) & 0xFFFFu;
-    if (low != 0x8000u) return f32_to_bf16_bits(pf.hi);
-    if (fabsf(pf.lo) > fabsf(pf.hi) * 0x1p-40f * (1.0f + rat2)) {
+    if (low != 0x8000u && fabsf(pf.hi) >= 0x1p-100f) return f32_to_bf16_bits(pf.hi);
+    if (low == 0x8000u && fabsf(pf.lo) > fabsf(pf.hi) * 0x1p-40f * (1.0f + rat2)) {
       // pf.hi is a bf16 midpoint; the exact value lies on pf.lo's side
       const uint32_t b = __float_as_uint(pf.hi);
       const bool up = (pf.lo > 0.0f) == (pf.hi > 0.0f);  // away from zero
@@ -280,16 +278,52 @@ MX_DEVINL uint32_t dg_bits_from(float dyf, float g, float u, const SigFast& f) {
   return dg_bits_fp64(dyf, g, u);
 }
 
-// ------------------------------------------------------------------ forward
+// dg = RN_bf16(dy * u * sigma * (1 + g (1 - sigma))), one rounding.
+// Tier 1 relative error of p <= (10 + 12 * ratio) * 2^-24.
+MX_DEVINL uint32_t dg_bits_from(float dyf, float g, float u, const SigFast& f) {
+  const float dyu = __fmul_rn(dyf, u);  // exact in the normal range
+  const float oms = __fmul_rn(f.t, f.s);
+  const float go = __fmul_rn(g, oms);
+  const float inner = __fadd_rn(1.0f, go);
+  const float p = __fmul_rn(dyu, __fmul_rn(f.s, inner));
+  const float ratio = fabsf(go) * rcp_approx(fabsf(inner));
+  const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
+  const float ap = fabsf(p), adyu = fabsf(dyu);
+  if (f.ok && margin < 16384.0f && adyu >= 0x1p-100f && adyu <= 0x1p100f && ap >= 0x1p-100f &&
+      clear_of_midpoint(p, (uint32_t)margin))
+    return f32_to_bf16_bits(p);
+  return dg_bits_slow(dyf, g, u);
+}
 
-constexpr int SF_R = 128;            // tile rows
-constexpr int SF_C = 64;             // tile y-columns
+// ------------------------------------------------------------------ kernels
+//
+// Both kernels stream tiles through a 2-stage TMA ring (one producer warp,
+// eight consumer warps, two CTAs per SM) and work on each tile in three
+// phases separated by named barriers:
+//   A  every element through the fp32 fast path; results (bf16) into a
+//      shared-memory tile; elements whose rounding the fast path cannot
+//      certify are queued (their tile index) in shared memory
+//   B  the queued elements, spread over all consumer threads, recomputed by
+//      the exact tiers and patched into the tile
+//   C  warps 0-3 quantize columns (two adjacent columns per thread), warps
+//      4-7 quantize rows, both reading the tile
+// The result tiles are double-buffered, so phase C of one tile overlaps
+// phase A of the next without a third barrier.  The queue counter is
+// double-buffered by tile parity for the same reason.
+
+constexpr int CW = 8;                    // consumer warps
+constexpr int CT = CW * 32;              // consumer threads
+constexpr int THREADS = CT + 32;
+
+MX_DEVINL void bar_consumers() { named_bar_sync(1, CT); }
+
+// ---- forward: tile = 128 rows x 64 y-columns
+constexpr int SF_R = 128, SF_C = 64;
 constexpr int SF_STAGES = 2;
-constexpr int SF_BOX = SF_R * SF_C * 2;  // 16 KB
-constexpr int SF_STAGE_BYTES = 2 * SF_BOX;
-constexpr int SF_CW = 8;
-constexpr int SF_THREADS = (SF_CW + 1) * 32;
-constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + 1024 + 64;
+constexpr int SF_BOX = SF_R * SF_C * 2;       // 16 KB
+constexpr int SF_STAGE_BYTES = 2 * SF_BOX;    // g, u
+constexpr int SF_Q = SF_R * SF_C;             // queue capacity (whole tile)
+constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + SF_Q * 2 + 1024 + 128;
 
 struct SwiFwdParams {
   int64_t M, h;
@@ -300,25 +334,28 @@ struct SwiFwdParams {
 };
 
 template <bool COL>
-__global__ void __launch_bounds__(SF_THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 2)
     swiglu_fwd_kernel(const __grid_constant__ CUtensorMap tmh, SwiFwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ytile = smem + SF_STAGES * SF_STAGE_BYTES;           // 2 x 16 KB
-  uint64_t* full = reinterpret_cast<uint64_t*>(ytile + 2 * SF_BOX);
+  uint8_t* ytile = smem + SF_STAGES * SF_STAGE_BYTES;            // 2 x 16 KB
+  uint16_t* queue = reinterpret_cast<uint16_t*>(ytile + 2 * SF_BOX);
+  uint64_t* full = reinterpret_cast<uint64_t*>(queue + SF_Q);
   uint64_t* empty = full + SF_STAGES;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int s_qn[2];
+  __shared__ long long s_abort;  // first tile index whose wait timed out
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
 
-  __shared__ long long s_abort;  // first tile index whose wait timed out
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], SF_CW); }
+  if (tid == 0) {
+    for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CW); }
     fence_mbar_init();
+    s_qn[0] = s_qn[1] = 0;
     s_abort = 0x7FFFFFFFFFFFFFFFll;
   }
   __syncthreads();
 
-  if (warp == SF_CW) {
+  if (warp == CW) {
     if (lane == 0) {
       prefetch_tmap(&tmh);
       int stage = 0; uint32_t phase = 0;
@@ -336,81 +373,114 @@ __global__ void __launch_bounds__(SF_THREADS, 2)
   }
 
   int stage = 0; uint32_t phase = 0; int buf = 0;
-  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+  const int seg = lane & 7;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, buf ^= 1) {
     const int64_t rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
     const int64_t r0 = rt * SF_R, c0 = ct * SF_C;
-    // On a timed-out wait the warp still takes part in this tile's named
-    // barrier (so no other warp is left waiting there), then all leave.
     const bool ok = mbar_wait(&full[stage], phase, p.err);
     if (!ok) atomicMin(&s_abort, (long long)t);
     const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
     const uint8_t* ut = gt + SF_BOX;
     uint8_t* yt = ytile + buf * SF_BOX;
-    const int seg = lane & 7;
+    int* qn = &s_qn[buf];
+    // ---- phase A
+    if (ok) {
 #pragma unroll 1
-    for (int it = 0; ok && it < SF_R / (4 * SF_CW); ++it) {
-      const int rr = it * (4 * SF_CW) + warp * 4 + (lane >> 3);
-      const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
-      const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
-      const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
-      const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-      uint32_t yp[4];
+      for (int it = 0; it < SF_R / (4 * CW); ++it) {
+        const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
+        const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
+        const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
+        const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
+        const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
+        uint32_t yp[4];
+        uint32_t slow = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a0 = bf16_lo(silu_bits(bf16_lo(gp[i])));
-        const float a1 = bf16_lo(silu_bits(bf16_hi(gp[i])));
-        const uint32_t y0 = f32_to_bf16_bits(__fmul_rn(a0, bf16_lo(up[i])));
-        const uint32_t y1 = f32_to_bf16_bits(__fmul_rn(a1, bf16_hi(up[i])));
-        yp[i] = y0 | (y1 << 16);
+        for (int i = 0; i < 4; ++i) {
+          const float g0 = bf16_lo(gp[i]), g1 = bf16_hi(gp[i]);
+          const SigFast f0 = sig_fast(g0), f1 = sig_fast(g1);
+          const float p0 = __fmul_rn(g0, f0.s), p1 = __fmul_rn(g1, f1.s);
+          slow |= (f0.ok && clear_of_midpoint(p0, 16) ? 0u : 1u) << (2 * i);
+          slow |= (f1.ok && clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
+          const __nv_bfloat162 a2 = __floats2bfloat162_rn(p0, p1);
+          const float2 af = __bfloat1622float2(a2);
+          const __nv_bfloat162 y2 = __floats2bfloat162_rn(__fmul_rn(af.x, bf16_lo(up[i])),
+                                                          __fmul_rn(af.y, bf16_hi(up[i])));
+          yp[i] = *reinterpret_cast<const uint32_t*>(&y2);
+        }
+        *reinterpret_cast<uint4*>(yt + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
+        while (slow) {
+          const int j = __ffs(slow) - 1;
+          slow &= slow - 1;
+          queue[atomicAdd(qn, 1)] = (uint16_t)(rr * SF_C + seg * 8 + j);
+        }
       }
-      uint32_t s;
-      const uint2 codes = quant_row8(yp, s);
-      const int64_t r = r0 + rr;
-      const int64_t c = c0 + seg * 8;
-      if (r < p.M) {
-        *reinterpret_cast<uint2*>(p.q_row + r * p.h + c) = codes;
-        if ((seg & 3) == 0) p.s_row.put(r, c >> 5, s);
-      }
-      if (COL) *reinterpret_cast<uint4*>(yt + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
     }
-    __syncwarp();
+    bar_consumers();
+    if (tid == 0) s_qn[buf ^ 1] = 0;
+    // ---- phase B
+    if (ok) {
+      const int n = *qn;
+      for (int i = tid; i < n; i += CT) {
+        const int idx = queue[i];
+        const int rr = idx / SF_C, cc = idx % SF_C;
+        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + rr * 128 + cc * 2));
+        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + rr * 128 + cc * 2));
+        const float a = bf16_lo(silu_bits_slow(g));
+        *reinterpret_cast<uint16_t*>(yt + rr * 128 + cc * 2) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
+      }
+    }
+    bar_consumers();
     if (ok && lane == 0) mbar_arrive(&empty[stage]);
     if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
-
-    if (COL) {
-      named_bar_sync(1, SF_CW * 32);
-      if (s_abort <= t) break;
-      const int rb = warp & 3;
-      const int col = (warp >> 2) * 32 + lane;  // 0..63
+    if (s_abort <= t) break;
+    // ---- phase C
+    if (warp >= 4 || !COL) {
+      // rows: 8 lanes per 64-column row; 4 rows per warp step
+      const int w = COL ? warp - 4 : warp;
+      const int nw = COL ? 4 : CW;
+      for (int rr = w * 4 + (lane >> 3); rr < SF_R; rr += nw * 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(yt + rr * 128 + seg * 16);
+        const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
+        uint32_t sc;
+        const uint2 codes = quant_row8(pk, sc);
+        const int64_t r = r0 + rr;
+        const int64_t c = c0 + seg * 8;
+        if (r < p.M) {
+          *reinterpret_cast<uint2*>(p.q_row + r * p.h + c) = codes;
+          if ((seg & 3) == 0) p.s_row.put(r, c >> 5, sc);
+        }
+      }
+    } else {
+      // columns: 32 column pairs x 4 row blocks = 128 items on warps 0-3
+      const int item = warp * 32 + lane;
+      const int pc = item & 31, rb = item >> 5;
       uint32_t v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint16_t*>(yt + (rb * 32 + i) * 128 + col * 2);
-      uint32_t codes[8];
-      const uint32_t s = quant_col32(v, codes);
+      for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(yt + (rb * 32 + i) * 128 + pc * 4);
+      uint32_t ca[8], cb[8], sa, sb;
+      quant_col32x2(v, ca, cb, sa, sb);
       const int64_t rg = r0 + rb * 32;
       if (rg < p.M) {
-        uint8_t* dst = p.q_col + (c0 + col) * p.M + rg;
-        store16(dst, codes[0], codes[1], codes[2], codes[3]);
-        store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
-        p.s_col.put(c0 + col, rg >> 5, s);
+        const int64_t col = c0 + 2 * pc;
+        uint8_t* dst = p.q_col + col * p.M + rg;
+        store16(dst, ca[0], ca[1], ca[2], ca[3]);
+        store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
+        store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
+        store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
+        p.s_col.put(col, rg >> 5, sa);
+        p.s_col.put(col + 1, rg >> 5, sb);
       }
-      buf ^= 1;
-    } else if (!ok) {
-      break;
     }
   }
 }
 
-// ------------------------------------------------------------------ backward
-
-constexpr int SB_R = 64;
-constexpr int SB_C = 64;
+// ---- backward: tile = 64 rows x 64 y-columns
+constexpr int SB_R = 64, SB_C = 64;
 constexpr int SB_STAGES = 2;
-constexpr int SB_BOX = SB_R * SB_C * 2;      // 8 KB
-constexpr int SB_STAGE_BYTES = 3 * SB_BOX;   // dy, g, u
-constexpr int SB_CW = 8;
-constexpr int SB_THREADS = (SB_CW + 1) * 32;
-constexpr size_t SB_SMEM = SB_STAGES * SB_STAGE_BYTES + 2 * 3 * SB_BOX + 1024 + 64;
+constexpr int SB_BOX = SB_R * SB_C * 2;       // 8 KB
+constexpr int SB_STAGE_BYTES = 3 * SB_BOX;    // dy, g, u
+constexpr int SB_Q = SB_R * SB_C;
+constexpr size_t SB_SMEM = SB_STAGES * SB_STAGE_BYTES + 2 * 3 * SB_BOX + SB_Q * 2 + 1024 + 128;
 
 struct SwiBwdParams {
   int64_t M, h;
@@ -425,26 +495,29 @@ struct SwiBwdParams {
 // MODE 0: rowwise only; 1: rowwise + columnwise MX; 2: rowwise + bf16 transposed
 // dh13 and y.
 template <int MODE>
-__global__ void __launch_bounds__(SB_THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 2)
     swiglu_bwd_kernel(const __grid_constant__ CUtensorMap tmdy, const __grid_constant__ CUtensorMap tmh,
                       SwiBwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* otile = smem + SB_STAGES * SB_STAGE_BYTES;  // 2 buffers x {dg, du, y}
-  uint64_t* full = reinterpret_cast<uint64_t*>(otile + 2 * 3 * SB_BOX);
+  uint16_t* queue = reinterpret_cast<uint16_t*>(otile + 2 * 3 * SB_BOX);
+  uint64_t* full = reinterpret_cast<uint64_t*>(queue + SB_Q);
   uint64_t* empty = full + SB_STAGES;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int s_qn[2];
+  __shared__ long long s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
 
-  __shared__ long long s_abort;  // first tile index whose wait timed out
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < SB_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], SB_CW); }
+  if (tid == 0) {
+    for (int s = 0; s < SB_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CW); }
     fence_mbar_init();
+    s_qn[0] = s_qn[1] = 0;
     s_abort = 0x7FFFFFFFFFFFFFFFll;
   }
   __syncthreads();
 
-  if (warp == SB_CW) {
+  if (warp == CW) {
     if (lane == 0) {
       prefetch_tmap(&tmdy);
       prefetch_tmap(&tmh);
@@ -465,7 +538,8 @@ __global__ void __launch_bounds__(SB_THREADS, 2)
   }
 
   int stage = 0; uint32_t phase = 0; int buf = 0;
-  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+  const int seg = lane & 7;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, buf ^= 1) {
     const int64_t rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
     const int64_t r0 = rt * SB_R, c0 = ct * SB_C;
     const bool ok = mbar_wait(&full[stage], phase, p.err);
@@ -474,110 +548,162 @@ __global__ void __launch_bounds__(SB_THREADS, 2)
     const uint8_t* gt = dyt + SB_BOX;
     const uint8_t* ut = dyt + 2 * SB_BOX;
     uint8_t* ot = otile + buf * 3 * SB_BOX;   // dg | du | y
-    const int seg = lane & 7;
+    int* qn = &s_qn[buf];
+    // ---- phase A
+    if (ok) {
 #pragma unroll 1
-    for (int it = 0; ok && it < SB_R / (4 * SB_CW); ++it) {
-      const int rr = it * (4 * SB_CW) + warp * 4 + (lane >> 3);
-      const uint4 dv = *reinterpret_cast<const uint4*>(dyt + rr * 128 + seg * 16);
-      const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
-      const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
-      const uint32_t dp[4] = {dv.x, dv.y, dv.z, dv.w};
-      const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
-      const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-      uint32_t dgp[4], dup[4], yp[4];
+      for (int it = 0; it < SB_R / (4 * CW); ++it) {
+        const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
+        const uint4 dv = *reinterpret_cast<const uint4*>(dyt + rr * 128 + seg * 16);
+        const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
+        const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
+        const uint32_t dp[4] = {dv.x, dv.y, dv.z, dv.w};
+        const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
+        const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
+        uint32_t dgp[4], dup[4], yp[4];
+        uint32_t slow = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t dgw = 0, duw = 0, yw = 0;
+        for (int i = 0; i < 4; ++i) {
+          uint32_t dgw = 0;
+          float pa[2], dyv[2], uvv[2];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float dyf = hh ? bf16_hi(dp[i]) : bf16_lo(dp[i]);
-          const float g = hh ? bf16_hi(gp[i]) : bf16_lo(gp[i]);
-          const float u = hh ? bf16_hi(up[i]) : bf16_lo(up[i]);
-          const SigFast sf = sig_fast(g);
-          const float a = bf16_lo(silu_bits_from(g, sf));
-          const uint32_t du = f32_to_bf16_bits(__fmul_rn(dyf, a));
-          const uint32_t dg = dg_bits_from(dyf, g, u, sf);
-          dgw |= dg << (16 * hh);
-          duw |= du << (16 * hh);
-          if (MODE == 2) yw |= f32_to_bf16_bits(__fmul_rn(a, u)) << (16 * hh);
+          for (int hh = 0; hh < 2; ++hh) {
+            const float dyf = hh ? bf16_hi(dp[i]) : bf16_lo(dp[i]);
+            const float g = hh ? bf16_hi(gp[i]) : bf16_lo(gp[i]);
+            const float u = hh ? bf16_hi(up[i]) : bf16_lo(up[i]);
+            const SigFast sf = sig_fast(g);
+            pa[hh] = __fmul_rn(g, sf.s);
+            dyv[hh] = dyf;
+            uvv[hh] = u;
+            bool ok_e = sf.ok && clear_of_midpoint(pa[hh], 16);
+            // dg tier 1 (see dg_bits_from)
+            const float dyu = __fmul_rn(dyf, u);
+            const float oms = __fmul_rn(sf.t, sf.s);
+            const float go = __fmul_rn(g, oms);
+            const float inner = __fadd_rn(1.0f, go);
+            const float pg = __fmul_rn(dyu, __fmul_rn(sf.s, inner));
+            const float ratio = fabsf(go) * rcp_approx(fabsf(inner));
+            const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
+            const float adyu = fabsf(dyu), apg = fabsf(pg);
+            ok_e = ok_e && margin < 16384.0f && adyu >= 0x1p-100f && adyu <= 0x1p100f && apg >= 0x1p-100f &&
+                   clear_of_midpoint(pg, (uint32_t)margin);
+            slow |= (ok_e ? 0u : 1u) << (2 * i + hh);
+            dgw |= f32_to_bf16_bits(pg) << (16 * hh);
+          }
+          const __nv_bfloat162 a2 = __floats2bfloat162_rn(pa[0], pa[1]);
+          const float2 af = __bfloat1622float2(a2);
+          const __nv_bfloat162 du2 = __floats2bfloat162_rn(__fmul_rn(dyv[0], af.x), __fmul_rn(dyv[1], af.y));
+          dup[i] = *reinterpret_cast<const uint32_t*>(&du2);
+          dgp[i] = dgw;
+          if (MODE == 2) {
+            const __nv_bfloat162 y2 = __floats2bfloat162_rn(__fmul_rn(af.x, uvv[0]), __fmul_rn(af.y, uvv[1]));
+            yp[i] = *reinterpret_cast<const uint32_t*>(&y2);
+          }
         }
-        dgp[i] = dgw; dup[i] = duw; yp[i] = yw;
-      }
-      uint32_t sg, su;
-      const uint2 cg = quant_row8(dgp, sg);
-      const uint2 cu = quant_row8(dup, su);
-      const int64_t r = r0 + rr;
-      const int64_t c = c0 + seg * 8;
-      if (r < p.M) {
-        *reinterpret_cast<uint2*>(p.q_row + r * 2 * p.h + c) = cg;
-        *reinterpret_cast<uint2*>(p.q_row + r * 2 * p.h + p.h + c) = cu;
-        if ((seg & 3) == 0) {
-          p.s_row.put(r, c >> 5, sg);
-          p.s_row.put(r, (p.h + c) >> 5, su);
-        }
-      }
-      if (MODE != 0) {
         *reinterpret_cast<uint4*>(ot + rr * 128 + seg * 16) = make_uint4(dgp[0], dgp[1], dgp[2], dgp[3]);
         *reinterpret_cast<uint4*>(ot + SB_BOX + rr * 128 + seg * 16) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
         if (MODE == 2)
           *reinterpret_cast<uint4*>(ot + 2 * SB_BOX + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
+        while (slow) {
+          const int j = __ffs(slow) - 1;
+          slow &= slow - 1;
+          queue[atomicAdd(qn, 1)] = (uint16_t)(rr * SB_C + seg * 8 + j);
+        }
       }
     }
-    __syncwarp();
+    bar_consumers();
+    if (tid == 0) s_qn[buf ^ 1] = 0;
+    // ---- phase B: exact tiers for the queued elements
+    if (ok) {
+      const int n = *qn;
+      for (int i = tid; i < n; i += CT) {
+        const int idx = queue[i];
+        const int off = (idx / SB_C) * 128 + (idx % SB_C) * 2;
+        const float dyf = bf16_lo(*reinterpret_cast<const uint16_t*>(dyt + off));
+        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off));
+        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off));
+        const SigFast sf = sig_fast(g);
+        const float a = bf16_lo(silu_bits_from(g, sf));
+        *reinterpret_cast<uint16_t*>(ot + off) = (uint16_t)dg_bits_from(dyf, g, u, sf);
+        *reinterpret_cast<uint16_t*>(ot + SB_BOX + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(dyf, a));
+        if (MODE == 2) *reinterpret_cast<uint16_t*>(ot + 2 * SB_BOX + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
+      }
+    }
+    bar_consumers();
     if (ok && lane == 0) mbar_arrive(&empty[stage]);
     if (++stage == SB_STAGES) { stage = 0; phase ^= 1; }
-
-    if (MODE != 0) {
-      named_bar_sync(1, SB_CW * 32);
-      if (s_abort <= t) break;
-      if (MODE == 1) {
-        // 128 columns (dg 0..63, du 64..127) x 2 row blocks = 256 items
-        const int item = warp * 32 + lane;
-        const int colx = item & 127, rb = item >> 7;
-        const int which = colx >> 6, col = colx & 63;
-        const uint8_t* src = ot + which * SB_BOX;
-        uint32_t v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint16_t*>(src + (rb * 32 + i) * 128 + col * 2);
-        uint32_t codes[8];
-        const uint32_t s = quant_col32(v, codes);
-        const int64_t rg = r0 + rb * 32;
-        const int64_t orow = (which ? p.h : 0) + c0 + col;
-        if (rg < p.M) {
-          uint8_t* dst = p.q_col + orow * p.M + rg;
-          store16(dst, codes[0], codes[1], codes[2], codes[3]);
-          store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
-          p.s_col.put(orow, rg >> 5, s);
+    if (s_abort <= t) break;
+    // ---- phase C
+    if (warp >= 4 || MODE == 0) {
+      // rows of dg and du: 8 lanes per 64-column row; 4 rows per warp step
+      const int w = MODE == 0 ? warp : warp - 4;
+      const int nw = MODE == 0 ? CW : 4;
+      for (int k = w * 4 + (lane >> 3); k < 2 * SB_R; k += nw * 4) {
+        const int which = k / SB_R, rr = k % SB_R;
+        const uint4 v = *reinterpret_cast<const uint4*>(ot + which * SB_BOX + rr * 128 + seg * 16);
+        const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
+        uint32_t sc;
+        const uint2 codes = quant_row8(pk, sc);
+        const int64_t r = r0 + rr;
+        const int64_t c = (which ? p.h : 0) + c0 + seg * 8;
+        if (r < p.M) {
+          *reinterpret_cast<uint2*>(p.q_row + r * 2 * p.h + c) = codes;
+          if ((seg & 3) == 0) p.s_row.put(r, c >> 5, sc);
         }
-      } else {
-        // bf16 transposed dg, du (into dh13_t) and y (into y_t): 192 columns x
-        // 2 half-tiles of 32 rows = 384 items
-        for (int item = warp * 32 + lane; item < 384; item += SB_CW * 32) {
-          const int colx = item % 192, rb = item / 192;
-          const int which = colx / 64, col = colx % 64;
-          const uint8_t* src = ot + which * SB_BOX;
-          uint32_t w[16];
+      }
+    } else if (MODE == 1) {
+      // columns of dg, du: 64 column pairs x 2 row blocks = 128 items on warps 0-3
+      const int item = warp * 32 + lane;
+      const int pcx = item & 63, rb = item >> 6;
+      const int which = pcx >> 5, pc = pcx & 31;
+      const uint8_t* src = ot + which * SB_BOX;
+      uint32_t v[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + (rb * 32 + 2 * i) * 128 + col * 2);
-            const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + (rb * 32 + 2 * i + 1) * 128 + col * 2);
-            w[i] = a0 | (a1 << 16);
-          }
-          const int64_t rg = r0 + rb * 32;
-          if (rg < p.M) {
-            uint16_t* dst;
-            if (which == 2) dst = p.y_t ? p.y_t + (c0 + col) * p.M + rg : nullptr;
-            else dst = p.dh13_t ? p.dh13_t + ((which ? p.h : 0) + c0 + col) * p.M + rg : nullptr;
-            if (dst) {
+      for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + i) * 128 + pc * 4);
+      uint32_t ca[8], cb[8], sa, sb;
+      quant_col32x2(v, ca, cb, sa, sb);
+      const int64_t rg = r0 + rb * 32;
+      if (rg < p.M) {
+        const int64_t orow = (which ? p.h : 0) + c0 + 2 * pc;
+        uint8_t* dst = p.q_col + orow * p.M + rg;
+        store16(dst, ca[0], ca[1], ca[2], ca[3]);
+        store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
+        store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
+        store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
+        p.s_col.put(orow, rg >> 5, sa);
+        p.s_col.put(orow + 1, rg >> 5, sb);
+      }
+    } else {
+      // bf16 transposed dg, du (into dh13_t) and y (into y_t): 96 column
+      // pairs x 2 blocks of 32 rows = 192 items on warps 0-3
+      for (int item = warp * 32 + lane; item < 192; item += 128) {
+        const int pcx = item % 96, rb = item / 96;
+        const int which = pcx / 32, pc = pcx % 32;
+        const uint8_t* src = ot + which * SB_BOX;
+        uint32_t wa[16], wb[16];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) store16(dst + q * 8, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t r0v = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + 2 * i) * 128 + pc * 4);
+          const uint32_t r1v = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + 2 * i + 1) * 128 + pc * 4);
+          wa[i] = (r0v & 0xFFFFu) | (r1v << 16);
+          wb[i] = (r0v >> 16) | (r1v & 0xFFFF0000u);
+        }
+        const int64_t rg = r0 + rb * 32;
+        if (rg < p.M) {
+          const int64_t col = c0 + 2 * pc;
+          uint16_t* base = which == 2 ? p.y_t : p.dh13_t;
+          if (base) {
+            const int64_t orow = (which == 1 ? p.h : 0) + col;
+            uint16_t* da = base + orow * p.M + rg;
+            uint16_t* db = da + p.M;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              store16(da + q * 8, wa[4 * q], wa[4 * q + 1], wa[4 * q + 2], wa[4 * q + 3]);
+              store16(db + q * 8, wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
             }
           }
         }
       }
-      buf ^= 1;
-    } else if (!ok) {
-      break;
     }
   }
 }
@@ -608,11 +734,11 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   if (s.q_col) {
     auto k = swiglu_fwd_kernel<true>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SF_SMEM);
-    if (e == cudaSuccess) { k<<<grid, SF_THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
+    if (e == cudaSuccess) { k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
   } else {
     auto k = swiglu_fwd_kernel<false>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SF_SMEM);
-    if (e == cudaSuccess) { k<<<grid, SF_THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
+    if (e == cudaSuccess) { k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
   }
   return cuda_status(e, "swiglu_fwd_kernel launch");
 }
@@ -654,7 +780,7 @@ int launch_swiglu_bwd(const SwigluLaunch& s, cudaStream_t stream) {
   do {                                                                                          \
     auto k = swiglu_bwd_kernel<MODE>;                                                           \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SB_SMEM);     \
-    if (e == cudaSuccess) { k<<<grid, SB_THREADS, SB_SMEM, stream>>>(tdy, th, p); e = cudaGetLastError(); } \
+    if (e == cudaSuccess) { k<<<grid, THREADS, SB_SMEM, stream>>>(tdy, th, p); e = cudaGetLastError(); } \
   } while (0)
   if (mode == 0) MX_LAUNCH_B(0);
   else if (mode == 1) MX_LAUNCH_B(1);

@@ -2,7 +2,8 @@
 // used by the standalone cast kernel and by the fused SwiGLU kernels.
 //
 // Row blocks: four consecutive lanes each hold 8 consecutive elements of one
-// 32-element block.  Column blocks: one thread holds all 32 elements.
+// 32-element block.  Column blocks: one thread holds the 32 elements of two
+// adjacent columns as packed pairs.
 #pragma once
 
 #include "common.cuh"
@@ -21,27 +22,31 @@ struct ScaleDst {
   }
 };
 
-// max |x| over 8 bf16 values given as 4 packed pairs -> bf16 bit pattern of
-// the maximum magnitude (integer compare of |bits| orders finite values and
-// puts Inf/NaN above every finite value).
-MX_DEVINL uint32_t absmax_bits8(const uint32_t (&p)[4]) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = max(m, p[i] & 0x7FFFu);
-    m = max(m, (p[i] >> 16) & 0x7FFFu);
-  }
-  return m;
+// |x| of a packed bf16 pair, and the pairwise maximum propagating NaN:
+// on magnitudes the float order equals the order of the bit patterns, and a
+// NaN or an infinity lands at or above 0x7F80, which the scale rule maps to
+// 0xFF.
+MX_DEVINL uint32_t abs2(uint32_t p) { return p & 0x7FFF7FFFu; }
+MX_DEVINL uint32_t max2(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r =
+      __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// larger magnitude of the two halves, as a 16-bit pattern (NaN -> >= 0x7F80)
+MX_DEVINL uint32_t max_halves(uint32_t m2) {
+  const uint32_t lo = m2 & 0xFFFFu, hi = m2 >> 16;
+  const uint32_t isnan = (lo > 0x7F80u) | (hi > 0x7F80u);
+  return isnan ? 0x7FC0u : max(lo, hi);
 }
 
 // Quantize 8 elements (4 packed bf16 pairs, element 2i in the low half) of a
 // row block spread over 4 consecutive lanes.  Returns the 8 codes as two
 // 32-bit words (element 0 in the lowest byte) and the block scale byte.
 MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out) {
-  uint32_t m = absmax_bits8(p);
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-  const uint32_t s = e8m0_from_amax_bits(m);
+  uint32_t m2 = max2(max2(abs2(p[0]), abs2(p[1])), max2(abs2(p[2]), abs2(p[3])));
+  m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
+  m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 2));
+  const uint32_t s = e8m0_from_amax_bits(max_halves(m2));
   scale_out = s;
   uint2 out;
   if (s == 0xFF) {
@@ -58,26 +63,33 @@ MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out) {
   return out;
 }
 
-// Quantize one 32-element column block held by one thread as 32 bf16 bit
-// patterns (low 16 bits of each word).  Writes 8 words of codes.
-MX_DEVINL uint32_t quant_col32(const uint32_t (&v)[32], uint32_t (&codes)[8]) {
-  uint32_t m = 0;
+// Quantize two 32-element column blocks held by one thread as 32 packed
+// words (row i of column A in the low half of v[i], column B in the high
+// half).  Writes 8 words of codes per column and returns both scales.
+MX_DEVINL void quant_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_t (&cb)[8], uint32_t& sa,
+                             uint32_t& sb) {
+  uint32_t m2 = abs2(v[0]);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) m = max(m, v[i] & 0x7FFFu);
-  const uint32_t s = e8m0_from_amax_bits(m);
-  if (s == 0xFF) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
-    return s;
-  }
-  const float inv = inv_scale_from_e8m0(s);
+  for (int i = 1; i < 32; ++i) m2 = max2(m2, abs2(v[i]));
+  const uint32_t la = m2 & 0xFFFFu, lb = m2 >> 16;
+  sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la);
+  sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb);
+  const float ia = inv_scale_from_e8m0(sa), ib = inv_scale_from_e8m0(sb);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t lo = cvt_e4m3x2(bf16_lo(v[4 * i]) * inv, bf16_lo(v[4 * i + 1]) * inv);
-    const uint32_t hi = cvt_e4m3x2(bf16_lo(v[4 * i + 2]) * inv, bf16_lo(v[4 * i + 3]) * inv);
-    codes[i] = lo | (hi << 16);
+    const uint32_t a01 = cvt_e4m3x2(bf16_lo(v[4 * i]) * ia, bf16_lo(v[4 * i + 1]) * ia);
+    const uint32_t a23 = cvt_e4m3x2(bf16_lo(v[4 * i + 2]) * ia, bf16_lo(v[4 * i + 3]) * ia);
+    const uint32_t b01 = cvt_e4m3x2(bf16_hi(v[4 * i]) * ib, bf16_hi(v[4 * i + 1]) * ib);
+    const uint32_t b23 = cvt_e4m3x2(bf16_hi(v[4 * i + 2]) * ib, bf16_hi(v[4 * i + 3]) * ib);
+    ca[i] = a01 | (a23 << 16);
+    cb[i] = b01 | (b23 << 16);
   }
-  return s;
+  if (sa == 0xFF)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ca[i] = 0x7F7F7F7Fu;
+  if (sb == 0xFF)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cb[i] = 0x7F7F7F7Fu;
 }
 
 MX_DEVINL void store16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
