@@ -24,7 +24,7 @@ __all__ = [
     "MxError", "lib", "library_path", "ROW", "COL", "BOTH", "SCALE_LINEAR", "SCALE_MMA",
     "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "GROUP_M", "GROUP_K", "mma_scale_bytes",
     "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
-    "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "MlpContext", "ErrorWord",
+    "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
 ]
 
 ROW, COL, BOTH = 1, 2, 3
@@ -52,6 +52,7 @@ _SIGS = {
     "mx_mlp_fwd": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V], _I),
     "mx_mlp_bwd": ([_V, _V, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V,
                     _V, _V], _I),
+    "mx_mlp_fwd_static_scratch": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V], _I),
 }
 
 
@@ -277,6 +278,27 @@ def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL, pad_multiple=128, scr
         out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
     _check(lib().mx_mlp_fwd(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), M, d, h, _ptr(offs), max(E, 1), pad_multiple,
                             recipe, _ptr(ctx), _ptr(scratch), _ptr(out), err.ptr() if err else None, _stream()))
+    return out, MlpContext(ctx, dict(x=x, w1=w1, w3=w3, w2=w2, offs=offs, recipe=recipe, M=M, d=d, h=h, E=E,
+                                     pad=pad_multiple))
+
+
+def mlp_fwd_static_scratch(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL, pad_multiple=128,
+                           err: ErrorWord | None = None, out=None):
+    """mlp_fwd whose temporary buffer is the library's fixed device array
+    (for callers that cannot allocate device memory; only problems whose
+    scratch fits MX_STATIC_SCRATCH_BYTES).  Returns (out, ctx)."""
+    for n, t in (("x", x), ("w1", w1), ("w3", w3), ("w2", w2)):
+        _need(t, torch.bfloat16, n)
+    M, d = x.shape
+    h = w1.shape[-2]
+    E = 0 if offs is None else offs.numel()
+    cb, _ = mlp_workspace_size(M, d, h, E, recipe)
+    ctx = torch.empty(cb, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mx_mlp_fwd_static_scratch(_ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), M, d, h, _ptr(offs), max(E, 1),
+                                           pad_multiple, recipe, _ptr(ctx), _ptr(out), err.ptr() if err else None,
+                                           _stream()))
     return out, MlpContext(ctx, dict(x=x, w1=w1, w3=w3, w2=w2, offs=offs, recipe=recipe, M=M, d=d, h=h, E=E,
                                      pad=pad_multiple))
 

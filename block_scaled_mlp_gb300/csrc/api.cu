@@ -494,3 +494,47 @@ int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const void* w1,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward pass with a library-owned scratch array (no allocation anywhere).
+
+namespace {
+// The temporary buffer of mx_mlp_fwd_static_scratch.  In host code this name
+// is only a host-side handle, not a device address: the device address is
+// looked up per device with cudaGetSymbolAddress and cached below.
+static __device__ __align__(256) uint8_t g_static_scratch[MX_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {nullptr};
+}  // namespace
+
+extern "C" int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const void* w3, const void* w2,
+                                         int64_t M_total, int64_t d, int64_t h, const int32_t* offs, int32_t E,
+                                         int32_t pad_multiple, int recipe, void* ctx, void* out, int32_t* err_word,
+                                         void* stream) {
+  size_t ctx_bytes = 0, scratch_bytes = 0;
+  int rc = mx_mlp_workspace_size(M_total, d, h, offs ? E : 0, recipe, &ctx_bytes, &scratch_bytes);
+  if (rc) return rc;
+  if (scratch_bytes > (size_t)MX_STATIC_SCRATCH_BYTES)
+    return fail(MX_ERR_UNSUPPORTED,
+                "mx_mlp_fwd_static_scratch: this problem needs %zu scratch bytes, more than the static "
+                "array's %u; use mx_mlp_fwd with a caller buffer",
+                scratch_bytes, (unsigned)MX_STATIC_SCRATCH_BYTES);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MX_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+      if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(static scratch)");
+      g_static_ptr[dev] = ptr;
+    }
+    scratch = g_static_ptr[dev];
+  }
+  return mx_mlp_fwd(x, w1, w3, w2, M_total, d, h, offs, E, pad_multiple, recipe, ctx, scratch, out, err_word,
+                    stream);
+}

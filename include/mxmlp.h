@@ -236,6 +236,35 @@ MX_API int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const vo
                int32_t E, int32_t pad_multiple, int recipe, void* scratch, void* dx, void* dw1,
                void* dw3, void* dw2, int32_t* err_word, void* stream);
 
+/*
+ * mx_mlp_fwd_static_scratch - mx_mlp_fwd for callers that cannot allocate
+ * device memory (no cudaMalloc at all: for instance code running where only
+ * pre-registered buffers may be touched, or a host framework whose allocator
+ * is not reachable from the call site).  The pages have no counterpart of
+ * this entry point; it is a convenience of this library.
+ *
+ * Same arguments and results as mx_mlp_fwd, except that the temporary
+ * buffer comes from a fixed device array inside the library
+ * (MX_STATIC_SCRATCH_BYTES bytes, held by every GPU that loads the library
+ * until the process exits) instead of from the caller.  The caller still
+ * passes the inputs, ctx (as sized by mx_mlp_workspace_size) and out.
+ * - Problems whose scratch_bytes (mx_mlp_workspace_size) exceed
+ *   MX_STATIC_SCRATCH_BYTES are rejected with MX_ERR_UNSUPPORTED.
+ * - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   CUDA stream capture.
+ * - All calls share the one array and the kernels overwrite every byte they
+ *   read back, so no clearing is needed between calls; calls that overlap
+ *   on the GPU (different streams, or different threads without ordering)
+ *   race on the array and must not be issued.
+ */
+#define MX_STATIC_SCRATCH_BYTES (16u << 20)
+MX_API int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const void* w3, const void* w2,
+                                     int64_t M_total, int64_t d, int64_t h, const int32_t* offs,
+                                     int32_t E, int32_t pad_multiple, int recipe, void* ctx,
+                                     void* out, int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
