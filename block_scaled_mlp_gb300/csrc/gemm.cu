@@ -10,8 +10,9 @@
 //   warp 1      TMEM allocation + single-thread MMA issue: per 128-element
 //               K step it copies the scale tiles into TMEM (tcgen05.cp) and
 //               issues 4 x tcgen05.mma (K = 32 for E4M3, 16 x 4 for bf16)
-//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, RN to bf16,
-//               128-byte-swizzled staging in shared memory, TMA store
+//   warps 2-9   epilogue (two warps per TMEM lane quarter, half of the
+//               columns each): tcgen05.ld of the fp32 accumulator, RN to
+//               bf16, 64-byte-swizzled staging in shared memory, TMA store
 // Modes: dense; M-grouped (forward / input gradient: token rows of group e
 // use expert e's weights, rows past the last group are zero); K-grouped
 // (weight gradient: expert e contracts over its own token range; an empty
@@ -24,23 +25,23 @@ namespace mx {
 namespace {
 
 constexpr int BM = 128;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each draining half of the columns
 constexpr int GEMM_THREADS = 64 + EPI_WARPS * 32;
 constexpr int MAX_GROUPS = 1024;
 
 template <bool MX, int BN>
 struct Cfg {
-  static constexpr int BK = MX ? 128 : 64;                 // elements per stage (128 bytes)
-  static constexpr int UK = MX ? 32 : 16;                  // elements per MMA
+  static constexpr int BK = MX ? 128 : 64;                 // elements per stage (128 bytes of K)
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int SFA_BYTES = MX ? 512 : 0;
+  static constexpr int SFA_BYTES = MX ? 512 : 0;           // one scale tile of A per stage
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int NUM_ACC = BN == 256 ? 1 : 2;
-  static constexpr int EPI_BYTES = EPI_WARPS * 32 * 128;   // one 32x64 bf16 buffer per warp
+  static constexpr int EPI_BYTES = EPI_WARPS * 32 * 64;    // one 32x32 bf16 buffer per warp
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SF_COL = NUM_ACC * BN;
+  static constexpr int SF_COL = NUM_ACC * BN;               // per-stage scale slots from here
+  static constexpr int SF_SLOT = 4 + 4 * (BN / 128);       // TMEM columns of one stage's scales
   static constexpr size_t SMEM = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES +
                                  MAX_GROUPS * 4 + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr uint32_t IDESC =
@@ -51,7 +52,8 @@ struct Cfg {
 struct GemmParams {
   int mode;
   int64_t M, N, K;            // K: contraction length of A (GROUP_K: total tokens)
-  int64_t m_tiles, n_tiles, tiles;
+  int64_t m_tiles, n_tiles, tiles;  // tiles: work units (tiles, or tile pairs with clusters)
+  int64_t m_pairs;            // ceil(m_tiles / 2)
   int32_t E;
   const int32_t* offs;
   const uint8_t* sfa;         // MMA-layout scales of A ([M, K/32])
@@ -67,79 +69,129 @@ struct TileInfo {
   int32_t e;       // expert (GROUP_M / GROUP_K), 0 for dense
   int64_t k0;      // first contraction element
   int32_t num_kb;  // number of BK steps (0: write zeros)
+  bool store;      // false: a pair's filler tile (computed, never stored)
 };
 
-// Group ends in shared memory; ok == false if they break the contract.
+// Group data in shared memory; ok == false if the offsets break the contract.
+//   ends[e]     cumulative group ends (CL == 1, and GROUP_K with clusters)
+//   pair_end[e] cumulative 128-row tile pairs of groups 0..e (GROUP_M with
+//               clusters; the offsets themselves are then read from global)
 struct Groups {
   const int32_t* ends;
+  const int32_t* pair_end;
   int32_t E;
+  int64_t units_per_n;  // GROUP_M with clusters: tile pairs in one 128-row column
   bool ok;
 };
 
-template <int BK>
-MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t t) {
+// Work unit -> the tile this CTA (cluster rank `rank`) computes.  Without
+// clusters a unit is one tile.  With 2-CTA clusters a unit is a pair of
+// vertically adjacent tiles sharing one B tile (multicast), the same expert
+// and the same K range; a group with an odd number of 128-row tiles pads its
+// last pair with a filler tile that is computed but not stored.
+template <int BK, int CL>
+MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, int rank) {
   TileInfo ti{};
+  ti.store = true;
   if (p.mode == GEMM_GROUP_K) {
-    const int64_t per_e = p.m_tiles * p.n_tiles;
-    const int64_t e = t / per_e;
-    const int64_t rem = t - e * per_e;
+    const int64_t mt = CL == 2 ? p.m_pairs : p.m_tiles;
+    const int64_t per_e = mt * p.n_tiles;
+    const int64_t e = u / per_e;
+    const int64_t rem = u - e * per_e;
     ti.e = (int32_t)e;
-    ti.m_blk = rem % p.m_tiles;
-    ti.n_blk = rem / p.m_tiles;
+    ti.m_blk = CL == 2 ? 2 * (rem % mt) + rank : rem % mt;
+    ti.n_blk = rem / mt;
+    ti.store = ti.m_blk < p.m_tiles;
     const int64_t s = e == 0 ? 0 : g.ends[e - 1];
     const int64_t en = g.ends[e];
     ti.k0 = s;
     ti.num_kb = g.ok ? (int32_t)((en - s) / BK) : 0;
     return ti;
   }
-  ti.m_blk = t % p.m_tiles;
-  ti.n_blk = t / p.m_tiles;
   ti.k0 = 0;
   ti.num_kb = (int32_t)(p.K / BK);
   ti.e = 0;
-  if (p.mode == GEMM_GROUP_M) {
-    const int64_t row = ti.m_blk * BM;
-    if (!g.ok || g.E == 0 || row >= g.ends[g.E - 1]) {
-      ti.num_kb = 0;  // tail rows (or invalid offsets): zeros
-    } else {
-      int lo = 0, hi = g.E - 1;  // first group whose end is > row
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (g.ends[mid] > row) hi = mid; else lo = mid + 1;
+  if (CL == 1) {
+    ti.m_blk = u % p.m_tiles;
+    ti.n_blk = u / p.m_tiles;
+    if (p.mode == GEMM_GROUP_M) {
+      const int64_t row = ti.m_blk * BM;
+      if (!g.ok || g.E == 0 || row >= g.ends[g.E - 1]) {
+        ti.num_kb = 0;  // tail rows (or invalid offsets): zeros
+      } else {
+        int lo = 0, hi = g.E - 1;  // first group whose end is > row
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (g.ends[mid] > row) hi = mid; else lo = mid + 1;
+        }
+        ti.e = lo;
       }
-      ti.e = lo;
     }
+    return ti;
   }
+  if (p.mode == GEMM_DENSE) {
+    ti.m_blk = 2 * (u % p.m_pairs) + rank;
+    ti.n_blk = u / p.m_pairs;
+    ti.store = ti.m_blk < p.m_tiles;
+    return ti;
+  }
+  // GROUP_M with clusters
+  const int64_t P = u % g.units_per_n;
+  ti.n_blk = u / g.units_per_n;
+  const int64_t last_end = g.ok ? (int64_t)p.offs[g.E - 1] : 0;
+  const int64_t groups_pairs = g.ok ? g.pair_end[g.E - 1] : 0;
+  if (P >= groups_pairs) {  // tail (or every tile, for invalid offsets): zeros
+    ti.m_blk = last_end / BM + 2 * (P - groups_pairs) + rank;
+    ti.num_kb = 0;
+    ti.store = ti.m_blk < p.m_tiles;
+    return ti;
+  }
+  int lo = 0, hi = g.E - 1;  // first group whose pair_end is > P
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (g.pair_end[mid] > P) hi = mid; else lo = mid + 1;
+  }
+  const int64_t p_in = P - (lo == 0 ? 0 : g.pair_end[lo - 1]);
+  const int64_t start = lo == 0 ? 0 : (int64_t)p.offs[lo - 1];
+  const int64_t mb = ((int64_t)p.offs[lo] - start) / BM;
+  ti.e = lo;
+  ti.m_blk = start / BM + 2 * p_in + rank;
+  ti.store = 2 * p_in + rank < mb;
   return ti;
 }
 
-template <bool MX, int BN>
+template <bool MX, int BN, int CL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                GemmParams p) {
+                const __grid_constant__ CUtensorMap tmSFB, GemmParams p) {
   using C = Cfg<MX, BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + C::STAGES * C::A_BYTES;
   uint8_t* sEpi = sB + C::STAGES * C::B_BYTES;
-  uint8_t* sSFA = sEpi + C::EPI_BYTES;
-  uint8_t* sSFB = sSFA + C::STAGES * C::SFA_BYTES;
-  int32_t* sEnds = reinterpret_cast<int32_t*>(sSFB + C::STAGES * C::SFB_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sEnds + MAX_GROUPS);
+  uint8_t* sSFA = sEpi + C::EPI_BYTES;                       // [STAGES][512]
+  uint8_t* sSFB = sSFA + C::STAGES * C::SFA_BYTES;            // [STAGES][BN/128][512]
+  int32_t* sGroups = reinterpret_cast<int32_t*>(sSFB + C::STAGES * C::SFB_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sGroups + MAX_GROUPS);
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + C::NUM_ACC;
   uint64_t* done_bar = acc_empty + C::NUM_ACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
   __shared__ int s_groups_ok;
+  __shared__ long long s_units_per_n;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
+  const int64_t unit0 = CL == 2 ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t ustep = CL == 2 ? gridDim.x / 2 : gridDim.x;
+  const bool pairs_m = CL == 2 && p.mode == GEMM_GROUP_M;
 
-  // ---- setup: barriers, group ends, TMEM
+  // ---- setup: barriers, group data, TMEM
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
     for (int a = 0; a < C::NUM_ACC; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], EPI_WARPS); }
     mbar_init(done_bar, 1);
     fence_mbar_init();
@@ -151,8 +203,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
       const int32_t v = p.offs[e];
       const int32_t prev = e == 0 ? 0 : p.offs[e - 1];
-      sEnds[e] = v;
+      if (!pairs_m) sGroups[e] = v;
       if (v < prev || (v & 127) != 0 || (int64_t)v > limit) s_groups_ok = 0;
+    }
+  }
+  __syncthreads();
+  if (pairs_m && threadIdx.x == 0) {
+    int64_t acc = 0;
+    if (s_groups_ok) {
+      int32_t prev = 0;
+      for (int e = 0; e < p.E; ++e) {
+        const int32_t v = p.offs[e];
+        acc += ((v - prev) / BM + 1) / 2;
+        sGroups[e] = (int32_t)acc;
+        prev = v;
+      }
+      const int64_t tail = p.m_tiles - prev / BM;
+      s_units_per_n = acc + (tail + 1) / 2;
+    } else {
+      s_units_per_n = p.m_pairs;
     }
   }
   if (warp == 1) {
@@ -162,46 +231,56 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
   const uint32_t tmem = *tmem_holder;
-  Groups grp{sEnds, p.E, s_groups_ok != 0};
+  Groups grp{sGroups, sGroups, p.E, pairs_m ? s_units_per_n : 0, s_groups_ok != 0};
   if (!grp.ok && threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, MX_ERR_BAD_OFFSETS);
+  const int64_t n_units = pairs_m ? grp.units_per_n * p.n_tiles : p.tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
+      if (MX) prefetch_tmap(&tmSFB);
       int stage = 0; uint32_t phase = 0;
       const int64_t sfa_row_tiles = p.K / 128;  // scale tiles per 128-row block of A
-      for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-        const TileInfo ti = tile_info<C::BK>(p, grp, t);
+      for (int64_t u = unit0; u < n_units; u += ustep) {
+        const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
         bool ok = true;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.err)) { ok = false; break; }
           const int64_t k = ti.k0 + (int64_t)kb * C::BK;
-          uint32_t bytes = C::A_BYTES + C::B_BYTES;
-          int nsfb = 0;
-          if (MX) {
-            const int64_t n_sub_total = p.N / 128;
-            const int64_t left = n_sub_total - ti.n_blk * (BN / 128);
-            nsfb = (int)(left < BN / 128 ? left : BN / 128);
-            bytes += 512 + 512 * nsfb;
-          }
+          const uint32_t bytes = C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? 512 : 0) + C::SFB_BYTES : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * BM), &full[stage]);
-          if (p.mode == GEMM_GROUP_M)
-            tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
-          else
-            tma_load_2d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), &full[stage]);
+          if (CL == 1) {
+            if (p.mode == GEMM_GROUP_M)
+              tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
+            else
+              tma_load_2d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), &full[stage]);
+          } else {
+            // this CTA's half of the B tile, delivered to both CTAs of the pair
+            uint8_t* dst = sB + stage * C::B_BYTES + rank * (C::B_BYTES / 2);
+            const int32_t nrow = (int32_t)(ti.n_blk * BN + rank * (BN / 2));
+            if (p.mode == GEMM_GROUP_M)
+              tma_load_3d_mc(dst, &tmB, (int32_t)k, nrow, ti.e, &full[stage], (uint16_t)0x3);
+            else
+              tma_load_2d_mc(dst, &tmB, (int32_t)k, nrow, &full[stage], (uint16_t)0x3);
+          }
           if (MX) {
             const int64_t kt = k / 128;
-            bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, 512, &full[stage]);
-            const uint8_t* sfb = p.sfb + (p.mode == GEMM_GROUP_M ? (int64_t)ti.e * p.sfb_expert_stride : 0);
-            for (int j = 0; j < nsfb; ++j) {
-              const int64_t nsub = ti.n_blk * (BN / 128) + j;
-              bulk_load(sSFB + stage * C::SFB_BYTES + j * 512, sfb + (nsub * sfa_row_tiles + kt) * 512, 512,
+            if (ti.store)
+              bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, 512,
                         &full[stage]);
-            }
+            // all of the tile's B scale tiles (BN/128 tile rows) in one copy;
+            // rows past N are zero-filled and counted
+            if (p.mode == GEMM_GROUP_M)
+              tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)), ti.e,
+                          &full[stage]);
+            else
+              tma_load_3d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)),
+                          &full[stage]);
           }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -211,12 +290,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are formed once and advanced by adding the byte offset
+    // (>> 4) to their start-address field.
     if (lane == 0) {
+      const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
+      const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 128, 128, 0);
+      const uint64_t sfb_desc0 = smem_desc(smem_u32(sSFB), 128, 128, 0);
       int stage = 0; uint32_t phase = 0;
       int acc = 0; uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
-        const TileInfo ti = tile_info<C::BK>(p, grp, t);
+      for (int64_t u = unit0; u < n_units && ok; u += ustep) {
+        const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
         if (ti.num_kb == 0) continue;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, p.err)) { ok = false; break; }
         tc_fence_after();
@@ -224,28 +309,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+          const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT;
           if (MX) {
-            tmem_cp_32x128b_x4(tmem + C::SF_COL, smem_desc(smem_u32(sSFA + stage * C::SFA_BYTES), 128, 128, 0));
+            tmem_cp_32x128b_x4(sf_col, sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES) >> 4));
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)
-              tmem_cp_32x128b_x4(tmem + C::SF_COL + 4 + 4 * j,
-                                 smem_desc(smem_u32(sSFB + stage * C::SFB_BYTES + j * 512), 128, 128, 0));
+              tmem_cp_32x128b_x4(sf_col + 4 + 4 * j, sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + j * 512) >> 4));
           }
+          const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < 128 / 32; ++k) {
-            const uint64_t ad = smem_desc(a_base + k * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_base + k * 32, 16, 1024, 2);
+          for (int k = 0; k < 4; ++k) {
             const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
-            if (MX) {
-              const uint32_t idesc = C::IDESC | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              mma_mxf8(d_tmem, ad, bd, idesc, tmem + C::SF_COL, tmem + C::SF_COL + 4, accum);
-            } else {
-              mma_bf16(d_tmem, ad, bd, C::IDESC, accum);
-            }
+            if (MX)
+              mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, C::IDESC | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf_col,
+                       sf_col + 4, accum);
+            else
+              mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, C::IDESC, accum);
           }
-          tc_commit(&empty[stage]);
+          // the stage is free once these MMAs are done; with clusters both
+          // CTAs of the pair must release it before either refills it
+          if (CL == 2) tc_commit_mc(&empty[stage], (uint16_t)0x3);
+          else tc_commit(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -259,40 +344,51 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    uint8_t* stg = sEpi + (warp - 2) * (32 * 128);
+    // warp -> TMEM lane quarter q (rows 32q..32q+31 of the tile) and column
+    // half; 32-column chunks staged with the 64-byte swizzle and TMA-stored
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    uint8_t* stg = sEpi + ew * (32 * 64);
     int acc = 0; uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-      const TileInfo ti = tile_info<C::BK>(p, grp, t);
-      // output row of this warp's 32 rows
+    for (int64_t u = unit0; u < n_units; u += ustep) {
+      const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
       int64_t mrow = ti.m_blk * BM + q * 32;
       const CUtensorMap* tmC = &tmC0;
       if (p.split > 0 && mrow >= p.split) { tmC = &tmC1; mrow -= p.split; }
       if (p.mode == GEMM_GROUP_K) mrow += (int64_t)ti.e * p.msub;
-      const int64_t ncol0 = ti.n_blk * BN;
-      const int64_t cleft = (p.N - ncol0 + 63) / 64;
-      const int nchunks = (int)(cleft < BN / 64 ? cleft : BN / 64);
+      const int64_t ncol0 = ti.n_blk * BN + half * (BN / 2);
+      const int64_t cleft = (p.N - ncol0 + 31) / 32;
+      const int nchunks = (int)(cleft < BN / 64 ? (cleft > 0 ? cleft : 0) : BN / 64);
       if (ti.num_kb == 0) {
+        if (!ti.store) continue;
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        uint4* row = reinterpret_cast<uint4*>(stg + lane * 128);
+        uint4* row = reinterpret_cast<uint4*>(stg + lane * 64);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) row[j] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 4; ++j) row[j] = make_uint4(0, 0, 0, 0);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          for (int c = 0; c < nchunks; ++c) tma_store_2d(tmC, stg, (int32_t)(ncol0 + 64 * c), (int32_t)mrow);
+          for (int c = 0; c < nchunks; ++c) tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
           bulk_commit();
         }
         continue;
       }
       if (!mbar_wait(&acc_full[acc], acc_phase, p.err)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (!ti.store) {  // filler tile: release the accumulator unread
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
+        continue;
+      }
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * (BN / 2));
+#pragma unroll 1
       for (int c = 0; c < BN / 64; ++c) {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32cols(tbase + c * 64, r0);
-        tmem_ld_32cols(tbase + c * 64 + 32, r1);
+        uint32_t r[32];
+        tmem_ld_32cols(tbase + c * 32, r);
         tmem_ld_wait();
         if (c == BN / 64 - 1) {
           // accumulator fully read: hand it back to the MMA warp
@@ -301,22 +397,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
         if (c >= nchunks) continue;
-        uint32_t w[32];
+        uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          w[i] = f32_to_bf16_bits(__uint_as_float(r0[2 * i])) | (f32_to_bf16_bits(__uint_as_float(r0[2 * i + 1])) << 16);
-          w[16 + i] = f32_to_bf16_bits(__uint_as_float(r1[2 * i])) | (f32_to_bf16_bits(__uint_as_float(r1[2 * i + 1])) << 16);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        uint8_t* row = stg + lane * 128;
+        uint8_t* row = stg + lane * 64;
+        const int sw = (lane >> 1) & 3;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) * 16)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(tmC, stg, (int32_t)(ncol0 + 64 * c), (int32_t)mrow);
+          tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
           bulk_commit();
         }
       }
@@ -328,54 +425,86 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (CL == 2) cluster_sync();  // no multicast or remote arrive targets an exited CTA
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <bool MX, int BN>
+template <bool MX, int BN, int CL>
 int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC0,
-               const CUtensorMap& tC1, GemmParams& p, cudaStream_t stream) {
+               const CUtensorMap& tC1, const CUtensorMap& tSFB, GemmParams& p, cudaStream_t stream) {
   using C = Cfg<MX, BN>;
   p.n_tiles = (p.N + BN - 1) / BN;
-  p.tiles = p.m_tiles * p.n_tiles * (g.mode == GEMM_GROUP_K ? g.E : 1);
-  if (p.tiles == 0) return MX_OK;
-  const int grid = (int)std::min<int64_t>(p.tiles, num_sms());
-  auto k = gemm_kernel<MX, BN>;
+  p.m_pairs = (p.m_tiles + 1) / 2;
+  const int64_t experts = g.mode == GEMM_GROUP_K ? g.E : 1;
+  int64_t units;
+  if (CL == 1) units = p.m_tiles * p.n_tiles * experts;
+  else if (g.mode == GEMM_GROUP_M) units = (p.m_pairs + g.E) * p.n_tiles;  // upper bound; exact count on device
+  else units = p.m_pairs * p.n_tiles * experts;
+  p.tiles = units;
+  if (units == 0) return MX_OK;
+  auto k = gemm_kernel<MX, BN, CL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-  if (e == cudaSuccess) {
-    k<<<grid, GEMM_THREADS, C::SMEM, stream>>>(tA, tB, tC0, tC1, p);
-    e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
+  if (CL == 1) {
+    const int grid = (int)std::min<int64_t>(units, num_sms());
+    k<<<grid, GEMM_THREADS, C::SMEM, stream>>>(tA, tB, tC0, tC1, tSFB, p);
+    return cuda_status(cudaGetLastError(), "gemm_kernel launch");
   }
-  return cuda_status(e, "gemm_kernel launch");
+  const int clusters = (int)std::min<int64_t>(units, num_sms() / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, tA, tB, tC0, tC1, tSFB, p);
+  return cuda_status(e, "gemm_kernel cluster launch");
 }
 
 }  // namespace
 
+#ifndef MX_GEMM_BN
+#define MX_GEMM_BN 256
+#endif
+#ifndef MX_GEMM_CLUSTER
+#define MX_GEMM_CLUSTER 1
+#endif
+
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
-  constexpr int BN = 256;
+  constexpr int BN = MX_GEMM_BN;
+  constexpr int CL = MX_GEMM_CLUSTER;
+  constexpr uint32_t BROWS = CL == 2 ? BN / 2 : BN;  // rows of one B load
   const bool mx = g.mx != 0;
   const int esz = mx ? 1 : 2;
   const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t bk = mx ? 128 : 64;
+  const CUtensorMapSwizzle opswz = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap tA, tB, tC0, tC1;
   int rc;
   {
     uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.M};
     uint64_t strides[1] = {(uint64_t)g.K * esz};
     uint32_t box[2] = {bk, (uint32_t)BM};
-    rc = make_tmap(&tA, dt, 2, const_cast<void*>(g.a), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    rc = make_tmap(&tA, dt, 2, const_cast<void*>(g.a), dims, strides, box, opswz);
     if (rc) return rc;
   }
   if (g.mode == GEMM_GROUP_M) {
     uint64_t dims[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
     uint64_t strides[2] = {(uint64_t)g.K * esz, (uint64_t)g.K * g.N * esz};
-    uint32_t box[3] = {bk, (uint32_t)BN, 1};
-    rc = make_tmap(&tB, dt, 3, const_cast<void*>(g.b), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t box[3] = {bk, BROWS, 1};
+    rc = make_tmap(&tB, dt, 3, const_cast<void*>(g.b), dims, strides, box, opswz);
   } else {
     uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.N};
     uint64_t strides[1] = {(uint64_t)g.K * esz};
-    uint32_t box[2] = {bk, (uint32_t)BN};
-    rc = make_tmap(&tB, dt, 2, const_cast<void*>(g.b), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t box[2] = {bk, BROWS};
+    rc = make_tmap(&tB, dt, 2, const_cast<void*>(g.b), dims, strides, box, opswz);
   }
   if (rc) return rc;
   // output maps
@@ -385,15 +514,15 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   {
     uint64_t dims[2] = {(uint64_t)g.N, (uint64_t)(rows0 * experts)};
     uint64_t strides[1] = {(uint64_t)g.N * 2};
-    uint32_t box[2] = {64, 32};
-    rc = make_tmap(&tC0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.c0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t box[2] = {32, 32};
+    rc = make_tmap(&tC0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.c0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc) return rc;
   }
   if (g.split > 0) {
     uint64_t dims[2] = {(uint64_t)g.N, (uint64_t)(rows1 * experts)};
     uint64_t strides[1] = {(uint64_t)g.N * 2};
-    uint32_t box[2] = {64, 32};
-    rc = make_tmap(&tC1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.c1, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    uint32_t box[2] = {32, 32};
+    rc = make_tmap(&tC1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.c1, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc) return rc;
   } else {
     tC1 = tC0;
@@ -410,8 +539,30 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   p.split = g.split;
   p.msub = g.split > 0 ? g.split : g.M;
   p.err = g.err;
-  if (mx) return launch_cfg<true, BN>(g, tA, tB, tC0, tC1, p, stream);
-  return launch_cfg<false, BN>(g, tA, tB, tC0, tC1, p, stream);
+  // B scales viewed as 32-bit words: one 512-byte tile = 128 words; tile
+  // (row rb, column cb) of a [R, S] scale matrix at word (rb*ceil(S/4) + cb)*128.
+  // Box: one column tile of each of the BN/128 tile rows.
+  CUtensorMap tSFB = tB;
+  if (mx) {
+    const uint64_t col_tiles = (uint64_t)(g.K / 128);
+    const uint64_t tile_rows = (uint64_t)(g.N / 128);
+    if (g.mode == GEMM_GROUP_M) {
+      uint64_t dims[4] = {128, col_tiles, tile_rows, (uint64_t)g.E};
+      uint64_t strides[3] = {512, col_tiles * 512, col_tiles * 512 * tile_rows};
+      uint32_t box[4] = {128, 1, (uint32_t)(BN / 128), 1};
+      rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(g.sfb), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      uint64_t dims[3] = {128, col_tiles, tile_rows};
+      uint64_t strides[2] = {512, col_tiles * 512};
+      uint32_t box[3] = {128, 1, (uint32_t)(BN / 128)};
+      rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(g.sfb), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (rc) return rc;
+  }
+  if (mx) return launch_cfg<true, BN, CL>(g, tA, tB, tC0, tC1, tSFB, p, stream);
+  return launch_cfg<false, BN, CL>(g, tA, tB, tC0, tC1, tSFB, p, stream);
 }
 
 }  // namespace mx
