@@ -297,33 +297,39 @@ MX_DEVINL uint32_t dg_bits_from(float dyf, float g, float u, const SigFast& f) {
 
 // ------------------------------------------------------------------ kernels
 //
-// Both kernels stream tiles through a 2-stage TMA ring (one producer warp,
-// eight consumer warps, two CTAs per SM) and work on each tile in three
-// phases separated by named barriers:
-//   A  every element through the fp32 fast path; results (bf16) into a
-//      shared-memory tile; elements whose rounding the fast path cannot
-//      certify are queued (their tile index) in shared memory
-//   B  the queued elements, spread over all consumer threads, recomputed by
-//      the exact tiers and patched into the tile
-//   C  warps 0-3 quantize columns (two adjacent columns per thread), warps
-//      4-7 quantize rows, both reading the tile
-// The result tiles are double-buffered, so phase C of one tile overlaps
-// phase A of the next without a third barrier.  The queue counter is
-// double-buffered by tile parity for the same reason.
+// Both kernels stream tiles through a 2-stage TMA ring and run three roles:
+//   producer warp  TMA loads of the input tiles
+//   8 consumer     phase A: every element through the fp32 fast path into a
+//   warps          shared-memory result tile; elements whose rounding the
+//                  fast path cannot certify are queued.  Phase C: MX
+//                  quantization of the previous (complete) tile, rows on
+//                  warps 4-7 and columns on warps 0-3
+//   fixer warp     phase B: recomputes the queued elements of a tile with
+//                  the exact tiers (32 at a time) and patches the result
+//                  tile, then releases the input stage
+// Per tile, one barrier of consumers + fixer (A done) and one of consumers
+// only (C done).  The long dependency chains of the exact tiers run on the
+// fixer while the consumers quantize the previous tile and start the next,
+// so they stay off the critical path.  Result tiles and queues are double-
+// buffered; a queue that overflows (adversarial inputs) is resolved in
+// place by the consumer that found the element.
 
 constexpr int CW = 8;                    // consumer warps
 constexpr int CT = CW * 32;              // consumer threads
-constexpr int THREADS = CT + 32;
+constexpr int PRODUCER = CW;             // warp index
+constexpr int FIXER = CW + 1;            // warp index
+constexpr int THREADS = (CW + 2) * 32;
+constexpr int QCAP = 1024;               // queued elements per tile buffer
 
-MX_DEVINL void bar_consumers() { named_bar_sync(1, CT); }
+MX_DEVINL void bar_ab() { named_bar_sync(1, CT + 32); }  // consumers + fixer
+MX_DEVINL void bar_c() { named_bar_sync(2, CT); }        // consumers
 
 // ---- forward: tile = 128 rows x 64 y-columns
 constexpr int SF_R = 128, SF_C = 64;
 constexpr int SF_STAGES = 2;
 constexpr int SF_BOX = SF_R * SF_C * 2;       // 16 KB
 constexpr int SF_STAGE_BYTES = 2 * SF_BOX;    // g, u
-constexpr int SF_Q = SF_R * SF_C;             // queue capacity (whole tile)
-constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + SF_Q * 2 + 1024 + 128;
+constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + 2 * QCAP * 2 + 1024 + 128;
 
 struct SwiFwdParams {
   int64_t M, h;
@@ -339,8 +345,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ytile = smem + SF_STAGES * SF_STAGE_BYTES;            // 2 x 16 KB
-  uint16_t* queue = reinterpret_cast<uint16_t*>(ytile + 2 * SF_BOX);
-  uint64_t* full = reinterpret_cast<uint64_t*>(queue + SF_Q);
+  uint16_t* queue = reinterpret_cast<uint16_t*>(ytile + 2 * SF_BOX);   // 2 x QCAP
+  uint64_t* full = reinterpret_cast<uint64_t*>(queue + 2 * QCAP);
   uint64_t* empty = full + SF_STAGES;
   __shared__ int s_qn[2];
   __shared__ long long s_abort;  // first tile index whose wait timed out
@@ -348,14 +354,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
 
   if (tid == 0) {
-    for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CW); }
+    for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     fence_mbar_init();
     s_qn[0] = s_qn[1] = 0;
     s_abort = 0x7FFFFFFFFFFFFFFFll;
   }
   __syncthreads();
 
-  if (warp == CW) {
+  if (warp == PRODUCER) {
     if (lane == 0) {
       prefetch_tmap(&tmh);
       int stage = 0; uint32_t phase = 0;
@@ -372,105 +378,141 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
 
+  if (warp == FIXER) {
+    // ---- phase B for tile t, between its A barrier and the next one
+    int stage = 0, buf = 0;
+    for (int64_t t = blockIdx.x;; t += gridDim.x, buf ^= 1) {
+      const bool have = t < n_tiles;
+      bar_ab();
+      if (!have || s_abort <= t) break;
+      const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
+      const uint8_t* ut = gt + SF_BOX;
+      uint8_t* yt = ytile + buf * SF_BOX;
+      const uint16_t* q = queue + buf * QCAP;
+      const int n = min(s_qn[buf], QCAP);
+      for (int i = lane; i < n; i += 32) {
+        const int idx = q[i];
+        const int off = (idx / SF_C) * 128 + (idx % SF_C) * 2;
+        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off));
+        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off));
+        const float a = bf16_lo(silu_bits_slow(g));
+        *reinterpret_cast<uint16_t*>(yt + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
+      }
+      __syncwarp();
+      if (lane == 0) {
+        s_qn[buf] = 0;
+        mbar_arrive(&empty[stage]);   // inputs of tile t no longer needed
+      }
+      if (++stage == SF_STAGES) stage = 0;
+    }
+    return;
+  }
+
+  // ---- consumers
   int stage = 0; uint32_t phase = 0; int buf = 0;
   const int seg = lane & 7;
-  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, buf ^= 1) {
-    const int64_t rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
-    const int64_t r0 = rt * SF_R, c0 = ct * SF_C;
-    const bool ok = mbar_wait(&full[stage], phase, p.err);
-    if (!ok) atomicMin(&s_abort, (long long)t);
-    const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
-    const uint8_t* ut = gt + SF_BOX;
-    uint8_t* yt = ytile + buf * SF_BOX;
-    int* qn = &s_qn[buf];
-    // ---- phase A
-    if (ok) {
+  int64_t t_prev = -1;
+  for (int64_t t = blockIdx.x;; t += gridDim.x, buf ^= 1) {
+    const bool have = t < n_tiles;
+    if (have) {
+      const bool ok = mbar_wait(&full[stage], phase, p.err);
+      if (!ok) atomicMin(&s_abort, (long long)t);
+      const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
+      const uint8_t* ut = gt + SF_BOX;
+      uint8_t* yt = ytile + buf * SF_BOX;
+      uint16_t* q = queue + buf * QCAP;
+      // ---- phase A
+      if (ok) {
 #pragma unroll 1
-      for (int it = 0; it < SF_R / (4 * CW); ++it) {
-        const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
-        const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
-        const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
-        const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
-        const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-        uint32_t yp[4];
-        uint32_t slow = 0;
+        for (int it = 0; it < SF_R / (4 * CW); ++it) {
+          const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
+          const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
+          const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
+          const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
+          const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
+          uint32_t yp[4];
+          uint32_t slow = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float g0 = bf16_lo(gp[i]), g1 = bf16_hi(gp[i]);
-          const SigFast f0 = sig_fast(g0), f1 = sig_fast(g1);
-          const float p0 = __fmul_rn(g0, f0.s), p1 = __fmul_rn(g1, f1.s);
-          slow |= (f0.ok && clear_of_midpoint(p0, 16) ? 0u : 1u) << (2 * i);
-          slow |= (f1.ok && clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
-          const __nv_bfloat162 a2 = __floats2bfloat162_rn(p0, p1);
-          const float2 af = __bfloat1622float2(a2);
-          const __nv_bfloat162 y2 = __floats2bfloat162_rn(__fmul_rn(af.x, bf16_lo(up[i])),
-                                                          __fmul_rn(af.y, bf16_hi(up[i])));
-          yp[i] = *reinterpret_cast<const uint32_t*>(&y2);
-        }
-        *reinterpret_cast<uint4*>(yt + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
-        while (slow) {
-          const int j = __ffs(slow) - 1;
-          slow &= slow - 1;
-          queue[atomicAdd(qn, 1)] = (uint16_t)(rr * SF_C + seg * 8 + j);
+          for (int i = 0; i < 4; ++i) {
+            const float g0 = bf16_lo(gp[i]), g1 = bf16_hi(gp[i]);
+            const SigFast f0 = sig_fast(g0), f1 = sig_fast(g1);
+            const float p0 = __fmul_rn(g0, f0.s), p1 = __fmul_rn(g1, f1.s);
+            slow |= (f0.ok && clear_of_midpoint(p0, 16) ? 0u : 1u) << (2 * i);
+            slow |= (f1.ok && clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
+            const __nv_bfloat162 a2 = __floats2bfloat162_rn(p0, p1);
+            const float2 af = __bfloat1622float2(a2);
+            const __nv_bfloat162 y2 = __floats2bfloat162_rn(__fmul_rn(af.x, bf16_lo(up[i])),
+                                                            __fmul_rn(af.y, bf16_hi(up[i])));
+            yp[i] = *reinterpret_cast<const uint32_t*>(&y2);
+          }
+          while (slow) {
+            const int j = __ffs(slow) - 1;
+            slow &= slow - 1;
+            const int slot = atomicAdd(&s_qn[buf], 1);
+            if (slot < QCAP) {
+              q[slot] = (uint16_t)(rr * SF_C + seg * 8 + j);
+            } else {  // queue full: resolve here
+              const uint32_t gw = gp[j >> 1], uw = up[j >> 1];
+              const float g = (j & 1) ? bf16_hi(gw) : bf16_lo(gw);
+              const float u = (j & 1) ? bf16_hi(uw) : bf16_lo(uw);
+              const uint32_t y = f32_to_bf16_bits(__fmul_rn(bf16_lo(silu_bits_slow(g)), u));
+              uint32_t& w = yp[j >> 1];
+              w = (j & 1) ? ((w & 0xFFFFu) | (y << 16)) : ((w & 0xFFFF0000u) | y);
+            }
+          }
+          *reinterpret_cast<uint4*>(yt + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
         }
       }
+      if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
     }
-    bar_consumers();
-    if (tid == 0) s_qn[buf ^ 1] = 0;
-    // ---- phase B
-    if (ok) {
-      const int n = *qn;
-      for (int i = tid; i < n; i += CT) {
-        const int idx = queue[i];
-        const int rr = idx / SF_C, cc = idx % SF_C;
-        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + rr * 128 + cc * 2));
-        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + rr * 128 + cc * 2));
-        const float a = bf16_lo(silu_bits_slow(g));
-        *reinterpret_cast<uint16_t*>(yt + rr * 128 + cc * 2) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
-      }
-    }
-    bar_consumers();
-    if (ok && lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
-    if (s_abort <= t) break;
-    // ---- phase C
-    if (warp >= 4 || !COL) {
-      // rows: 8 lanes per 64-column row; 4 rows per warp step
-      const int w = COL ? warp - 4 : warp;
-      const int nw = COL ? 4 : CW;
-      for (int rr = w * 4 + (lane >> 3); rr < SF_R; rr += nw * 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(yt + rr * 128 + seg * 16);
-        const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
-        uint32_t sc;
-        const uint2 codes = quant_row8(pk, sc);
-        const int64_t r = r0 + rr;
-        const int64_t c = c0 + seg * 8;
-        if (r < p.M) {
-          *reinterpret_cast<uint2*>(p.q_row + r * p.h + c) = codes;
-          if ((seg & 3) == 0) p.s_row.put(r, c >> 5, sc);
+    bar_ab();
+    if (s_abort <= (have ? t : t_prev)) break;
+    // ---- phase C of the previous tile (complete: the fixer patched it
+    // before this barrier)
+    if (t_prev >= 0) {
+      const int pb = buf ^ 1;
+      const uint8_t* yt = ytile + pb * SF_BOX;
+      const int64_t rt = t_prev / p.col_tiles, ct = t_prev - rt * p.col_tiles;
+      const int64_t r0 = rt * SF_R, c0 = ct * SF_C;
+      if (warp >= 4 || !COL) {
+        const int w = COL ? warp - 4 : warp;
+        const int nw = COL ? 4 : CW;
+        for (int rr = w * 4 + (lane >> 3); rr < SF_R; rr += nw * 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(yt + rr * 128 + seg * 16);
+          const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
+          uint32_t sc;
+          const uint2 codes = quant_row8(pk, sc);
+          const int64_t r = r0 + rr;
+          const int64_t c = c0 + seg * 8;
+          if (r < p.M) {
+            *reinterpret_cast<uint2*>(p.q_row + r * p.h + c) = codes;
+            if ((seg & 3) == 0) p.s_row.put(r, c >> 5, sc);
+          }
         }
-      }
-    } else {
-      // columns: 32 column pairs x 4 row blocks = 128 items on warps 0-3
-      const int item = warp * 32 + lane;
-      const int pc = item & 31, rb = item >> 5;
-      uint32_t v[32];
+      } else {
+        const int item = warp * 32 + lane;
+        const int pc = item & 31, rb = item >> 5;
+        uint32_t v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(yt + (rb * 32 + i) * 128 + pc * 4);
-      uint32_t ca[8], cb[8], sa, sb;
-      quant_col32x2(v, ca, cb, sa, sb);
-      const int64_t rg = r0 + rb * 32;
-      if (rg < p.M) {
-        const int64_t col = c0 + 2 * pc;
-        uint8_t* dst = p.q_col + col * p.M + rg;
-        store16(dst, ca[0], ca[1], ca[2], ca[3]);
-        store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
-        store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
-        store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
-        p.s_col.put(col, rg >> 5, sa);
-        p.s_col.put(col + 1, rg >> 5, sb);
+        for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(yt + (rb * 32 + i) * 128 + pc * 4);
+        uint32_t ca[8], cb[8], sa, sb;
+        quant_col32x2(v, ca, cb, sa, sb);
+        const int64_t rg = r0 + rb * 32;
+        if (rg < p.M) {
+          const int64_t col = c0 + 2 * pc;
+          uint8_t* dst = p.q_col + col * p.M + rg;
+          store16(dst, ca[0], ca[1], ca[2], ca[3]);
+          store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
+          store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
+          store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
+          p.s_col.put(col, rg >> 5, sa);
+          p.s_col.put(col + 1, rg >> 5, sb);
+        }
       }
     }
+    if (!have) break;
+    bar_c();   // the previous tile's buffers are free for the next phase A
+    t_prev = t;
   }
 }
 
@@ -479,8 +521,7 @@ constexpr int SB_R = 64, SB_C = 64;
 constexpr int SB_STAGES = 2;
 constexpr int SB_BOX = SB_R * SB_C * 2;       // 8 KB
 constexpr int SB_STAGE_BYTES = 3 * SB_BOX;    // dy, g, u
-constexpr int SB_Q = SB_R * SB_C;
-constexpr size_t SB_SMEM = SB_STAGES * SB_STAGE_BYTES + 2 * 3 * SB_BOX + SB_Q * 2 + 1024 + 128;
+constexpr size_t SB_SMEM = SB_STAGES * SB_STAGE_BYTES + 2 * 3 * SB_BOX + 2 * QCAP * 2 + 1024 + 128;
 
 struct SwiBwdParams {
   int64_t M, h;
@@ -492,6 +533,16 @@ struct SwiBwdParams {
   int32_t* err;
 };
 
+// exact dg, du (and y) of one element, written into the result tile
+template <int MODE>
+MX_DEVINL void bwd_exact(float dyf, float g, float u, uint8_t* ot, int off) {
+  const SigFast sf = sig_fast(g);
+  const float a = bf16_lo(silu_bits_from(g, sf));
+  *reinterpret_cast<uint16_t*>(ot + off) = (uint16_t)dg_bits_from(dyf, g, u, sf);
+  *reinterpret_cast<uint16_t*>(ot + SB_BOX + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(dyf, a));
+  if (MODE == 2) *reinterpret_cast<uint16_t*>(ot + 2 * SB_BOX + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
+}
+
 // MODE 0: rowwise only; 1: rowwise + columnwise MX; 2: rowwise + bf16 transposed
 // dh13 and y.
 template <int MODE>
@@ -502,7 +553,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* otile = smem + SB_STAGES * SB_STAGE_BYTES;  // 2 buffers x {dg, du, y}
   uint16_t* queue = reinterpret_cast<uint16_t*>(otile + 2 * 3 * SB_BOX);
-  uint64_t* full = reinterpret_cast<uint64_t*>(queue + SB_Q);
+  uint64_t* full = reinterpret_cast<uint64_t*>(queue + 2 * QCAP);
   uint64_t* empty = full + SB_STAGES;
   __shared__ int s_qn[2];
   __shared__ long long s_abort;
@@ -510,14 +561,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
 
   if (tid == 0) {
-    for (int s = 0; s < SB_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CW); }
+    for (int s = 0; s < SB_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     fence_mbar_init();
     s_qn[0] = s_qn[1] = 0;
     s_abort = 0x7FFFFFFFFFFFFFFFll;
   }
   __syncthreads();
 
-  if (warp == CW) {
+  if (warp == PRODUCER) {
     if (lane == 0) {
       prefetch_tmap(&tmdy);
       prefetch_tmap(&tmh);
@@ -537,174 +588,203 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
 
-  int stage = 0; uint32_t phase = 0; int buf = 0;
-  const int seg = lane & 7;
-  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, buf ^= 1) {
-    const int64_t rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
-    const int64_t r0 = rt * SB_R, c0 = ct * SB_C;
-    const bool ok = mbar_wait(&full[stage], phase, p.err);
-    if (!ok) atomicMin(&s_abort, (long long)t);
-    const uint8_t* dyt = smem + stage * SB_STAGE_BYTES;
-    const uint8_t* gt = dyt + SB_BOX;
-    const uint8_t* ut = dyt + 2 * SB_BOX;
-    uint8_t* ot = otile + buf * 3 * SB_BOX;   // dg | du | y
-    int* qn = &s_qn[buf];
-    // ---- phase A
-    if (ok) {
-#pragma unroll 1
-      for (int it = 0; it < SB_R / (4 * CW); ++it) {
-        const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
-        const uint4 dv = *reinterpret_cast<const uint4*>(dyt + rr * 128 + seg * 16);
-        const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
-        const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
-        const uint32_t dp[4] = {dv.x, dv.y, dv.z, dv.w};
-        const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
-        const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-        uint32_t dgp[4], dup[4], yp[4];
-        uint32_t slow = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t dgw = 0;
-          float pa[2], dyv[2], uvv[2];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float dyf = hh ? bf16_hi(dp[i]) : bf16_lo(dp[i]);
-            const float g = hh ? bf16_hi(gp[i]) : bf16_lo(gp[i]);
-            const float u = hh ? bf16_hi(up[i]) : bf16_lo(up[i]);
-            const SigFast sf = sig_fast(g);
-            pa[hh] = __fmul_rn(g, sf.s);
-            dyv[hh] = dyf;
-            uvv[hh] = u;
-            bool ok_e = sf.ok && clear_of_midpoint(pa[hh], 16);
-            // dg tier 1 (see dg_bits_from)
-            const float dyu = __fmul_rn(dyf, u);
-            const float oms = __fmul_rn(sf.t, sf.s);
-            const float go = __fmul_rn(g, oms);
-            const float inner = __fadd_rn(1.0f, go);
-            const float pg = __fmul_rn(dyu, __fmul_rn(sf.s, inner));
-            const float ratio = fabsf(go) * rcp_approx(fabsf(inner));
-            const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
-            const float adyu = fabsf(dyu), apg = fabsf(pg);
-            ok_e = ok_e && margin < 16384.0f && adyu >= 0x1p-100f && adyu <= 0x1p100f && apg >= 0x1p-100f &&
-                   clear_of_midpoint(pg, (uint32_t)margin);
-            slow |= (ok_e ? 0u : 1u) << (2 * i + hh);
-            dgw |= f32_to_bf16_bits(pg) << (16 * hh);
-          }
-          const __nv_bfloat162 a2 = __floats2bfloat162_rn(pa[0], pa[1]);
-          const float2 af = __bfloat1622float2(a2);
-          const __nv_bfloat162 du2 = __floats2bfloat162_rn(__fmul_rn(dyv[0], af.x), __fmul_rn(dyv[1], af.y));
-          dup[i] = *reinterpret_cast<const uint32_t*>(&du2);
-          dgp[i] = dgw;
-          if (MODE == 2) {
-            const __nv_bfloat162 y2 = __floats2bfloat162_rn(__fmul_rn(af.x, uvv[0]), __fmul_rn(af.y, uvv[1]));
-            yp[i] = *reinterpret_cast<const uint32_t*>(&y2);
-          }
-        }
-        *reinterpret_cast<uint4*>(ot + rr * 128 + seg * 16) = make_uint4(dgp[0], dgp[1], dgp[2], dgp[3]);
-        *reinterpret_cast<uint4*>(ot + SB_BOX + rr * 128 + seg * 16) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
-        if (MODE == 2)
-          *reinterpret_cast<uint4*>(ot + 2 * SB_BOX + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
-        while (slow) {
-          const int j = __ffs(slow) - 1;
-          slow &= slow - 1;
-          queue[atomicAdd(qn, 1)] = (uint16_t)(rr * SB_C + seg * 8 + j);
-        }
-      }
-    }
-    bar_consumers();
-    if (tid == 0) s_qn[buf ^ 1] = 0;
-    // ---- phase B: exact tiers for the queued elements
-    if (ok) {
-      const int n = *qn;
-      for (int i = tid; i < n; i += CT) {
-        const int idx = queue[i];
+  if (warp == FIXER) {
+    int stage = 0, buf = 0;
+    for (int64_t t = blockIdx.x;; t += gridDim.x, buf ^= 1) {
+      const bool have = t < n_tiles;
+      bar_ab();
+      if (!have || s_abort <= t) break;
+      const uint8_t* dyt = smem + stage * SB_STAGE_BYTES;
+      uint8_t* ot = otile + buf * 3 * SB_BOX;
+      const uint16_t* q = queue + buf * QCAP;
+      const int n = min(s_qn[buf], QCAP);
+      for (int i = lane; i < n; i += 32) {
+        const int idx = q[i];
         const int off = (idx / SB_C) * 128 + (idx % SB_C) * 2;
         const float dyf = bf16_lo(*reinterpret_cast<const uint16_t*>(dyt + off));
-        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off));
-        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off));
-        const SigFast sf = sig_fast(g);
-        const float a = bf16_lo(silu_bits_from(g, sf));
-        *reinterpret_cast<uint16_t*>(ot + off) = (uint16_t)dg_bits_from(dyf, g, u, sf);
-        *reinterpret_cast<uint16_t*>(ot + SB_BOX + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(dyf, a));
-        if (MODE == 2) *reinterpret_cast<uint16_t*>(ot + 2 * SB_BOX + off) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
+        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(dyt + SB_BOX + off));
+        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(dyt + 2 * SB_BOX + off));
+        bwd_exact<MODE>(dyf, g, u, ot, off);
       }
+      __syncwarp();
+      if (lane == 0) {
+        s_qn[buf] = 0;
+        mbar_arrive(&empty[stage]);
+      }
+      if (++stage == SB_STAGES) stage = 0;
     }
-    bar_consumers();
-    if (ok && lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == SB_STAGES) { stage = 0; phase ^= 1; }
-    if (s_abort <= t) break;
-    // ---- phase C
-    if (warp >= 4 || MODE == 0) {
-      // rows of dg and du: 8 lanes per 64-column row; 4 rows per warp step
-      const int w = MODE == 0 ? warp : warp - 4;
-      const int nw = MODE == 0 ? CW : 4;
-      for (int k = w * 4 + (lane >> 3); k < 2 * SB_R; k += nw * 4) {
-        const int which = k / SB_R, rr = k % SB_R;
-        const uint4 v = *reinterpret_cast<const uint4*>(ot + which * SB_BOX + rr * 128 + seg * 16);
-        const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
-        uint32_t sc;
-        const uint2 codes = quant_row8(pk, sc);
-        const int64_t r = r0 + rr;
-        const int64_t c = (which ? p.h : 0) + c0 + seg * 8;
-        if (r < p.M) {
-          *reinterpret_cast<uint2*>(p.q_row + r * 2 * p.h + c) = codes;
-          if ((seg & 3) == 0) p.s_row.put(r, c >> 5, sc);
+    return;
+  }
+
+  int stage = 0; uint32_t phase = 0; int buf = 0;
+  const int seg = lane & 7;
+  int64_t t_prev = -1;
+  for (int64_t t = blockIdx.x;; t += gridDim.x, buf ^= 1) {
+    const bool have = t < n_tiles;
+    if (have) {
+      const bool ok = mbar_wait(&full[stage], phase, p.err);
+      if (!ok) atomicMin(&s_abort, (long long)t);
+      const uint8_t* dyt = smem + stage * SB_STAGE_BYTES;
+      const uint8_t* gt = dyt + SB_BOX;
+      const uint8_t* ut = dyt + 2 * SB_BOX;
+      uint8_t* ot = otile + buf * 3 * SB_BOX;   // dg | du | y
+      uint16_t* q = queue + buf * QCAP;
+      // ---- phase A
+      if (ok) {
+#pragma unroll 1
+        for (int it = 0; it < SB_R / (4 * CW); ++it) {
+          const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
+          const uint4 dv = *reinterpret_cast<const uint4*>(dyt + rr * 128 + seg * 16);
+          const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
+          const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
+          const uint32_t dp[4] = {dv.x, dv.y, dv.z, dv.w};
+          const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
+          const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
+          uint32_t dgp[4], dup[4], yp[4];
+          uint32_t slow = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t dgw = 0;
+            float pa[2], dyv[2], uvv[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float dyf = hh ? bf16_hi(dp[i]) : bf16_lo(dp[i]);
+              const float g = hh ? bf16_hi(gp[i]) : bf16_lo(gp[i]);
+              const float u = hh ? bf16_hi(up[i]) : bf16_lo(up[i]);
+              const SigFast sf = sig_fast(g);
+              pa[hh] = __fmul_rn(g, sf.s);
+              dyv[hh] = dyf;
+              uvv[hh] = u;
+              bool ok_e = sf.ok && clear_of_midpoint(pa[hh], 16);
+              // dg tier 1 (see dg_bits_from)
+              const float dyu = __fmul_rn(dyf, u);
+              const float oms = __fmul_rn(sf.t, sf.s);
+              const float go = __fmul_rn(g, oms);
+              const float inner = __fadd_rn(1.0f, go);
+              const float pg = __fmul_rn(dyu, __fmul_rn(sf.s, inner));
+              const float ratio = fabsf(go) * rcp_approx(fabsf(inner));
+              const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
+              const float adyu = fabsf(dyu), apg = fabsf(pg);
+              ok_e = ok_e && margin < 16384.0f && adyu >= 0x1p-100f && adyu <= 0x1p100f && apg >= 0x1p-100f &&
+                     clear_of_midpoint(pg, (uint32_t)margin);
+              slow |= (ok_e ? 0u : 1u) << (2 * i + hh);
+              dgw |= f32_to_bf16_bits(pg) << (16 * hh);
+            }
+            const __nv_bfloat162 a2 = __floats2bfloat162_rn(pa[0], pa[1]);
+            const float2 af = __bfloat1622float2(a2);
+            const __nv_bfloat162 du2 = __floats2bfloat162_rn(__fmul_rn(dyv[0], af.x), __fmul_rn(dyv[1], af.y));
+            dup[i] = *reinterpret_cast<const uint32_t*>(&du2);
+            dgp[i] = dgw;
+            if (MODE == 2) {
+              const __nv_bfloat162 y2 = __floats2bfloat162_rn(__fmul_rn(af.x, uvv[0]), __fmul_rn(af.y, uvv[1]));
+              yp[i] = *reinterpret_cast<const uint32_t*>(&y2);
+            }
+          }
+          *reinterpret_cast<uint4*>(ot + rr * 128 + seg * 16) = make_uint4(dgp[0], dgp[1], dgp[2], dgp[3]);
+          *reinterpret_cast<uint4*>(ot + SB_BOX + rr * 128 + seg * 16) = make_uint4(dup[0], dup[1], dup[2], dup[3]);
+          if (MODE == 2)
+            *reinterpret_cast<uint4*>(ot + 2 * SB_BOX + rr * 128 + seg * 16) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
+          while (slow) {
+            const int j = __ffs(slow) - 1;
+            slow &= slow - 1;
+            const int slot = atomicAdd(&s_qn[buf], 1);
+            const int idx = rr * SB_C + seg * 8 + j;
+            if (slot < QCAP) {
+              q[slot] = (uint16_t)idx;
+            } else {  // queue full: resolve here (after this thread's own stores above)
+              const int off = rr * 128 + (seg * 8 + j) * 2;
+              bwd_exact<MODE>(bf16_lo(*reinterpret_cast<const uint16_t*>(dyt + off)),
+                              bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off)),
+                              bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off)), ot, off);
+            }
+          }
         }
       }
-    } else if (MODE == 1) {
-      // columns of dg, du: 64 column pairs x 2 row blocks = 128 items on warps 0-3
-      const int item = warp * 32 + lane;
-      const int pcx = item & 63, rb = item >> 6;
-      const int which = pcx >> 5, pc = pcx & 31;
-      const uint8_t* src = ot + which * SB_BOX;
-      uint32_t v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + i) * 128 + pc * 4);
-      uint32_t ca[8], cb[8], sa, sb;
-      quant_col32x2(v, ca, cb, sa, sb);
-      const int64_t rg = r0 + rb * 32;
-      if (rg < p.M) {
-        const int64_t orow = (which ? p.h : 0) + c0 + 2 * pc;
-        uint8_t* dst = p.q_col + orow * p.M + rg;
-        store16(dst, ca[0], ca[1], ca[2], ca[3]);
-        store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
-        store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
-        store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
-        p.s_col.put(orow, rg >> 5, sa);
-        p.s_col.put(orow + 1, rg >> 5, sb);
-      }
-    } else {
-      // bf16 transposed dg, du (into dh13_t) and y (into y_t): 96 column
-      // pairs x 2 blocks of 32 rows = 192 items on warps 0-3
-      for (int item = warp * 32 + lane; item < 192; item += 128) {
-        const int pcx = item % 96, rb = item / 96;
-        const int which = pcx / 32, pc = pcx % 32;
+      if (++stage == SB_STAGES) { stage = 0; phase ^= 1; }
+    }
+    bar_ab();
+    if (s_abort <= (have ? t : t_prev)) break;
+    // ---- phase C of the previous tile
+    if (t_prev >= 0) {
+      const int pb = buf ^ 1;
+      const uint8_t* ot = otile + pb * 3 * SB_BOX;
+      const int64_t rt = t_prev / p.col_tiles, ct = t_prev - rt * p.col_tiles;
+      const int64_t r0 = rt * SB_R, c0 = ct * SB_C;
+      if (warp >= 4 || MODE == 0) {
+        // rows of dg and du: 8 lanes per 64-column row; 4 rows per warp step
+        const int w = MODE == 0 ? warp : warp - 4;
+        const int nw = MODE == 0 ? CW : 4;
+        for (int k = w * 4 + (lane >> 3); k < 2 * SB_R; k += nw * 4) {
+          const int which = k / SB_R, rr = k % SB_R;
+          const uint4 v = *reinterpret_cast<const uint4*>(ot + which * SB_BOX + rr * 128 + seg * 16);
+          const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
+          uint32_t sc;
+          const uint2 codes = quant_row8(pk, sc);
+          const int64_t r = r0 + rr;
+          const int64_t c = (which ? p.h : 0) + c0 + seg * 8;
+          if (r < p.M) {
+            *reinterpret_cast<uint2*>(p.q_row + r * 2 * p.h + c) = codes;
+            if ((seg & 3) == 0) p.s_row.put(r, c >> 5, sc);
+          }
+        }
+      } else if (MODE == 1) {
+        // columns of dg, du: 64 column pairs x 2 row blocks = 128 items on warps 0-3
+        const int item = warp * 32 + lane;
+        const int pcx = item & 63, rb = item >> 6;
+        const int which = pcx >> 5, pc = pcx & 31;
         const uint8_t* src = ot + which * SB_BOX;
-        uint32_t wa[16], wb[16];
+        uint32_t v[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t r0v = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + 2 * i) * 128 + pc * 4);
-          const uint32_t r1v = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + 2 * i + 1) * 128 + pc * 4);
-          wa[i] = (r0v & 0xFFFFu) | (r1v << 16);
-          wb[i] = (r0v >> 16) | (r1v & 0xFFFF0000u);
-        }
+        for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + i) * 128 + pc * 4);
+        uint32_t ca[8], cb[8], sa, sb;
+        quant_col32x2(v, ca, cb, sa, sb);
         const int64_t rg = r0 + rb * 32;
         if (rg < p.M) {
-          const int64_t col = c0 + 2 * pc;
-          uint16_t* base = which == 2 ? p.y_t : p.dh13_t;
-          if (base) {
-            const int64_t orow = (which == 1 ? p.h : 0) + col;
-            uint16_t* da = base + orow * p.M + rg;
-            uint16_t* db = da + p.M;
+          const int64_t orow = (which ? p.h : 0) + c0 + 2 * pc;
+          uint8_t* dst = p.q_col + orow * p.M + rg;
+          store16(dst, ca[0], ca[1], ca[2], ca[3]);
+          store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
+          store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
+          store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
+          p.s_col.put(orow, rg >> 5, sa);
+          p.s_col.put(orow + 1, rg >> 5, sb);
+        }
+      } else {
+        // bf16 transposed dg, du (into dh13_t) and y (into y_t): 96 column
+        // pairs x 2 blocks of 32 rows = 192 items on warps 0-3
+        for (int item = warp * 32 + lane; item < 192; item += 128) {
+          const int pcx = item % 96, rb = item / 96;
+          const int which = pcx / 32, pc = pcx % 32;
+          const uint8_t* src = ot + which * SB_BOX;
+          uint32_t wa[16], wb[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              store16(da + q * 8, wa[4 * q], wa[4 * q + 1], wa[4 * q + 2], wa[4 * q + 3]);
-              store16(db + q * 8, wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t r0v = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + 2 * i) * 128 + pc * 4);
+            const uint32_t r1v = *reinterpret_cast<const uint32_t*>(src + (rb * 32 + 2 * i + 1) * 128 + pc * 4);
+            wa[i] = (r0v & 0xFFFFu) | (r1v << 16);
+            wb[i] = (r0v >> 16) | (r1v & 0xFFFF0000u);
+          }
+          const int64_t rg = r0 + rb * 32;
+          if (rg < p.M) {
+            const int64_t col = c0 + 2 * pc;
+            uint16_t* base = which == 2 ? p.y_t : p.dh13_t;
+            if (base) {
+              const int64_t orow = (which == 1 ? p.h : 0) + col;
+              uint16_t* da = base + orow * p.M + rg;
+              uint16_t* db = da + p.M;
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                store16(da + q4 * 8, wa[4 * q4], wa[4 * q4 + 1], wa[4 * q4 + 2], wa[4 * q4 + 3]);
+                store16(db + q4 * 8, wb[4 * q4], wb[4 * q4 + 1], wb[4 * q4 + 2], wb[4 * q4 + 3]);
+              }
             }
           }
         }
       }
     }
+    if (!have) break;
+    bar_c();
+    t_prev = t;
   }
 }
 
