@@ -29,15 +29,20 @@ constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each draining half o
 constexpr int GEMM_THREADS = 64 + EPI_WARPS * 32;
 constexpr int MAX_GROUPS = 1024;
 
-template <bool MX, int BN>
+// SUB: 128-row sub-tiles per tile sharing each B stage (2 only for bf16, whose
+// two 128x256 fp32 accumulators then fill TMEM; MXFP8 needs TMEM columns for
+// its scales).
+template <bool MX, int BN, int SUB = 1>
 struct Cfg {
+  static_assert(SUB == 1 || (!MX && BN == 256), "two sub-tiles only for the bf16 kernel");
+  static constexpr int TM = SUB * BM;                      // tile rows
   static constexpr int BK = MX ? 128 : 64;                 // elements per stage (128 bytes of K)
-  static constexpr int A_BYTES = BM * 128;
+  static constexpr int A_BYTES = TM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int SFA_BYTES = MX ? 512 : 0;           // one scale tile of A per stage
   static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr int NUM_ACC = BN == 256 ? 1 : 2;
+  static constexpr int STAGES = SUB == 2 ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int NUM_ACC = (BN == 256 || SUB == 2) ? 1 : 2;
   static constexpr int EPI_BYTES = EPI_WARPS * 32 * 64;    // one 32x32 bf16 buffer per warp
   static constexpr int TMEM_COLS = 512;
   static constexpr int SF_COL = NUM_ACC * BN;               // per-stage scale slots from here
@@ -160,12 +165,13 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
   return ti;
 }
 
-template <bool MX, int BN, int CL>
+template <bool MX, int BN, int CL, int SUB>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                 const __grid_constant__ CUtensorMap tmSFB, GemmParams p) {
-  using C = Cfg<MX, BN>;
+  using C = Cfg<MX, BN, SUB>;
+  static_assert(CL == 1 || SUB == 1, "clusters only with single sub-tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int64_t k = ti.k0 + (int64_t)kb * C::BK;
           const uint32_t bytes = C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? 512 : 0) + C::SFB_BYTES : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * BM), &full[stage]);
+          tma_load_2d(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * C::TM), &full[stage]);
           if (CL == 1) {
             if (p.mode == GEMM_GROUP_M)
               tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
@@ -319,13 +325,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
-            if (MX)
-              mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, C::IDESC | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf_col,
-                       sf_col + 4, accum);
-            else
-              mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, C::IDESC, accum);
+          for (int sub = 0; sub < SUB; ++sub) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+              const uint64_t a = ad + (uint64_t)((sub * BM * 128) >> 4) + 2 * k;
+              if (MX)
+                mma_mxf8(d_tmem, a, bd + 2 * k, C::IDESC | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf_col,
+                         sf_col + 4, accum);
+              else
+                mma_bf16(d_tmem + (uint32_t)(sub * BN), a, bd + 2 * k, C::IDESC, accum);
+            }
           }
           // the stage is free once these MMAs are done; with clusters both
           // CTAs of the pair must release it before either refills it
@@ -353,13 +363,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     int acc = 0; uint32_t acc_phase = 0;
     for (int64_t u = unit0; u < n_units; u += ustep) {
       const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
-      int64_t mrow = ti.m_blk * BM + q * 32;
-      const CUtensorMap* tmC = &tmC0;
-      if (p.split > 0 && mrow >= p.split) { tmC = &tmC1; mrow -= p.split; }
-      if (p.mode == GEMM_GROUP_K) mrow += (int64_t)ti.e * p.msub;
       const int64_t ncol0 = ti.n_blk * BN + half * (BN / 2);
       const int64_t cleft = (p.N - ncol0 + 31) / 32;
       const int nchunks = (int)(cleft < BN / 64 ? (cleft > 0 ? cleft : 0) : BN / 64);
+      // output rows of this warp in sub-tile `sub`, and the map they go to
+      auto out_rows = [&](int sub, const CUtensorMap*& tmC) {
+        int64_t mrow = ti.m_blk * C::TM + sub * BM + q * 32;
+        tmC = &tmC0;
+        if (p.split > 0 && mrow >= p.split) { tmC = &tmC1; mrow -= p.split; }
+        if (p.mode == GEMM_GROUP_K) mrow += (int64_t)ti.e * p.msub;
+        return mrow;
+      };
       if (ti.num_kb == 0) {
         if (!ti.store) continue;
         if (lane == 0) bulk_wait_read<0>();
@@ -370,7 +384,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          for (int c = 0; c < nchunks; ++c) tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
+          for (int sub = 0; sub < SUB; ++sub) {
+            if (ti.m_blk * C::TM + sub * BM >= p.M) break;  // sub-tile past the last row
+            const CUtensorMap* tmC;
+            const int64_t mrow = out_rows(sub, tmC);
+            for (int c = 0; c < nchunks; ++c) tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
+          }
           bulk_commit();
         }
         continue;
@@ -384,37 +403,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
         continue;
       }
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * (BN / 2));
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tbase + c * 32, r);
-        tmem_ld_wait();
-        if (c == BN / 64 - 1) {
-          // accumulator fully read: hand it back to the MMA warp
-          tc_fence_before();
+      for (int sub = 0; sub < SUB; ++sub) {
+        const CUtensorMap* tmC;
+        const int64_t mrow = out_rows(sub, tmC);
+        // a sub-tile past the last row is drained but not stored
+        const int live = ti.m_blk * C::TM + sub * BM < p.M ? nchunks : 0;
+        const uint32_t tbase =
+            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((acc + sub) * BN + half * (BN / 2));
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + c * 32, r);
+          tmem_ld_wait();
+          if (sub == SUB - 1 && c == BN / 64 - 1) {
+            // accumulator fully read: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          if (c >= live) continue;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b2 =
+                __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        }
-        if (c >= nchunks) continue;
-        uint32_t w[16];
+          uint8_t* row = stg + lane * 64;
+          const int sw = (lane >> 1) & 3;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-        uint8_t* row = stg + lane * 64;
-        const int sw = (lane >> 1) & 3;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
-          bulk_commit();
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
+            bulk_commit();
+          }
         }
       }
       if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
@@ -430,10 +459,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <bool MX, int BN, int CL>
+template <bool MX, int BN, int CL, int SUB>
 int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC0,
                const CUtensorMap& tC1, const CUtensorMap& tSFB, GemmParams& p, cudaStream_t stream) {
-  using C = Cfg<MX, BN>;
+  using C = Cfg<MX, BN, SUB>;
+  p.m_tiles = (p.M + C::TM - 1) / C::TM;
   p.n_tiles = (p.N + BN - 1) / BN;
   p.m_pairs = (p.m_tiles + 1) / 2;
   const int64_t experts = g.mode == GEMM_GROUP_K ? g.E : 1;
@@ -443,7 +473,7 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   else units = p.m_pairs * p.n_tiles * experts;
   p.tiles = units;
   if (units == 0) return MX_OK;
-  auto k = gemm_kernel<MX, BN, CL>;
+  auto k = gemm_kernel<MX, BN, CL, SUB>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
   if (CL == 1) {
@@ -491,7 +521,8 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   {
     uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.M};
     uint64_t strides[1] = {(uint64_t)g.K * esz};
-    uint32_t box[2] = {bk, (uint32_t)BM};
+    const bool two_sub = !mx && CL == 1 && BN == 256 && g.mode != GEMM_GROUP_M;
+    uint32_t box[2] = {bk, (uint32_t)(two_sub ? 2 * BM : BM)};
     rc = make_tmap(&tA, dt, 2, const_cast<void*>(g.a), dims, strides, box, opswz);
     if (rc) return rc;
   }
@@ -530,7 +561,6 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   GemmParams p{};
   p.mode = g.mode;
   p.M = g.M; p.N = g.N; p.K = g.K;
-  p.m_tiles = g.M / BM;
   p.E = g.mode == GEMM_DENSE ? 1 : g.E;
   p.offs = g.offs;
   p.sfa = (const uint8_t*)g.sfa;
@@ -561,8 +591,10 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     }
     if (rc) return rc;
   }
-  if (mx) return launch_cfg<true, BN, CL>(g, tA, tB, tC0, tC1, tSFB, p, stream);
-  return launch_cfg<false, BN, CL>(g, tA, tB, tC0, tC1, tSFB, p, stream);
+  if (mx) return launch_cfg<true, BN, CL, 1>(g, tA, tB, tC0, tC1, tSFB, p, stream);
+  if (CL == 1 && BN == 256 && g.mode != GEMM_GROUP_M)
+    return launch_cfg<false, BN, 1, 2>(g, tA, tB, tC0, tC1, tSFB, p, stream);
+  return launch_cfg<false, BN, CL, 1>(g, tA, tB, tC0, tC1, tSFB, p, stream);
 }
 
 }  // namespace mx
