@@ -31,17 +31,20 @@ constexpr int MAX_GROUPS = 1024;
 
 // SUB: 128-row sub-tiles per tile sharing each B stage (2 only for bf16, whose
 // two 128x256 fp32 accumulators then fill TMEM; MXFP8 needs TMEM columns for
-// its scales).
-template <bool MX, int BN, int SUB = 1>
+// its scales).  CL = 2: CTA pairs, each CTA holding its 128 rows of A and
+// half of the B rows, the MMA (M = 256) issued by the even CTA.
+template <bool MX, int BN, int SUB = 1, int CL = 1>
 struct Cfg {
   static_assert(SUB == 1 || (!MX && BN == 256), "two sub-tiles only for the bf16 kernel");
+  static_assert(CL == 1 || SUB == 1, "CTA pairs only with single sub-tiles");
   static constexpr int TM = SUB * BM;                      // tile rows
   static constexpr int BK = MX ? 128 : 64;                 // elements per stage (128 bytes of K)
   static constexpr int A_BYTES = TM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = (BN / CL) * 128;           // this CTA's rows of the B tile
   static constexpr int SFA_BYTES = MX ? 512 : 0;           // one scale tile of A per stage
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
-  static constexpr int STAGES = SUB == 2 ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;  // all of the tile's B scales
+  static constexpr int STAGES = CL == 2 ? 6 : SUB == 2 ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // bytes one CTA loads
   static constexpr int NUM_ACC = (BN == 256 || SUB == 2) ? 1 : 2;
   static constexpr int EPI_BYTES = EPI_WARPS * 32 * 64;    // one 32x32 bf16 buffer per warp
   static constexpr int TMEM_COLS = 512;
@@ -50,8 +53,8 @@ struct Cfg {
   static constexpr size_t SMEM = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES +
                                  MAX_GROUPS * 4 + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr uint32_t IDESC =
-      MX ? ((1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24))
-         : ((1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24));
+      MX ? ((1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24))
+         : ((1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24));
 };
 
 struct GemmParams {
@@ -169,9 +172,9 @@ template <bool MX, int BN, int CL, int SUB>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                const __grid_constant__ CUtensorMap tmSFB, GemmParams p) {
-  using C = Cfg<MX, BN, SUB>;
-  static_assert(CL == 1 || SUB == 1, "clusters only with single sub-tiles");
+                const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                GemmParams p) {
+  using C = Cfg<MX, BN, SUB, CL>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -197,8 +200,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   // ---- setup: barriers, group data, TMEM
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
-    for (int a = 0; a < C::NUM_ACC; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], EPI_WARPS); }
+    // with CTA pairs the even CTA's full and acc_empty barriers serve both
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < C::NUM_ACC; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], CL * EPI_WARPS); }
     mbar_init(done_bar, 1);
     fence_mbar_init();
     s_groups_ok = 1;
@@ -231,8 +235,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, C::TMEM_COLS);
-    tmem_relinquish();
+    if (CL == 2) { tmem_alloc_pair(tmem_holder, C::TMEM_COLS); tmem_relinquish_pair(); }
+    else { tmem_alloc(tmem_holder, C::TMEM_COLS); tmem_relinquish(); }
   }
   tc_fence_before();
   __syncthreads();
@@ -249,6 +253,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       if (MX) prefetch_tmap(&tmSFB);
+      if (MX && CL == 2) prefetch_tmap(&tmSFA);
       int stage = 0; uint32_t phase = 0;
       const int64_t sfa_row_tiles = p.K / 128;  // scale tiles per 128-row block of A
       for (int64_t u = unit0; u < n_units; u += ustep) {
@@ -257,25 +262,40 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.err)) { ok = false; break; }
           const int64_t k = ti.k0 + (int64_t)kb * C::BK;
+          const int64_t kt = k / 128;
+          if (CL == 2) {
+            // both CTAs' copies complete on the even CTA's barrier, which
+            // expects the bytes of the pair; a filler tile's rows and scales
+            // past the end read as zeros
+            const uint32_t bar = cluster_map(smem_u32(&full[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_TX);
+            tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * BM), bar);
+            const int32_t nrow = (int32_t)(ti.n_blk * BN + rank * (BN / 2));
+            if (p.mode == GEMM_GROUP_M)
+              tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, (int32_t)k, nrow, ti.e, bar);
+            else
+              tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, (int32_t)k, nrow, bar);
+            if (MX) {
+              tma_load_2d_pair(sSFA + stage * C::SFA_BYTES, &tmSFA, 0, (int32_t)(ti.m_blk * sfa_row_tiles + kt),
+                               bar);
+              if (p.mode == GEMM_GROUP_M)
+                tma_load_4d_pair(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)),
+                                 ti.e, bar);
+              else
+                tma_load_3d_pair(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)),
+                                 bar);
+            }
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+            continue;
+          }
           const uint32_t bytes = C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? 512 : 0) + C::SFB_BYTES : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * C::TM), &full[stage]);
-          if (CL == 1) {
-            if (p.mode == GEMM_GROUP_M)
-              tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
-            else
-              tma_load_2d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), &full[stage]);
-          } else {
-            // this CTA's half of the B tile, delivered to both CTAs of the pair
-            uint8_t* dst = sB + stage * C::B_BYTES + rank * (C::B_BYTES / 2);
-            const int32_t nrow = (int32_t)(ti.n_blk * BN + rank * (BN / 2));
-            if (p.mode == GEMM_GROUP_M)
-              tma_load_3d_mc(dst, &tmB, (int32_t)k, nrow, ti.e, &full[stage], (uint16_t)0x3);
-            else
-              tma_load_2d_mc(dst, &tmB, (int32_t)k, nrow, &full[stage], (uint16_t)0x3);
-          }
+          if (p.mode == GEMM_GROUP_M)
+            tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
+          else
+            tma_load_2d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), &full[stage]);
           if (MX) {
-            const int64_t kt = k / 128;
             if (ti.store)
               bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, 512,
                         &full[stage]);
@@ -297,8 +317,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Descriptors are formed once and advanced by adding the byte offset
-    // (>> 4) to their start-address field.
-    if (lane == 0) {
+    // (>> 4) to their start-address field.  With CTA pairs only the even CTA
+    // issues; its MMAs and scale copies act on both CTAs.
+    if (lane == 0 && rank == 0) {
       const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
       const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 128, 128, 0);
@@ -317,10 +338,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
           const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT;
           if (MX) {
-            tmem_cp_32x128b_x4(sf_col, sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES) >> 4));
+            const uint64_t sfa = sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES) >> 4);
+            if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col, sfa);
+            else tmem_cp_32x128b_x4(sf_col, sfa);
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tmem_cp_32x128b_x4(sf_col + 4 + 4 * j, sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + j * 512) >> 4));
+            for (int j = 0; j < BN / 128; ++j) {
+              const uint64_t sfb = sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + j * 512) >> 4);
+              if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col + 4 + 4 * j, sfb);
+              else tmem_cp_32x128b_x4(sf_col + 4 + 4 * j, sfb);
+            }
           }
           const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES) >> 4);
@@ -330,25 +356,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int k = 0; k < 4; ++k) {
               const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
               const uint64_t a = ad + (uint64_t)((sub * BM * 128) >> 4) + 2 * k;
-              if (MX)
-                mma_mxf8(d_tmem, a, bd + 2 * k, C::IDESC | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf_col,
-                         sf_col + 4, accum);
+              const uint32_t sf_ids = ((uint32_t)k << 4) | ((uint32_t)k << 29);
+              if (MX && CL == 2)
+                mma_mxf8_pair(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
+              else if (MX)
+                mma_mxf8(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
+              else if (CL == 2)
+                mma_bf16_pair(d_tmem, a, bd + 2 * k, C::IDESC, accum);
               else
                 mma_bf16(d_tmem + (uint32_t)(sub * BN), a, bd + 2 * k, C::IDESC, accum);
             }
           }
-          // the stage is free once these MMAs are done; with clusters both
-          // CTAs of the pair must release it before either refills it
-          if (CL == 2) tc_commit_mc(&empty[stage], (uint16_t)0x3);
+          // the stage is free (in both CTAs of a pair) once these MMAs are done
+          if (CL == 2) tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
           else tc_commit(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
+        if (CL == 2) tc_commit_pair_mc(&acc_full[acc], (uint16_t)0x3);
+        else tc_commit(&acc_full[acc]);
         if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
       }
       // all issued MMAs complete before TMEM is released
-      tc_commit(done_bar);
+      if (CL == 2) tc_commit_pair_mc(done_bar, (uint16_t)0x1);
+      else tc_commit(done_bar);
       mbar_wait(done_bar, 0, p.err);
     }
     __syncwarp();
@@ -361,6 +392,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int half = ew >> 2;
     uint8_t* stg = sEpi + ew * (32 * 64);
     int acc = 0; uint32_t acc_phase = 0;
+    // accumulator drained: arrive on the barrier of the CTA whose thread issues the MMAs
+    auto release_acc = [&](int a) {
+      if (CL == 2 && rank != 0) mbar_arrive_cluster(cluster_map(smem_u32(&acc_empty[a]), 0));
+      else mbar_arrive(&acc_empty[a]);
+    };
     for (int64_t u = unit0; u < n_units; u += ustep) {
       const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
       const int64_t ncol0 = ti.n_blk * BN + half * (BN / 2);
@@ -399,50 +435,82 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ti.store) {  // filler tile: release the accumulator unread
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (lane == 0) release_acc(acc);
         if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
         continue;
       }
-#pragma unroll 1
-      for (int sub = 0; sub < SUB; ++sub) {
+      // stage one 32x32 chunk of bf16 words (one row per lane) with the 64-byte
+      // swizzle and TMA-store it
+      auto store_chunk = [&](const uint32_t (&w)[16], const CUtensorMap* tmC, int64_t col, int64_t mrow) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        uint8_t* row = stg + lane * 64;
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
+              make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmC, stg, (int32_t)col, (int32_t)mrow);
+          bulk_commit();
+        }
+      };
+      auto pack = [](const uint32_t (&r)[32], uint32_t (&w)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+      };
+      if (SUB == 1) {
+        // drain this warp's whole share into registers (as bf16), hand the
+        // accumulator back, then store: the next tile's MMAs overlap the stores
         const CUtensorMap* tmC;
-        const int64_t mrow = out_rows(sub, tmC);
-        // a sub-tile past the last row is drained but not stored
-        const int live = ti.m_blk * C::TM + sub * BM < p.M ? nchunks : 0;
-        const uint32_t tbase =
-            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((acc + sub) * BN + half * (BN / 2));
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(tbase + c * 32, r);
+        const int64_t mrow = out_rows(0, tmC);
+        const int live = ti.m_blk * C::TM < p.M ? nchunks : 0;
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + half * (BN / 2));
+        uint32_t w[BN / 64][16];
+#pragma unroll
+        for (int c = 0; c < BN / 64; c += 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32cols(tbase + c * 32, r0);
+          tmem_ld_32cols(tbase + (c + 1) * 32, r1);
           tmem_ld_wait();
-          if (sub == SUB - 1 && c == BN / 64 - 1) {
-            // accumulator fully read: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-          }
-          if (c >= live) continue;
-          uint32_t w[16];
+          pack(r0, w[c]);
+          pack(r1, w[c + 1]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release_acc(acc);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 b2 =
-                __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-          uint8_t* row = stg + lane * 64;
-          const int sw = (lane >> 1) & 3;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
-                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(tmC, stg, (int32_t)(ncol0 + 32 * c), (int32_t)mrow);
-            bulk_commit();
+        for (int c = 0; c < BN / 64; ++c)
+          if (c < live) store_chunk(w[c], tmC, ncol0 + 32 * c, mrow);
+      } else {
+#pragma unroll 1
+        for (int sub = 0; sub < SUB; ++sub) {
+          const CUtensorMap* tmC;
+          const int64_t mrow = out_rows(sub, tmC);
+          // a sub-tile past the last row is drained but not stored
+          const int live = ti.m_blk * C::TM + sub * BM < p.M ? nchunks : 0;
+          const uint32_t tbase =
+              tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((acc + sub) * BN + half * (BN / 2));
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(tbase + c * 32, r);
+            tmem_ld_wait();
+            if (sub == SUB - 1 && c == BN / 64 - 1) {
+              // accumulator fully read: hand it back to the MMA warp
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) release_acc(acc);
+            }
+            if (c >= live) continue;
+            uint32_t w[16];
+            pack(r, w);
+            store_chunk(w, tmC, ncol0 + 32 * c, mrow);
           }
         }
       }
@@ -454,15 +522,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CL == 2) cluster_sync();  // no multicast or remote arrive targets an exited CTA
+  if (CL == 2) cluster_sync();  // no pair MMA, copy or remote arrive targets an exited CTA
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 1) {
+    if (CL == 2) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else tmem_dealloc(tmem, C::TMEM_COLS);
+  }
 }
 
 template <bool MX, int BN, int CL, int SUB>
 int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC0,
-               const CUtensorMap& tC1, const CUtensorMap& tSFB, GemmParams& p, cudaStream_t stream) {
-  using C = Cfg<MX, BN, SUB>;
+               const CUtensorMap& tC1, const CUtensorMap& tSFA, const CUtensorMap& tSFB, GemmParams& p,
+               cudaStream_t stream) {
+  using C = Cfg<MX, BN, SUB, CL>;
   p.m_tiles = (p.M + C::TM - 1) / C::TM;
   p.n_tiles = (p.N + BN - 1) / BN;
   p.m_pairs = (p.m_tiles + 1) / 2;
@@ -478,12 +550,10 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
   if (CL == 1) {
     const int grid = (int)std::min<int64_t>(units, num_sms());
-    k<<<grid, GEMM_THREADS, C::SMEM, stream>>>(tA, tB, tC0, tC1, tSFB, p);
+    k<<<grid, GEMM_THREADS, C::SMEM, stream>>>(tA, tB, tC0, tC1, tSFA, tSFB, p);
     return cuda_status(cudaGetLastError(), "gemm_kernel launch");
   }
-  const int clusters = (int)std::min<int64_t>(units, num_sms() / 2);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(GEMM_THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
@@ -494,7 +564,23 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k, tA, tB, tC0, tC1, tSFB, p);
+  // persistent grid: as many pairs as can be resident at once (SMs that
+  // cannot be paired within their GPC stay idle rather than forming a tail)
+  static int resident[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& nres = resident[dev & 63];
+  if (nres == 0) {
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+    if (e != cudaSuccess || n <= 0) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                                                       "cudaOccupancyMaxActiveClusters");
+    nres = n;
+  }
+  const int clusters = (int)std::min<int64_t>(units, nres);
+  cfg.gridDim = dim3(2 * clusters);
+  e = cudaLaunchKernelEx(&cfg, k, tA, tB, tC0, tC1, tSFA, tSFB, p);
   return cuda_status(e, "gemm_kernel cluster launch");
 }
 
@@ -503,15 +589,22 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
 #ifndef MX_GEMM_BN
 #define MX_GEMM_BN 256
 #endif
-#ifndef MX_GEMM_CLUSTER
-#define MX_GEMM_CLUSTER 1
+// MXFP8 on CTA pairs (cta_group::2, 256x256 tiles, six stages): exact, but
+// slower than single CTAs on GB300 (2.54 vs 2.82 PFLOP/s at 8192x8192x4096),
+// so built only on request.
+#ifndef MX_GEMM_PAIR
+#define MX_GEMM_PAIR 0
 #endif
 
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   constexpr int BN = MX_GEMM_BN;
-  constexpr int CL = MX_GEMM_CLUSTER;
-  constexpr uint32_t BROWS = CL == 2 ? BN / 2 : BN;  // rows of one B load
   const bool mx = g.mx != 0;
+  // MXFP8: 128x256 tiles (256x256 on CTA pairs when built so).  bf16:
+  // 256x256 tiles on one CTA as two 128-row sub-tiles (128-row tiles for the
+  // grouped forward form).
+  const bool pair = mx && MX_GEMM_PAIR && BN == 256;
+  const bool two_sub = !mx && BN == 256 && g.mode != GEMM_GROUP_M;
+  const uint32_t BROWS = pair ? BN / 2 : BN;  // rows of one B load
   const int esz = mx ? 1 : 2;
   const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t bk = mx ? 128 : 64;
@@ -521,7 +614,6 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   {
     uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.M};
     uint64_t strides[1] = {(uint64_t)g.K * esz};
-    const bool two_sub = !mx && CL == 1 && BN == 256 && g.mode != GEMM_GROUP_M;
     uint32_t box[2] = {bk, (uint32_t)(two_sub ? 2 * BM : BM)};
     rc = make_tmap(&tA, dt, 2, const_cast<void*>(g.a), dims, strides, box, opswz);
     if (rc) return rc;
@@ -591,10 +683,23 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     }
     if (rc) return rc;
   }
-  if (mx) return launch_cfg<true, BN, CL, 1>(g, tA, tB, tC0, tC1, tSFB, p, stream);
-  if (CL == 1 && BN == 256 && g.mode != GEMM_GROUP_M)
-    return launch_cfg<false, BN, 1, 2>(g, tA, tB, tC0, tC1, tSFB, p, stream);
-  return launch_cfg<false, BN, CL, 1>(g, tA, tB, tC0, tC1, tSFB, p, stream);
+  // A scales viewed as 32-bit words, one 512-byte tile per row: tile
+  // (row block rb, column cb) at row rb*(K/128) + cb.
+  CUtensorMap tSFA = tB;
+  if (pair) {
+    uint64_t dims[2] = {128, (uint64_t)(g.M / 128) * (uint64_t)(g.K / 128)};
+    uint64_t strides[1] = {512};
+    uint32_t box[2] = {128, 1};
+    rc = make_tmap(&tSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(g.sfa), dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  if (mx) {
+    if (pair) return launch_cfg<true, BN, 2, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+    return launch_cfg<true, BN, 1, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+  }
+  if (two_sub) return launch_cfg<false, BN, 1, 2>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+  return launch_cfg<false, BN, 1, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
 }
 
 }  // namespace mx
