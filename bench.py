@@ -443,10 +443,11 @@ def run_profile_case(args):
     def rnd(*shape, std=1.0):
         return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
 
-    if c == "quant":
+    if c in ("quant", "quant_row", "quant_col"):
         x = rnd(M, 8192)
-        fn = lambda: mx.quantize(x, mx.BOTH)
-        work, unit = M * 8192 * (2 + 2 * 1.03125), "B"
+        ax = {"quant": mx.BOTH, "quant_row": mx.ROW, "quant_col": mx.COL}[c]
+        fn = lambda: mx.quantize(x, ax)
+        work, unit = M * 8192 * (2 + (2 if ax == mx.BOTH else 1) * 1.03125), "B"
     elif c in ("swiglu_fwd", "swiglu_fwd_row"):
         h13 = rnd(M, 2 * 8192, std=1.3)
         ax = mx.ROW if c.endswith("row") else mx.BOTH
@@ -499,7 +500,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", default=None,
-                    choices=["quant", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd", "swiglu_bwd_hp", "gemm_mx",
+                    choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd", "swiglu_bwd_hp", "gemm_mx",
                              "gemm_bf16"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()

@@ -3,11 +3,14 @@
 // weight-gradient recipe.
 //
 // Design: a persistent kernel streams 128x128 bf16 tiles through a 3-stage
-// TMA ring in shared memory (one producer warp, eight consumer warps).  The
-// rowwise path reads 16-byte row segments from the tile (4 lanes per
-// 32-element block, warp-shuffle amax); the columnwise path reads 4-byte
-// column pairs down 32 rows (one thread per block) - the transpose happens
-// in shared memory, so every global load and store stays coalesced.
+// TMA ring in shared memory (one producer warp, eight consumer warps), each
+// tile as two 64-column boxes stored with the 128-byte swizzle (16-byte
+// chunk c of row r at chunk position c ^ (r & 7)).  The rowwise path gives
+// each thread one whole 32-element block (four 16-byte reads); the
+// columnwise path reads 4-byte column pairs down 32 rows (one thread per two
+// column blocks) - the transpose happens in shared memory, so every global
+// load and store stays coalesced, and the swizzle keeps both read patterns
+// free of bank conflicts.
 #include "tile_quant.cuh"
 #include "kernels.h"
 
@@ -96,24 +99,34 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
     const uint8_t* tile = smem + stage * QT_TILE_BYTES;
 
     if (ROW) {
-      // 16 lanes per 128-column row, 8 elements per lane; 2 rows per warp step.
-      const int seg = lane & 15;
-      const int box = seg >> 3, chunk = seg & 7;
+      // one thread per 32-element row block.  A quarter-warp covers rows
+      // 4g..4g+3 of one box, two blocks per row, so its eight 16-byte reads
+      // land on eight distinct swizzled chunk positions; quarter-warps 2k and
+      // 2k+1 write the two halves of the same 128-byte row segments.
+      const int qw = lane >> 3, e = lane & 7;
+      const int box = qw & 1, jj = e & 1;
       uint8_t* qrow = p.q_row + b * p.qr_bs;
       ScaleDst sd = p.s_row;
       sd.base += b * p.sr_bs;
-#pragma unroll 2
-      for (int it = 0; it < QT_R / (2 * QT_CONSUMER_WARPS); ++it) {
-        const int rr = it * (2 * QT_CONSUMER_WARPS) + warp * 2 + (lane >> 4);
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + box * QT_BOX_BYTES + rr * 128 + chunk * 16);
-        const uint32_t pk[4] = {v.x, v.y, v.z, v.w};
-        uint32_t s;
-        const uint2 codes = quant_row8(pk, s);
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int rr = it * 64 + warp * 8 + (qw >> 1) * 4 + (e >> 1);
+        const uint8_t* rowp = tile + box * QT_BOX_BYTES + rr * 128;
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((jj * 4 + k) ^ (rr & 7)) << 4));
+          pk[4 * k] = v.x; pk[4 * k + 1] = v.y; pk[4 * k + 2] = v.z; pk[4 * k + 3] = v.w;
+        }
+        uint32_t codes[8];
+        const uint32_t s = quant_row32(pk, codes);
         const int64_t r = r0 + rr;
-        const int64_t c = c0 + box * 64 + chunk * 8;
+        const int64_t c = c0 + box * 64 + jj * 32;
         if (r < p.rows && c < p.cols) {
-          *reinterpret_cast<uint2*>(qrow + r * p.qr_ld + c) = codes;
-          if ((chunk & 3) == 0) sd.put(r, c >> 5, s);
+          uint8_t* dst = qrow + r * p.qr_ld + c;
+          store16(dst, codes[0], codes[1], codes[2], codes[3]);
+          store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
+          sd.put(r, c >> 5, s);
         }
       }
     }
@@ -125,8 +138,9 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
       const int box = pair >> 5, pc = pair & 31;
       uint32_t v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        v[i] = *reinterpret_cast<const uint32_t*>(tile + box * QT_BOX_BYTES + (rb * 32 + i) * 128 + pc * 4);
+      for (int i = 0; i < 32; ++i)  // row rb*32+i: chunk pc/4 sits at (pc/4) ^ (i & 7)
+        v[i] = *reinterpret_cast<const uint32_t*>(tile + box * QT_BOX_BYTES + (rb * 32 + i) * 128 +
+                                                  ((((pc >> 2) ^ (i & 7)) << 4) | ((pc & 3) << 2)));
       const int64_t rg = r0 + rb * 32;
       const int64_t cg = c0 + box * 64 + pc * 2;
       if (rg < p.rows && cg < p.cols) {
@@ -179,7 +193,7 @@ int launch_quant(const QuantLaunch& q, cudaStream_t stream) {
     uint64_t strides[2] = {(uint64_t)q.cols * 2, (uint64_t)q.cols * q.rows * 2};
     uint32_t box[3] = {64, QT_R, 1};
     int rc = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q.x), dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   QuantKParams p{};

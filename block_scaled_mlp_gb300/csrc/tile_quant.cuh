@@ -1,9 +1,11 @@
 // tile_quant.cuh - MXFP8 block quantization of bf16 values held in registers,
 // used by the standalone cast kernel and by the fused SwiGLU kernels.
 //
-// Row blocks: four consecutive lanes each hold 8 consecutive elements of one
-// 32-element block.  Column blocks: one thread holds the 32 elements of two
-// adjacent columns as packed pairs.
+// Row blocks: one thread holds a whole 32-element block (quant_row32), or
+// four consecutive lanes each hold 8 of its elements (quant_row8).  Column
+// blocks: one thread holds the 32 elements of two adjacent columns as packed
+// pairs.  Scaling by the power-of-two inverse scale is exact; the E4M3
+// conversion rounds to nearest even and saturates.
 #pragma once
 
 #include "common.cuh"
@@ -37,6 +39,44 @@ MX_DEVINL uint32_t max_halves(uint32_t m2) {
   const uint32_t lo = m2 & 0xFFFFu, hi = m2 >> 16;
   const uint32_t isnan = (lo > 0x7F80u) | (hi > 0x7F80u);
   return isnan ? 0x7FC0u : max(lo, hi);
+}
+
+// Both elements of a packed bf16 pair times the power-of-two inverse scale
+// (inv2 holds it in both 32-bit halves), one packed fp32 multiply (RN, no
+// flush), then RNE saturating E4M3: the pair's two codes in the low 16 bits.
+MX_DEVINL uint32_t e4m3x2_scaled(uint32_t p, uint64_t inv2) {
+  uint64_t v, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(p << 16), "r"(p & 0xFFFF0000u));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(v), "l"(inv2));
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(r));
+  return cvt_e4m3x2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
+MX_DEVINL uint64_t splat_f32x2(float f) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(v) : "r"(__float_as_uint(f)));
+  return v;
+}
+
+// Quantize one whole 32-element block held by one thread as 16 packed bf16
+// pairs (element 2i in the low half of p[i]).  Writes the 32 codes as 8
+// words (element 0 in the lowest byte) and returns the scale byte.
+MX_DEVINL uint32_t quant_row32(const uint32_t (&p)[16], uint32_t (&codes)[8]) {
+  uint32_t m2 = abs2(p[0]);
+#pragma unroll
+  for (int i = 1; i < 16; ++i) m2 = max2(m2, abs2(p[i]));
+  const uint32_t s = e8m0_from_amax_bits(max_halves(m2));
+  if (s == 0xFF) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
+    return s;
+  }
+  const uint64_t inv2 = splat_f32x2(inv_scale_from_e8m0(s));
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    codes[i] = e4m3x2_scaled(p[2 * i], inv2) | (e4m3x2_scaled(p[2 * i + 1], inv2) << 16);
+  return s;
 }
 
 // Quantize 8 elements (4 packed bf16 pairs, element 2i in the low half) of a
@@ -74,13 +114,24 @@ MX_DEVINL void quant_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_
   const uint32_t la = m2 & 0xFFFFu, lb = m2 >> 16;
   sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la);
   sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb);
-  const float ia = inv_scale_from_e8m0(sa), ib = inv_scale_from_e8m0(sb);
+  // column A in the low lanes, column B in the high lanes: one packed
+  // multiply scales an element of each column
+  uint64_t iab;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(iab) : "f"(inv_scale_from_e8m0(sa)), "f"(inv_scale_from_e8m0(sb)));
+  uint32_t lo[32], hi[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    uint64_t x, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(v[i] << 16), "r"(v[i] & 0xFFFF0000u));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(iab));
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo[i]), "=r"(hi[i]) : "l"(r));
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t a01 = cvt_e4m3x2(bf16_lo(v[4 * i]) * ia, bf16_lo(v[4 * i + 1]) * ia);
-    const uint32_t a23 = cvt_e4m3x2(bf16_lo(v[4 * i + 2]) * ia, bf16_lo(v[4 * i + 3]) * ia);
-    const uint32_t b01 = cvt_e4m3x2(bf16_hi(v[4 * i]) * ib, bf16_hi(v[4 * i + 1]) * ib);
-    const uint32_t b23 = cvt_e4m3x2(bf16_hi(v[4 * i + 2]) * ib, bf16_hi(v[4 * i + 3]) * ib);
+    const uint32_t a01 = cvt_e4m3x2(__uint_as_float(lo[4 * i]), __uint_as_float(lo[4 * i + 1]));
+    const uint32_t a23 = cvt_e4m3x2(__uint_as_float(lo[4 * i + 2]), __uint_as_float(lo[4 * i + 3]));
+    const uint32_t b01 = cvt_e4m3x2(__uint_as_float(hi[4 * i]), __uint_as_float(hi[4 * i + 1]));
+    const uint32_t b23 = cvt_e4m3x2(__uint_as_float(hi[4 * i + 2]), __uint_as_float(hi[4 * i + 3]));
     ca[i] = a01 | (a23 << 16);
     cb[i] = b01 | (b23 << 16);
   }
