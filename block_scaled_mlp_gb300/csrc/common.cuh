@@ -418,6 +418,47 @@ MX_DEVINL uint32_t f32_to_bf16_bits(float f) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// Two fp32 lanes in one 64-bit register (lane 0 in the low word); the
+// f32x2 arithmetic rounds each lane to nearest even, without flushing.
+
+MX_DEVINL uint64_t f2_pack(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+MX_DEVINL void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+MX_DEVINL uint64_t f2_splat(float f) { return f2_pack(f, f); }
+// the two bf16 halves of p as fp32 (exact)
+MX_DEVINL uint64_t f2_from_bf16x2(uint32_t p) {
+  return f2_pack(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+}
+MX_DEVINL uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+MX_DEVINL uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+MX_DEVINL uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// RN to a packed bf16 pair (lane 0 in the low half)
+MX_DEVINL uint32_t f2_to_bf16x2(uint64_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Byte offset of scale (r, c) in the MMA tiled layout of an [R, S] scale
 // matrix whose tile row holds `tiles_per_row` = ceil(S/4) tiles.
 MX_DEVINL int64_t mma_scale_offset(int64_t r, int64_t c, int64_t tiles_per_row) {
