@@ -158,12 +158,12 @@ def run_gpu(args, rank, world, dev):
     L = mx.lib()
     P = mx._ptr
 
-    def step(x, dout):
+    def step(x, dout, y=out, dx=grads[0]):
         rc = L.mx_mlp_fwd(P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1), 128, recipe,
-                          P(ctx), P(scratch), P(out), err.ptr(), mx._stream())
+                          P(ctx), P(scratch), P(y), err.ptr(), mx._stream())
         mx._check(rc)
         rc = L.mx_mlp_bwd(P(ctx), P(dout), P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1),
-                          128, recipe, P(scratch), P(grads[0]), P(grads[1]), P(grads[2]), P(grads[3]), err.ptr(),
+                          128, recipe, P(scratch), P(dx), P(grads[1]), P(grads[2]), P(grads[3]), err.ptr(),
                           mx._stream())
         mx._check(rc)
 
@@ -199,22 +199,54 @@ def run_gpu(args, rank, world, dev):
     value = w["flops"] * world / (ms_max * 1e-3) / 1e12
     launches_per_step = 13 if E == 0 else 13
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies its inputs (x, dout) in from pinned host memory and its results
+    # (out, dx) back.  Double-buffered like a training input pipeline: step
+    # i+1's inputs go up on one copy stream and step i-1's results come down
+    # on another while step i computes; the timed region spans the first
+    # upload to the last download.
     hx = t["x"].cpu().pin_memory()
     hd = t["dout"].cpu().pin_memory()
-    ho = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
-    hdx = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
-    dx_buf, dd_buf = torch.empty_like(t["x"]), torch.empty_like(t["dout"])
+    ho = [torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hdx = [torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xin = [(torch.empty_like(t["x"]), torch.empty_like(t["dout"])) for _ in range(2)]
+    yout = [(out, grads[0]), (torch.empty_like(out), torch.empty_like(grads[0]))]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free = [ev(), ev()], [ev(), ev()]
+    out_ready, out_free = [ev(), ev()], [ev(), ev()]
+
+    def upload(k):
+        with torch.cuda.stream(up):
+            xin[k][0].copy_(hx, non_blocking=True)
+            xin[k][1].copy_(hd, non_blocking=True)
+            in_ready[k].record(up)
+
     barrier()
     torch.cuda.synchronize(dev)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(args.steps):
-        dx_buf.copy_(hx, non_blocking=True)
-        dd_buf.copy_(hd, non_blocking=True)
-        step(dx_buf, dd_buf)
-        ho.copy_(out, non_blocking=True)
-        hdx.copy_(grads[0], non_blocking=True)
+    up.wait_stream(stream)
+    down.wait_stream(stream)
+    upload(0)
+    for i in range(args.steps):
+        k = i % 2
+        if i + 1 < args.steps:
+            if i >= 1:
+                up.wait_event(in_free[(i + 1) % 2])    # step i-1 no longer reads that buffer
+            upload((i + 1) % 2)
+        stream.wait_event(in_ready[k])
+        if i >= 2:
+            stream.wait_event(out_free[k])              # step i-2's results are down
+        step(xin[k][0], xin[k][1], yout[k][0], yout[k][1])
+        in_free[k].record(stream)
+        out_ready[k].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(out_ready[k])
+            ho[k].copy_(yout[k][0], non_blocking=True)
+            hdx[k].copy_(yout[k][1], non_blocking=True)
+            out_free[k].record(down)
+    stream.wait_stream(down)
     a1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -224,7 +256,7 @@ def run_gpu(args, rank, world, dev):
         torch.distributed.all_reduce(et, op=torch.distributed.ReduceOp.MAX)
     e2e_value = w["flops"] * world / (float(et.item()) * 1e-3) / 1e12
     h2d = (hx.numel() + hd.numel()) * 2
-    d2h = (ho.numel() + hdx.numel()) * 2
+    d2h = (ho[0].numel() + hdx[0].numel()) * 2
 
     # ---- per-kernel pass: the same kernels launched one by one with events
     kern = kernel_breakdown(mx, w, t, offs, recipe, dev, max(1, min(args.steps, 10)))
