@@ -51,7 +51,7 @@ struct Cfg {
   static constexpr int SF_COL = NUM_ACC * BN;               // per-stage scale slots from here
   static constexpr int SF_SLOT = 4 + 4 * (BN / 128);       // TMEM columns of one stage's scales
   static constexpr size_t SMEM = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES +
-                                 MAX_GROUPS * 4 + 1024 /*align*/ + 256 /*barriers*/;
+                                 MAX_GROUPS * 4 * (CL == 1 ? 2 : 1) + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr uint32_t IDESC =
       MX ? ((1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24))
          : ((1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24));
@@ -69,6 +69,7 @@ struct GemmParams {
   int64_t sfb_expert_stride;  // bytes between experts (GROUP_M)
   int64_t split;              // row split of C between tmC0 / tmC1 (0: none)
   int64_t msub;               // GROUP_K: rows per expert in the output maps
+  int64_t band;               // DENSE: tile rows per band of the tile order
   int32_t* err;
 };
 
@@ -87,6 +88,7 @@ struct TileInfo {
 struct Groups {
   const int32_t* ends;
   const int32_t* pair_end;
+  const int32_t* unit_end;  // GROUP_M without clusters: work units of groups 0..e
   int32_t E;
   int64_t units_per_n;  // GROUP_M with clusters: tile pairs in one 128-row column
   bool ok;
@@ -120,21 +122,47 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
   ti.num_kb = (int32_t)(p.K / BK);
   ti.e = 0;
   if (CL == 1) {
-    ti.m_blk = u % p.m_tiles;
-    ti.n_blk = u / p.m_tiles;
     if (p.mode == GEMM_GROUP_M) {
-      const int64_t row = ti.m_blk * BM;
-      if (!g.ok || g.E == 0 || row >= g.ends[g.E - 1]) {
-        ti.num_kb = 0;  // tail rows (or invalid offsets): zeros
-      } else {
-        int lo = 0, hi = g.E - 1;  // first group whose end is > row
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (g.ends[mid] > row) hi = mid; else lo = mid + 1;
-        }
-        ti.e = lo;
+      // Expert-major: every tile of group e (its 128-row tiles x all tile
+      // columns, rows fastest) before group e+1, so that each group's rows and
+      // its expert's weights come from DRAM once; the rows past the last
+      // group follow as zero tiles.
+      if (!g.ok || g.E == 0) {  // invalid offsets: zeros everywhere
+        ti.m_blk = u % p.m_tiles;
+        ti.n_blk = u / p.m_tiles;
+        ti.num_kb = 0;
+        return ti;
       }
+      const int64_t grouped = g.unit_end[g.E - 1];
+      if (u >= grouped) {
+        const int64_t first = g.ends[g.E - 1] / BM;
+        const int64_t tt = p.m_tiles - first;
+        const int64_t r = u - grouped;
+        ti.n_blk = r / tt;
+        ti.m_blk = first + r % tt;
+        ti.num_kb = 0;
+        return ti;
+      }
+      int lo = 0, hi = g.E - 1;  // first group whose unit_end is > u
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (g.unit_end[mid] > u) hi = mid; else lo = mid + 1;
+      }
+      const int64_t start = lo == 0 ? 0 : g.ends[lo - 1];
+      const int64_t tiles_e = (g.ends[lo] - start) / BM;
+      const int64_t r = u - (lo == 0 ? 0 : g.unit_end[lo - 1]);
+      ti.e = lo;
+      ti.n_blk = r / tiles_e;
+      ti.m_blk = start / BM + r % tiles_e;
+      return ti;
     }
+    // dense: bands of p.band tile rows (sized so that a band of A stays in
+    // L2), rows fastest within a band
+    const int64_t per_band = p.band * p.n_tiles;
+    const int64_t b = u / per_band, r = u - b * per_band;
+    const int64_t bm = p.m_tiles - b * p.band < p.band ? p.m_tiles - b * p.band : p.band;
+    ti.n_blk = r / bm;
+    ti.m_blk = b * p.band + r % bm;
     return ti;
   }
   if (p.mode == GEMM_DENSE) {
@@ -183,7 +211,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* sSFA = sEpi + C::EPI_BYTES;                       // [STAGES][512]
   uint8_t* sSFB = sSFA + C::STAGES * C::SFA_BYTES;            // [STAGES][BN/128][512]
   int32_t* sGroups = reinterpret_cast<int32_t*>(sSFB + C::STAGES * C::SFB_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sGroups + MAX_GROUPS);
+  int32_t* sUnitEnd = sGroups + MAX_GROUPS;  // CL == 1 only
+  uint64_t* full = reinterpret_cast<uint64_t*>(sGroups + MAX_GROUPS * (CL == 1 ? 2 : 1));
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + C::NUM_ACC;
@@ -218,6 +247,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
   __syncthreads();
+  if (CL == 1 && p.mode == GEMM_GROUP_M && threadIdx.x == 0 && s_groups_ok) {
+    int64_t acc = 0;
+    int32_t prev = 0;
+    for (int e = 0; e < p.E; ++e) {
+      const int32_t v = sGroups[e];
+      acc += (int64_t)((v - prev) / BM) * p.n_tiles;
+      sUnitEnd[e] = (int32_t)acc;
+      prev = v;
+    }
+  }
   if (pairs_m && threadIdx.x == 0) {
     int64_t acc = 0;
     if (s_groups_ok) {
@@ -243,7 +282,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
   const uint32_t tmem = *tmem_holder;
-  Groups grp{sGroups, sGroups, p.E, pairs_m ? s_units_per_n : 0, s_groups_ok != 0};
+  Groups grp{sGroups, sGroups, sUnitEnd, p.E, pairs_m ? s_units_per_n : 0, s_groups_ok != 0};
   if (!grp.ok && threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, MX_ERR_BAD_OFFSETS);
   const int64_t n_units = pairs_m ? grp.units_per_n * p.n_tiles : p.tiles;
 
@@ -537,6 +576,12 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   using C = Cfg<MX, BN, SUB, CL>;
   p.m_tiles = (p.M + C::TM - 1) / C::TM;
   p.n_tiles = (p.N + BN - 1) / BN;
+  {
+    // dense tile order: bands of tile rows whose A slice fits in ~48 MB of L2
+    const int64_t row_bytes = (int64_t)C::TM * p.K * (MX ? 1 : 2);
+    int64_t band = (int64_t)(48ll << 20) / (row_bytes > 0 ? row_bytes : 1);
+    p.band = band < 1 ? 1 : (band > p.m_tiles ? p.m_tiles : band);
+  }
   p.m_pairs = (p.m_tiles + 1) / 2;
   const int64_t experts = g.mode == GEMM_GROUP_K ? g.E : 1;
   int64_t units;
@@ -545,6 +590,7 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   else units = p.m_pairs * p.n_tiles * experts;
   p.tiles = units;
   if (units == 0) return MX_OK;
+  if (units > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "gemm: too many tiles");
   auto k = gemm_kernel<MX, BN, CL, SUB>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");

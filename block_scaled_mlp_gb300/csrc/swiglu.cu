@@ -432,8 +432,10 @@ __global__ void __launch_bounds__(THREADS, 2)
               const float ratio = fabsf(gov[hh]) * rcp_approx(fabsf(inv[hh]));
               const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
               const float adyu = fabsf(dyuv[hh]), apg = fabsf(pgv[hh]);
+              // dy u == 0 (padding rows, exact zeros, underflow): dg is the
+              // signed zero dyu * si, whose sign is certain below this margin
               const bool ok_e = fabsf(gv2[hh]) <= 64.0f && clear_of_midpoint(pv[hh], 16) && margin < 16384.0f &&
-                                adyu >= 0x1p-100f && adyu <= 0x1p100f && apg >= 0x1p-100f &&
+                                (adyu == 0.0f || (adyu >= 0x1p-100f && adyu <= 0x1p100f && apg >= 0x1p-100f)) &&
                                 clear_of_midpoint(pgv[hh], (uint32_t)margin);
               slow |= (ok_e ? 0u : 1u) << (2 * i + hh);
             }
