@@ -577,9 +577,12 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   p.m_tiles = (p.M + C::TM - 1) / C::TM;
   p.n_tiles = (p.N + BN - 1) / BN;
   {
-    // dense tile order: bands of tile rows whose A slice fits in ~48 MB of L2
+    // dense tile order: one band (rows fastest over all of M) while the whole
+    // of A stays in L2; otherwise bands of tile rows whose A slice takes
+    // ~48 MB, so that A is read from DRAM once and B once per band
     const int64_t row_bytes = (int64_t)C::TM * p.K * (MX ? 1 : 2);
     int64_t band = (int64_t)(48ll << 20) / (row_bytes > 0 ? row_bytes : 1);
+    if (row_bytes * p.m_tiles <= (96ll << 20)) band = p.m_tiles;
     p.band = band < 1 ? 1 : (band > p.m_tiles ? p.m_tiles : band);
   }
   p.m_pairs = (p.m_tiles + 1) / 2;
