@@ -48,6 +48,16 @@ R6  GEMMs: C = deq(A) deq(B)^T accumulated exactly (fp64 of exact products),
 R7  Scale layout "MMA": the 128-row x 4-scale-column tiled layout of the
     block-scaled tensor-core MMA (public PTX / cuBLAS documentation), padded
     with 0x00.
+R12 Token-group padding ("[mxfp8] refactor model converter; use token group
+    padding kernels in torchao": per-group padding done by kernels instead of
+    host code; "Add MXFP8 fused-MLP overrides in torchtitan": the padded
+    dispatcher, pad_multiple=128, inert pad and tail rows).  Routed row r has
+    expert expert_of[r] in [0, E).  The padded layout places groups in expert
+    order, the rows of a group in increasing r (a stable sort by expert),
+    each group padded with zero rows to a multiple of pad_multiple; offs[e]
+    is the cumulative padded end of group e; padded rows past offs[E-1] up
+    to the buffer's capacity (the tail) are zero as well.  A routed row's
+    activations are those of token r // topk.
 
 Every function here that has a pin in ``tests/test_oracle_*.py`` says so.
 """
@@ -667,3 +677,48 @@ def e4m3_code_distance(c1, c2) -> np.ndarray:
         mag = c & 0x7F
         return np.where(c & 0x80, -mag, mag)
     return np.abs(ordinal(c1) - ordinal(c2))
+
+
+# --------------------------------------------------------------------------
+# Token-group padding (reading R12)
+# --------------------------------------------------------------------------
+
+
+def token_group_pad(expert_of, E: int, pad_multiple: int = 128, m_cap: int | None = None):
+    """Padded expert-major layout of routed rows (R12).
+
+    Returns (offs, row_dst, row_src): offs[e] the cumulative padded end of
+    group e (int32 [E]); row_dst[r] the padded row of routed row r (int32
+    [R]); row_src[i] the routed row held by padded row i, or -1 for padding
+    and tail rows (int32 [m_cap], m_cap defaulting to offs[-1]).  Pinned in
+    tests/test_oracle_dispatch.py."""
+    expert_of = np.asarray(expert_of, dtype=np.int64).reshape(-1)
+    R = expert_of.size
+    if R and (expert_of.min() < 0 or expert_of.max() >= E):
+        raise ValueError("expert id out of range")
+    counts = np.bincount(expert_of, minlength=E)[:E]
+    padded = (counts + pad_multiple - 1) // pad_multiple * pad_multiple
+    ends = np.cumsum(padded)
+    starts = ends - padded
+    if m_cap is None:
+        m_cap = int(ends[-1]) if E else 0
+    if E and ends[-1] > m_cap:
+        raise ValueError("padded layout exceeds the capacity")
+    order = np.argsort(expert_of, kind="stable")        # expert-major, r increasing within a group
+    row_dst = np.empty(R, dtype=np.int64)
+    rank = np.arange(R) - np.repeat(np.cumsum(counts) - counts, counts)  # position within the group
+    row_dst[order] = starts[expert_of[order]] + rank
+    row_src = np.full(m_cap, -1, dtype=np.int64)
+    row_src[row_dst] = np.arange(R)
+    return ends.astype(np.int32), row_dst.astype(np.int32), row_src.astype(np.int32)
+
+
+def gather_rows(x_bits, src, div: int = 1):
+    """y[i] = x[src[i] // div] for src[i] >= 0, zero rows otherwise (bf16 bit
+    patterns, copied exactly).  Pinned in tests/test_oracle_dispatch.py."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    src = np.asarray(src, dtype=np.int64)
+    y = np.zeros((src.size, x_bits.shape[1]), dtype=np.uint16)
+    live = src >= 0
+    y[live] = x_bits[src[live] // div]
+    return y
