@@ -25,6 +25,7 @@ __all__ = [
     "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "GROUP_M", "GROUP_K", "mma_scale_bytes",
     "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
     "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
+    "token_group_pad", "token_group_capacity", "gather_rows",
 ]
 
 ROW, COL, BOTH = 1, 2, 3
@@ -53,6 +54,9 @@ _SIGS = {
     "mx_mlp_bwd": ([_V, _V, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V,
                     _V, _V], _I),
     "mx_mlp_fwd_static_scratch": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V], _I),
+    "mx_token_group_pad_workspace": ([_I64, _I32], ctypes.c_size_t),
+    "mx_token_group_pad": ([_V, _I64, _I32, _I32, _I64, _V, _V, _V, _V, _V, _V], _I),
+    "mx_gather_rows": ([_V, _I64, _I64, _V, _I64, _I32, _V, _V, _V], _I),
 }
 
 
@@ -322,3 +326,40 @@ def mlp_bwd(ctx: MlpContext, dout, scratch=None, err: ErrorWord | None = None, g
                             M, d, h, _ptr(a["offs"]), max(E, 1), a["pad"], a["recipe"], _ptr(scratch), _ptr(dx),
                             _ptr(dw1), _ptr(dw3), _ptr(dw2), err.ptr() if err else None, _stream()))
     return dx, dw1, dw3, dw2
+
+
+# ---------------------------------------------------------------- token-group padding
+
+
+def token_group_capacity(R: int, E: int, pad_multiple: int = 128) -> int:
+    """Rows of a padded buffer that holds any routing of R rows over E experts."""
+    return -(-R // pad_multiple) * pad_multiple + pad_multiple * E
+
+
+def token_group_pad(expert_of, E: int, m_cap: int | None = None, pad_multiple: int = 128,
+                    err: ErrorWord | None = None):
+    """Padded expert-major layout of routed rows (int32 expert ids on the
+    device).  Returns (offs [E], row_dst [R], row_src [m_cap]), int32 on the
+    device, without a host synchronization."""
+    _need(expert_of, torch.int32, "expert_of")
+    R = expert_of.numel()
+    if m_cap is None:
+        m_cap = token_group_capacity(R, E, pad_multiple)
+    dev = expert_of.device
+    offs = torch.empty(E, dtype=torch.int32, device=dev)
+    row_dst = torch.empty(R, dtype=torch.int32, device=dev)
+    row_src = torch.empty(m_cap, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(lib().mx_token_group_pad_workspace(R, E), 16), dtype=torch.uint8, device=dev)
+    _check(lib().mx_token_group_pad(_ptr(expert_of), R, E, pad_multiple, m_cap, _ptr(offs), _ptr(row_dst),
+                                    _ptr(row_src), _ptr(ws), err.ptr() if err else None, _stream()))
+    return offs, row_dst, row_src
+
+
+def gather_rows(x, src, div: int = 1, err: ErrorWord | None = None):
+    """y[i] = x[src[i] // div] for src[i] >= 0, zero rows for src[i] < 0."""
+    _need(x, torch.bfloat16, "x")
+    _need(src, torch.int32, "src")
+    y = torch.empty((src.numel(), x.shape[1]), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mx_gather_rows(_ptr(x), x.shape[0], x.shape[1], _ptr(src), src.numel(), div, _ptr(y),
+                                err.ptr() if err else None, _stream()))
+    return y

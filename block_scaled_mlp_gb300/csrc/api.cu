@@ -493,6 +493,40 @@ int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const void* w1,
   return MX_OK;
 }
 
+// ---- token-group padding (pages "[mxfp8] refactor model converter; use token
+// group padding kernels in torchao" and "Add MXFP8 fused-MLP overrides in
+// torchtitan", Summary)
+
+size_t mx_token_group_pad_workspace(int64_t R, int32_t E) {
+  if (R < 0 || E < 1) return 0;
+  return token_group_pad_workspace(R, E);
+}
+
+int mx_token_group_pad(const int32_t* expert_of, int64_t R, int32_t E, int32_t pad_multiple, int64_t M_cap,
+                       int32_t* offs, int32_t* row_dst, int32_t* row_src, void* workspace, int32_t* err_word,
+                       void* stream) {
+  if (R < 0 || M_cap < 0) return fail(MX_ERR_INVALID_ARG, "R and M_cap must be >= 0");
+  if (E < 1 || E > 1024) return fail(MX_ERR_UNSUPPORTED, "need 1 <= E <= 1024 (got %d)", E);
+  if (pad_multiple != 128) return fail(MX_ERR_UNSUPPORTED, "pad_multiple must be 128 (got %d)", pad_multiple);
+  if (M_cap % 128) return fail(MX_ERR_UNSUPPORTED, "M_cap must be a multiple of 128");
+  if (M_cap > INT32_MAX || R > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "R and M_cap must fit in int32");
+  if (!offs || (M_cap > 0 && !row_src)) return fail(MX_ERR_INVALID_ARG, "offs or row_src is null");
+  if (R > 0 && (!expert_of || !row_dst || !workspace))
+    return fail(MX_ERR_INVALID_ARG, "expert_of, row_dst and workspace are required when R > 0");
+  return launch_token_group_pad(expert_of, R, E, pad_multiple, M_cap, offs, row_dst, row_src, workspace, err_word,
+                                (cudaStream_t)stream);
+}
+
+int mx_gather_rows(const void* x, int64_t rows_in, int64_t cols, const int32_t* src, int64_t rows_out,
+                   int32_t div, void* y, int32_t* err_word, void* stream) {
+  if (rows_in < 0 || rows_out < 0 || cols <= 0 || div < 1)
+    return fail(MX_ERR_INVALID_ARG, "need rows_in, rows_out >= 0, cols > 0, div >= 1");
+  if (cols % 8) return fail(MX_ERR_UNSUPPORTED, "cols must be a multiple of 8 (got %lld)", (long long)cols);
+  if (rows_out > 0 && (!src || !y || (rows_in > 0 && !x))) return fail(MX_ERR_INVALID_ARG, "null pointer");
+  if ((x && !aligned16(x)) || (y && !aligned16(y))) return fail(MX_ERR_ALIGNMENT, "x and y must be 16-byte aligned");
+  return launch_gather_rows(x, rows_in, cols, src, rows_out, div, y, err_word, (cudaStream_t)stream);
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -82,4 +82,12 @@ struct GemmLaunch {
 };
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream);
 
+// token-group padding (dispatch.cu)
+size_t token_group_pad_workspace(int64_t R, int32_t E);
+int launch_token_group_pad(const int32_t* expert_of, int64_t R, int32_t E, int32_t pad, int64_t M_cap,
+                           int32_t* offs, int32_t* row_dst, int32_t* row_src, void* workspace, int32_t* err,
+                           cudaStream_t stream);
+int launch_gather_rows(const void* x, int64_t rows_in, int64_t cols, const int32_t* src, int64_t rows_out,
+                       int32_t div, void* y, int32_t* err, cudaStream_t stream);
+
 }  // namespace mx

@@ -237,6 +237,52 @@ MX_API int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const vo
                void* dw3, void* dw2, int32_t* err_word, void* stream);
 
 /*
+ * mx_token_group_pad - the padded expert-major row layout that the grouped
+ * entry points take, built on the device from routing decisions ("[mxfp8]
+ * refactor model converter; use token group padding kernels in torchao",
+ * Summary: per-group padding done by kernels instead of host code; "Add
+ * MXFP8 fused-MLP overrides in torchtitan", Summary: the padded dispatcher
+ * with pad_multiple = 128, pad rows and the tail inert).
+ *
+ *   expert_of [R] int32: expert of routed row r, in [0, E) (for top-k
+ *             routing of T tokens, R = T*k rows, row r belongs to token r/k).
+ *   offs      [E] int32 out: cumulative padded group ends (the offs of
+ *             mx_grouped_mm / mx_mlp_fwd); group e holds its rows in
+ *             increasing r, padded up to a multiple of pad_multiple.
+ *   row_dst   [R] int32 out: padded row of routed row r.
+ *   row_src   [M_cap] int32 out: routed row held by padded row i, or -1 for
+ *             a padding row and for the tail past offs[E-1].
+ *   M_cap     rows of the padded buffers, a multiple of 128; the layout
+ *             always fits when M_cap >= ceil(R/128)*128 + 128*E.
+ *   workspace device scratch of mx_token_group_pad_workspace(R, E) bytes
+ *             (may be NULL when R == 0).
+ * No host synchronization: counts, offsets and ranks stay on the device.
+ * Requirements: 1 <= E <= 1024, pad_multiple == 128.  err_word (may be
+ * NULL) receives MX_ERR_BAD_OFFSETS if an expert id is out of range (that
+ * row is left unplaced) or if the layout exceeds M_cap (then no row is
+ * placed and offs is still written).
+ */
+MX_API size_t mx_token_group_pad_workspace(int64_t R, int32_t E);
+MX_API int mx_token_group_pad(const int32_t* expert_of, int64_t R, int32_t E, int32_t pad_multiple,
+                              int64_t M_cap, int32_t* offs, int32_t* row_dst, int32_t* row_src,
+                              void* workspace, int32_t* err_word, void* stream);
+
+/*
+ * mx_gather_rows - y[i, :] = x[src[i] / div, :] for src[i] >= 0 and zeros
+ * for src[i] < 0, i in [0, rows_out) (bf16 rows copied bit for bit).  With
+ * src = row_src of mx_token_group_pad and div = k it builds the padded
+ * expert-major activations from the token rows, pad and tail rows zero;
+ * with src = row_dst and div = 1 it brings padded results (out, dx) back to
+ * routed-row order (the same torchtitan page: dispatcher pad-row and tail
+ * inertness).
+ *   x [rows_in, cols], y [rows_out, cols]: bf16, 16-byte aligned, cols a
+ *   multiple of 8.  err_word (may be NULL) receives MX_ERR_BAD_OFFSETS for a
+ *   source row past rows_in; that output row is written as zeros.
+ */
+MX_API int mx_gather_rows(const void* x, int64_t rows_in, int64_t cols, const int32_t* src, int64_t rows_out,
+                          int32_t div, void* y, int32_t* err_word, void* stream);
+
+/*
  * mx_mlp_fwd_static_scratch - mx_mlp_fwd for callers that cannot allocate
  * device memory (no cudaMalloc at all: for instance code running where only
  * pre-registered buffers may be touched, or a host framework whose allocator

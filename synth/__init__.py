@@ -130,6 +130,22 @@ def dirichlet_group_counts(E: int, rows: int, alpha: float, seed: int, n_empty: 
     return c[rng.permutation(E)]
 
 
+def routed_expert_ids(counts: np.ndarray, seed: int) -> np.ndarray:
+    """Expert id of every routed row (int32): counts[e] rows of expert e, in a
+    seeded random order (the routing decisions of a batch, before dispatch)."""
+    rng = np.random.default_rng(seed)
+    ids = np.repeat(np.arange(len(counts), dtype=np.int32), np.asarray(counts, dtype=np.int64))
+    return ids[rng.permutation(ids.size)]
+
+
+def topk_expert_ids(tokens: int, E: int, k: int, seed: int) -> np.ndarray:
+    """Top-k routing: k distinct experts per token, flattened token-major
+    (routed row r belongs to token r // k)."""
+    rng = np.random.default_rng(seed)
+    keys = rng.random((tokens, E))
+    return np.argsort(keys, axis=1)[:, :k].astype(np.int32).reshape(-1)
+
+
 def pad_counts(counts: np.ndarray, pad_multiple: int = 128) -> np.ndarray:
     return ((np.asarray(counts) + pad_multiple - 1) // pad_multiple) * pad_multiple
 

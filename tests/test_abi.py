@@ -21,13 +21,14 @@ def L():
 
 def _declared():
     src = open(HEADER).read()
-    return sorted(set(re.findall(r"MX_API\s+(?:const\s+char\*|int)\s+(mx_[a-z0-9_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"MX_API\s+(?:const\s+char\*|int|size_t)\s+(mx_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
     names = _declared()
     for want in ["mx_quantize", "mx_swiglu_quant", "mx_swiglu_quant_bwd", "mx_scaled_mm", "mx_grouped_mm",
-                 "mx_bf16_wgrad", "mx_mlp_workspace_size", "mx_mlp_fwd", "mx_mlp_bwd"]:
+                 "mx_bf16_wgrad", "mx_mlp_workspace_size", "mx_mlp_fwd", "mx_mlp_bwd",
+                 "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows"]:
         assert want in names
 
 
@@ -78,6 +79,21 @@ def test_mlp_workspace_and_validation(L):
     assert L.mx_mlp_fwd(p, p, p, p, 200, 256, 512, None, 0, 128, 0, p, p, p, None, None) == 4
     assert L.mx_mlp_fwd(p, p, p, p, 256, 256, 512, p, 4, 128, 9, p, p, p, None, None) == 1
     assert L.mx_mlp_bwd(p, None, p, p, p, p, 256, 256, 512, None, 0, 128, 0, p, p, p, p, p, None, None) == 1
+
+
+def test_token_group_pad_rejects_bad_arguments(L):
+    p = _fake()
+    assert L.mx_token_group_pad_workspace(4096, 16) == 16 + 4 * 16 * 4     # 4 chunks of 1024 rows
+    assert L.mx_token_group_pad(p, 100, 0, 128, 256, p, p, p, p, None, None) == 4       # E = 0
+    assert L.mx_token_group_pad(p, 100, 2000, 128, 256, p, p, p, p, None, None) == 4    # E > 1024
+    assert L.mx_token_group_pad(p, 100, 4, 64, 256, p, p, p, p, None, None) == 4        # pad 64
+    assert L.mx_token_group_pad(p, 100, 4, 128, 200, p, p, p, p, None, None) == 4       # M_cap % 128
+    assert L.mx_token_group_pad(p, -1, 4, 128, 256, p, p, p, p, None, None) == 1        # R < 0
+    assert L.mx_token_group_pad(None, 100, 4, 128, 256, p, p, p, p, None, None) == 1    # no expert ids
+    assert L.mx_token_group_pad(p, 100, 4, 128, 256, p, p, p, None, None, None) == 1    # no workspace
+    assert L.mx_gather_rows(p, 10, 12, p, 10, 1, p, None, None) == 4                      # cols % 8
+    assert L.mx_gather_rows(p, 10, 16, p, 10, 0, p, None, None) == 1                      # div 0
+    assert L.mx_gather_rows(ctypes.c_void_p(0x1008), 10, 16, p, 10, 1, p, None, None) == 2  # alignment
 
 
 def test_python_binding_fails_loudly_without_cuda_tensors():
