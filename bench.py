@@ -79,6 +79,7 @@ def make_workload(name):
             counts = synth.dirichlet_group_counts(w["E"], w["tokens"], w["alpha"], w["seed"], w["n_empty"])
         inp = synth.grouped_mlp_inputs(counts, w["d"], w["h"], w["seed"])
         w["M_total"] = int(inp["offs"][-1])
+        w["counts_arr"] = counts
     w.setdefault("recipe", "rceil")
     w["flops"] = 18.0 * w["tokens"] * w["d"] * w["h"]   # real routed rows, padding excluded
     return w, inp
@@ -299,7 +300,65 @@ def run_gpu(args, rank, world, dev):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if w["kind"] == "grouped":
+        res["dispatch"] = dispatch_measure(mx, w, dev, peaks["hbm_gbs"])
+    if not args.no_quant_sweep and rank == 0:
+        res["quant_sweep"] = quant_sweep_measure(mx, dev, peaks["hbm_gbs"])
     return res
+
+
+def _event_ms(fn, iters):
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def dispatch_measure(mx, w, dev, hbm_gbs, iters=10):
+    """The token-group padding that precedes a grouped step: routing ids of
+    the workload's group counts -> padded layout (mx_token_group_pad), token
+    rows -> padded activations and padded results -> routed order
+    (mx_gather_rows).  HBM-bound; bytes = rows read + rows written."""
+    counts, k, d, E = w["counts_arr"], w["topk"], w["d"], w["E"]
+    ids = torch.as_tensor(synth.routed_expert_ids(counts, w["seed"] + 100), device=dev)
+    R = ids.numel()
+    T = R // k
+    m_cap = mx.token_group_capacity(R, E)
+    x = torch.randn((T, d), device=dev, dtype=torch.float32).to(torch.bfloat16)
+    offs, dst, src = mx.token_group_pad(ids, E, m_cap)
+    xp = mx.gather_rows(x, src, div=k)
+    pad_ms = _event_ms(lambda: mx.token_group_pad(ids, E, m_cap), iters)
+    gat_ms = _event_ms(lambda: mx.gather_rows(x, src, div=k), iters)
+    unp_ms = _event_ms(lambda: mx.gather_rows(xp, dst, div=1), iters)
+    g_bytes = (R + m_cap) * d * 2
+    u_bytes = 2 * R * d * 2
+    gbs = (g_bytes + u_bytes) / ((gat_ms + unp_ms) * 1e-3) / 1e9
+    return {"routed_rows": R, "topk": k, "padded_rows": m_cap, "pad_ms": round(pad_ms, 4),
+            "gather_ms": round(gat_ms, 4), "unpad_ms": round(unp_ms, 4), "gather_gbs": round(gbs, 1),
+            "frac": round(gbs / hbm_gbs, 4), "bytes": "gather (R + M_cap) d 2, unpad 2 R d 2"}
+
+
+def quant_sweep_measure(mx, dev, hbm_gbs, iters=5):
+    """The quantize sweep (N x N bf16, N(0,1) with 1% outliers x100) by axis:
+    algorithmic GB/s of mx_quantize against the HBM peak."""
+    out = {}
+    for n in (4096, 8192, 16384, 32768):
+        x = torch.randn((n, n), device=dev, dtype=torch.float32)
+        x = torch.where(torch.rand_like(x) < 0.01, x * 100, x).to(torch.bfloat16)
+        for name, ax, per in (("row", mx.ROW, 2 + 1.03125), ("col", mx.COL, 2 + 1.03125),
+                              ("both", mx.BOTH, 2 + 2 * 1.03125)):
+            ms = _event_ms(lambda: mx.quantize(x, ax), iters)
+            gbs = n * n * per / (ms * 1e-3) / 1e9
+            out[f"{n}_{name}"] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4)}
+        del x
+        torch.cuda.empty_cache()
+    return out
 
 
 def kernel_breakdown(mx, w, t, offs, recipe, dev, steps):
@@ -494,6 +553,16 @@ def run_profile_case(args):
             fn = lambda: mx.swiglu_quant_bwd(dy, h13, mx.ROW, bf16_transposed=True)
             work = M * 8192 * (6 + 2 * 1.03125 + 6)
         unit = "B"
+    elif c == "dispatch":   # MoE 64E routing: 16384 tokens x top-8 over 64 experts, d = 7168
+        E, k, T, d = 64, 8, 16384, 7168
+        ids = torch.as_tensor(synth.topk_expert_ids(T, E, k, 17), device=dev)
+        x = rnd(T, d)
+        m_cap = mx.token_group_capacity(T * k, E)
+
+        def fn():
+            offs, dst, src = mx.token_group_pad(ids, E, m_cap)
+            mx.gather_rows(x, src, div=k)
+        work, unit = (T * k + m_cap) * d * 2, "B"
     elif c in ("gemm_mx", "gemm_bf16"):
         N, K = 8192, 4096
         if c == "gemm_mx":
@@ -531,9 +600,10 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_ffn", choices=sorted(k for k in synth.WORKLOADS if k != "tiny_dense"))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-quant-sweep", action="store_true", help="skip the quantize-sweep GB/s object")
     ap.add_argument("--profile-case", default=None,
-                    choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd", "swiglu_bwd_hp", "gemm_mx",
-                             "gemm_bf16"])
+                    choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
+                             "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "dispatch"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

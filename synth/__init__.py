@@ -195,7 +195,7 @@ WORKLOADS = {
     "tiny_dense": dict(kind="dense", M=256, d=256, h=512, seed=0),
     "llama3_8b_ffn": dict(kind="dense", M=8192, d=4096, h=14336, seed=1, recipe="wgrad_hp"),
     "moe_16e": dict(kind="grouped", E=16, d=5120, h=8192, tokens=32768, seed=2,
-                    counts="zipf", s=1.1, n_empty=1),
+                    counts="zipf", s=1.1, n_empty=1, topk=1),
     "moe_64e": dict(kind="grouped", E=64, d=7168, h=2048, tokens=131072, seed=3,
-                    counts="dirichlet", alpha=0.3, n_empty=4),
+                    counts="dirichlet", alpha=0.3, n_empty=4, topk=8),
 }
