@@ -85,6 +85,31 @@ def make_workload(name):
     return w, inp
 
 
+def _cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if part:
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def bind_to_gpu_cpus(dev):
+    """Run on the host CPUs local to the GPU (its PCI device's local_cpulist),
+    so that pinned host buffers are allocated next to the GPU's host link.
+    Best effort: returns the CPU list, or None when it cannot be read."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        cpus = _cpulist(open(f"/sys/bus/pci/devices/{bus}/local_cpulist").read())
+        if cpus and len(cpus) < len(os.sched_getaffinity(0)):
+            os.sched_setaffinity(0, cpus)
+            return f"{min(cpus)}-{max(cpus)}" if max(cpus) - min(cpus) + 1 == len(cpus) else sorted(cpus)
+    except Exception:
+        return None
+    return None
+
+
 def to_dev(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
@@ -206,6 +231,7 @@ def run_gpu(args, rank, world, dev):
     # i+1's inputs go up on one copy stream and step i-1's results come down
     # on another while step i computes; the timed region spans the first
     # upload to the last download.
+    host_cpus = bind_to_gpu_cpus(dev)
     hx = t["x"].cpu().pin_memory()
     hd = t["dout"].cpu().pin_memory()
     ho = [torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -296,7 +322,7 @@ def run_gpu(args, rank, world, dev):
                          "peak_source": peaks["source"]},
         "kernels_ms_per_step": {k: round(v["ms"], 4) for k, v in kern.items() if isinstance(v, dict)},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "host_cpus": host_cpus},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
