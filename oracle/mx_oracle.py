@@ -58,6 +58,12 @@ R12 Token-group padding ("[mxfp8] refactor model converter; use token group
     is the cumulative padded end of group e; padded rows past offs[E-1] up
     to the buffer's capacity (the tail) are zero as well.  A routed row's
     activations are those of token r // topk.
+R13 Per-linear MXFP8 path ("TrainingWeightWrapperTensor base class ...",
+    linear override; "Add MXFP8 fused-MLP overrides in torchtitan": non-MLP
+    linears keep the per-linear MXFP8 path): out = x w^T with both operands
+    MX(R) along the contraction; dx = dout w with dout MX(R) and w MX(C);
+    dw = dout^T x with both MX(C) along the tokens, or in bf16 under the
+    wgrad_hp recipe; each GEMM rounded once to bf16.
 
 Every function here that has a pin in ``tests/test_oracle_*.py`` says so.
 """
@@ -677,6 +683,42 @@ def e4m3_code_distance(c1, c2) -> np.ndarray:
         mag = c & 0x7F
         return np.where(c & 0x80, -mag, mag)
     return np.abs(ordinal(c1) - ordinal(c2))
+
+
+# --------------------------------------------------------------------------
+# MXFP8 linear (reading R13)
+# --------------------------------------------------------------------------
+
+
+def linear_fwd(x, w):
+    """out = RN_bf16(x . w^T) with x [M,K] and w [N,K] both quantized MX(R)
+    along K (the per-linear MXFP8 path, reading R13).  Pinned in
+    tests/test_oracle_linear.py."""
+    xq, xs = quantize_rows(np.asarray(x, dtype=np.uint16))
+    wq, ws = quantize_rows(np.asarray(w, dtype=np.uint16))
+    return round_to_bf16_bits(mx_mm(xq, xs, wq, ws))
+
+
+def linear_bwd(x, w, dout, recipe=RECIPE_RCEIL):
+    """Gradients of out = x . w^T (reading R13).
+
+    dx = RN_bf16(dout . w): dout MX(R) along N, w MX(C) along N.
+    dw = RN_bf16(dout^T . x): default recipe dout and x MX(C) along M;
+    wgrad_hp recipe bf16 operands, float64 accumulation.
+    Returns (dx, dw) as bf16 bits.  Pinned in tests/test_oracle_linear.py."""
+    x = np.asarray(x, dtype=np.uint16)
+    w = np.asarray(w, dtype=np.uint16)
+    dout = np.asarray(dout, dtype=np.uint16)
+    dq, ds = quantize_rows(dout)
+    wq_c, ws_c = quantize_cols(w)                        # [K, N], blocks along N
+    dx = round_to_bf16_bits(mx_mm(dq, ds, wq_c, ws_c))
+    if recipe == RECIPE_RCEIL_WGRAD_HP:
+        dw = round_to_bf16_bits(bf16_mm(dout.T, x.T))
+    else:
+        dq_c, ds_c = quantize_cols(dout)                 # [N, M], blocks along M
+        xq_c, xs_c = quantize_cols(x)                    # [K, M]
+        dw = round_to_bf16_bits(mx_mm(dq_c, ds_c, xq_c, xs_c))
+    return dx, dw
 
 
 # --------------------------------------------------------------------------
