@@ -25,7 +25,7 @@ __all__ = [
     "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "GROUP_M", "GROUP_K", "mma_scale_bytes",
     "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
     "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
-    "token_group_pad", "token_group_capacity", "gather_rows",
+    "token_group_pad", "token_group_capacity", "gather_rows", "linear_fwd", "linear_bwd", "LinearContext",
 ]
 
 ROW, COL, BOTH = 1, 2, 3
@@ -55,6 +55,10 @@ _SIGS = {
                     _V, _V], _I),
     "mx_mlp_fwd_static_scratch": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V], _I),
     "mx_token_group_pad_workspace": ([_I64, _I32], ctypes.c_size_t),
+    "mx_linear_workspace_size": ([_I64, _I64, _I64, _I, ctypes.POINTER(ctypes.c_size_t),
+                                  ctypes.POINTER(ctypes.c_size_t)], _I),
+    "mx_linear_fwd": ([_V, _V, _I64, _I64, _I64, _I, _V, _V, _V, _V, _V], _I),
+    "mx_linear_bwd": ([_V, _V, _V, _I64, _I64, _I64, _I, _V, _V, _V, _V, _V], _I),
     "mx_token_group_pad": ([_V, _I64, _I32, _I32, _I64, _V, _V, _V, _V, _V, _V], _I),
     "mx_gather_rows": ([_V, _I64, _I64, _V, _I64, _I32, _V, _V, _V], _I),
 }
@@ -363,3 +367,44 @@ def gather_rows(x, src, div: int = 1, err: ErrorWord | None = None):
     _check(lib().mx_gather_rows(_ptr(x), x.shape[0], x.shape[1], _ptr(src), src.numel(), div, _ptr(y),
                                 err.ptr() if err else None, _stream()))
     return y
+
+
+# ---------------------------------------------------------------- MXFP8 linear
+
+
+class LinearContext:
+    """What mx_linear_fwd saves for mx_linear_bwd (opaque device buffer)."""
+
+    def __init__(self, buf, args):
+        self.buf = buf
+        self.args = args   # (w, M, K, N, recipe)
+
+
+def linear_fwd(x, w, recipe=RECIPE_RCEIL, err: ErrorWord | None = None):
+    """out = x . w^T in MXFP8 (x [M, K], w [N, K] bf16).  Returns (out, ctx)."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    M, K = x.shape
+    N = w.shape[0]
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().mx_linear_workspace_size(M, K, N, recipe, ctypes.byref(c), ctypes.byref(s)))
+    ctx = torch.empty(max(c.value, 16), dtype=torch.uint8, device=x.device)
+    scratch = torch.empty(max(s.value, 16), dtype=torch.uint8, device=x.device)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mx_linear_fwd(_ptr(x), _ptr(w), M, K, N, recipe, _ptr(ctx), _ptr(scratch), _ptr(out),
+                               err.ptr() if err else None, _stream()))
+    return out, LinearContext(ctx, (w, M, K, N, recipe))
+
+
+def linear_bwd(ctx: LinearContext, dout, err: ErrorWord | None = None):
+    """(dx [M, K], dw [N, K]) of out = x . w^T."""
+    w, M, K, N, recipe = ctx.args
+    _need(dout, torch.bfloat16, "dout")
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().mx_linear_workspace_size(M, K, N, recipe, ctypes.byref(c), ctypes.byref(s)))
+    scratch = torch.empty(max(s.value, 16), dtype=torch.uint8, device=dout.device)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dout.device)
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=dout.device)
+    _check(lib().mx_linear_bwd(_ptr(ctx.buf), _ptr(dout), _ptr(w), M, K, N, recipe, _ptr(scratch), _ptr(dx),
+                               _ptr(dw), err.ptr() if err else None, _stream()))
+    return dx, dw

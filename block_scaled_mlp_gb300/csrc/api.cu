@@ -187,6 +187,57 @@ int check_mlp_args(const void* x, const void* w1, const void* w3, const void* w2
   return MX_OK;
 }
 
+// ---- per-linear MXFP8 path: buffers
+struct LinearBuffers {
+  uint8_t *xq_c, *xs_c, *x_t;                 // ctx: columnwise x (default) or bf16 x^T (HP)
+  size_t ctx_bytes;
+  uint8_t *xq_r, *xs_r, *wq_r, *ws_r;         // forward scratch
+  uint8_t *dq_r, *ds_r, *wq_c, *ws_c, *dq_c, *ds_c, *dout_t;  // backward scratch
+  size_t scratch_bytes;
+};
+
+LinearBuffers carve_linear(void* ctx, void* scratch, int64_t M, int64_t K, int64_t N, int recipe) {
+  LinearBuffers b{};
+  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  Arena c(ctx);
+  if (hp) {
+    b.x_t = c.take(K * M * 2);
+  } else {
+    b.xq_c = c.take(K * M);
+    b.xs_c = c.take(mma_scale_bytes(K, M));
+  }
+  b.ctx_bytes = c.off;
+  Arena f(scratch);
+  b.xq_r = f.take(M * K);
+  b.xs_r = f.take(mma_scale_bytes(M, K));
+  b.wq_r = f.take(N * K);
+  b.ws_r = f.take(mma_scale_bytes(N, K));
+  Arena g(scratch);
+  b.dq_r = g.take(M * N);
+  b.ds_r = g.take(mma_scale_bytes(M, N));
+  b.wq_c = g.take(K * N);
+  b.ws_c = g.take(mma_scale_bytes(K, N));
+  if (hp) {
+    b.dout_t = g.take(N * M * 2);
+  } else {
+    b.dq_c = g.take(N * M);
+    b.ds_c = g.take(mma_scale_bytes(N, M));
+  }
+  b.scratch_bytes = std::max(f.off, g.off);
+  return b;
+}
+
+int check_linear_args(int64_t M, int64_t K, int64_t N, int recipe) {
+  if (M <= 0 || K <= 0 || N <= 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
+  if (M % 128 || K % 128 || N % 128)
+    return fail(MX_ERR_UNSUPPORTED, "M, K and N must be multiples of 128 (got %lld, %lld, %lld)", (long long)M,
+                (long long)K, (long long)N);
+  if (recipe != MX_RECIPE_RCEIL && recipe != MX_RECIPE_RCEIL_WGRAD_HP)
+    return fail(MX_ERR_INVALID_ARG, "unknown recipe %d", recipe);
+  if (M > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "dimension too large");
+  return MX_OK;
+}
+
 }  // namespace
 }  // namespace mx
 
@@ -491,6 +542,93 @@ int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const void* w1,
     if ((rc = launch_gemm(g, st))) return rc;
   }
   return MX_OK;
+}
+
+// ---- per-linear MXFP8 path ("TrainingWeightWrapperTensor base class ...",
+// linear override; "Add MXFP8 fused-MLP overrides in torchtitan": non-MLP
+// linears keep the per-linear path)
+
+int mx_linear_workspace_size(int64_t M, int64_t K, int64_t N, int recipe, size_t* ctx_bytes,
+                             size_t* scratch_bytes) {
+  int rc = check_linear_args(M, K, N, recipe);
+  if (rc) return rc;
+  if (!ctx_bytes || !scratch_bytes) return fail(MX_ERR_INVALID_ARG, "null output pointer");
+  LinearBuffers b = carve_linear(nullptr, nullptr, M, K, N, recipe);
+  *ctx_bytes = b.ctx_bytes;
+  *scratch_bytes = b.scratch_bytes;
+  return MX_OK;
+}
+
+int mx_linear_fwd(const void* x, const void* w, int64_t M, int64_t K, int64_t N, int recipe, void* ctx,
+                  void* scratch, void* out, int32_t* err_word, void* stream) {
+  int rc = check_linear_args(M, K, N, recipe);
+  if (rc) return rc;
+  if (!x || !w || !ctx || !scratch || !out) return fail(MX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(ctx) || !aligned16(scratch) || !aligned16(out))
+    return fail(MX_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  cudaStream_t st = (cudaStream_t)stream;
+  LinearBuffers b = carve_linear(ctx, scratch, M, K, N, recipe);
+  {  // x -> MX(R) along K; MX(C) along M (or bf16 x^T) saved for the weight gradient
+    QuantLaunch q{};
+    q.x = x; q.rows = M; q.cols = K; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
+    q.q_row = b.xq_r; q.s_row = b.xs_r;
+    if (hp) { q.t_col = b.x_t; q.tc_ld = M; }
+    else { q.q_col = b.xq_c; q.s_col = b.xs_c; q.qc_ld = M; }
+    if ((rc = launch_quant(q, st))) return rc;
+  }
+  {  // w -> MX(R) along K
+    QuantLaunch q{};
+    q.x = w; q.rows = N; q.cols = K; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
+    q.q_row = b.wq_r; q.s_row = b.ws_r;
+    if ((rc = launch_quant(q, st))) return rc;
+  }
+  GemmLaunch g{};
+  g.mx = 1; g.mode = GEMM_DENSE;
+  g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.wq_r; g.sfb = b.ws_r;
+  g.M = M; g.N = N; g.K = K; g.E = 1; g.c0 = out; g.err = err_word;
+  return launch_gemm(g, st);
+}
+
+int mx_linear_bwd(const void* ctx, const void* dout, const void* w, int64_t M, int64_t K, int64_t N, int recipe,
+                  void* scratch, void* dx, void* dw, int32_t* err_word, void* stream) {
+  int rc = check_linear_args(M, K, N, recipe);
+  if (rc) return rc;
+  if (!ctx || !dout || !w || !scratch || !dx || !dw) return fail(MX_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(ctx) || !aligned16(dout) || !aligned16(w) || !aligned16(scratch) || !aligned16(dx) ||
+      !aligned16(dw))
+    return fail(MX_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  cudaStream_t st = (cudaStream_t)stream;
+  LinearBuffers b = carve_linear(const_cast<void*>(ctx), scratch, M, K, N, recipe);
+  {  // dout -> MX(R) along N; MX(C) along M (or bf16 dout^T)
+    QuantLaunch q{};
+    q.x = dout; q.rows = M; q.cols = N; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
+    q.q_row = b.dq_r; q.s_row = b.ds_r;
+    if (hp) { q.t_col = b.dout_t; q.tc_ld = M; }
+    else { q.q_col = b.dq_c; q.s_col = b.ds_c; q.qc_ld = M; }
+    if ((rc = launch_quant(q, st))) return rc;
+  }
+  {  // w -> MX(C) along N: codes [K, N]
+    QuantLaunch q{};
+    q.x = w; q.rows = N; q.cols = K; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
+    q.q_col = b.wq_c; q.s_col = b.ws_c; q.qc_ld = N;
+    if ((rc = launch_quant(q, st))) return rc;
+  }
+  {  // dx = dout . w
+    GemmLaunch g{};
+    g.mx = 1; g.mode = GEMM_DENSE;
+    g.a = b.dq_r; g.sfa = b.ds_r; g.b = b.wq_c; g.sfb = b.ws_c;
+    g.M = M; g.N = K; g.K = N; g.E = 1; g.c0 = dx; g.err = err_word;
+    if ((rc = launch_gemm(g, st))) return rc;
+  }
+  // dw = dout^T . x
+  GemmLaunch g{};
+  g.mx = hp ? 0 : 1; g.mode = GEMM_DENSE;
+  if (hp) { g.a = b.dout_t; g.b = b.x_t; }
+  else { g.a = b.dq_c; g.sfa = b.ds_c; g.b = b.xq_c; g.sfb = b.xs_c; }
+  g.M = N; g.N = K; g.K = M; g.E = 1; g.c0 = dw; g.err = err_word;
+  return launch_gemm(g, st);
 }
 
 // ---- token-group padding (pages "[mxfp8] refactor model converter; use token

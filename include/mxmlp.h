@@ -237,6 +237,30 @@ MX_API int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const vo
                void* dw3, void* dw2, int32_t* err_word, void* stream);
 
 /*
+ * mx_linear_* - the per-linear MXFP8 path for linears outside the MLP
+ * (attention projections, lm_head): the linear override of the page
+ * "TrainingWeightWrapperTensor base class; subclasses for FP8/MXFP8 with
+ * grouped_mm and linear overrides" (Summary), kept for non-MLP linears by the
+ * page "Add MXFP8 fused-MLP overrides in torchtitan" (Summary).
+ *
+ *   forward   out [M, N] = x [M, K] . w [N, K]^T, x and w MX(R) along K.
+ *   backward  dx [M, K] = dout [M, N] . w, dout MX(R) and w MX(C) along N;
+ *             dw [N, K] = dout^T . x, both MX(C) along M (MX_RECIPE_RCEIL) or
+ *             bf16 operands (MX_RECIPE_RCEIL_WGRAD_HP).
+ *   ctx       caller buffer written by the forward and read by the backward
+ *             (columnwise x, or bf16 x^T); scratch: caller buffer, both sized by
+ *             mx_linear_workspace_size.  All bf16 in/out, fp32 accumulation,
+ *             one RN to bf16.
+ * Requirements: M, K, N multiples of 128; 16-byte aligned pointers.
+ */
+MX_API int mx_linear_workspace_size(int64_t M, int64_t K, int64_t N, int recipe, size_t* ctx_bytes,
+                                    size_t* scratch_bytes);
+MX_API int mx_linear_fwd(const void* x, const void* w, int64_t M, int64_t K, int64_t N, int recipe, void* ctx,
+                         void* scratch, void* out, int32_t* err_word, void* stream);
+MX_API int mx_linear_bwd(const void* ctx, const void* dout, const void* w, int64_t M, int64_t K, int64_t N,
+                         int recipe, void* scratch, void* dx, void* dw, int32_t* err_word, void* stream);
+
+/*
  * mx_token_group_pad - the padded expert-major row layout that the grouped
  * entry points take, built on the device from routing decisions ("[mxfp8]
  * refactor model converter; use token group padding kernels in torchao",

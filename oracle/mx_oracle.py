@@ -690,16 +690,18 @@ def e4m3_code_distance(c1, c2) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 
-def linear_fwd(x, w):
+def linear_fwd(x, w, rounded: bool = True):
     """out = RN_bf16(x . w^T) with x [M,K] and w [N,K] both quantized MX(R)
-    along K (the per-linear MXFP8 path, reading R13).  Pinned in
+    along K (the per-linear MXFP8 path, reading R13); rounded=False returns
+    the exact float64 product before the bf16 rounding.  Pinned in
     tests/test_oracle_linear.py."""
     xq, xs = quantize_rows(np.asarray(x, dtype=np.uint16))
     wq, ws = quantize_rows(np.asarray(w, dtype=np.uint16))
-    return round_to_bf16_bits(mx_mm(xq, xs, wq, ws))
+    out = mx_mm(xq, xs, wq, ws)
+    return round_to_bf16_bits(out) if rounded else out
 
 
-def linear_bwd(x, w, dout, recipe=RECIPE_RCEIL):
+def linear_bwd(x, w, dout, recipe=RECIPE_RCEIL, rounded: bool = True):
     """Gradients of out = x . w^T (reading R13).
 
     dx = RN_bf16(dout . w): dout MX(R) along N, w MX(C) along N.
@@ -711,13 +713,15 @@ def linear_bwd(x, w, dout, recipe=RECIPE_RCEIL):
     dout = np.asarray(dout, dtype=np.uint16)
     dq, ds = quantize_rows(dout)
     wq_c, ws_c = quantize_cols(w)                        # [K, N], blocks along N
-    dx = round_to_bf16_bits(mx_mm(dq, ds, wq_c, ws_c))
+    dx = mx_mm(dq, ds, wq_c, ws_c)
     if recipe == RECIPE_RCEIL_WGRAD_HP:
-        dw = round_to_bf16_bits(bf16_mm(dout.T, x.T))
+        dw = bf16_mm(dout.T, x.T)
     else:
         dq_c, ds_c = quantize_cols(dout)                 # [N, M], blocks along M
         xq_c, xs_c = quantize_cols(x)                    # [K, M]
-        dw = round_to_bf16_bits(mx_mm(dq_c, ds_c, xq_c, xs_c))
+        dw = mx_mm(dq_c, ds_c, xq_c, xs_c)
+    if rounded:
+        return round_to_bf16_bits(dx), round_to_bf16_bits(dw)
     return dx, dw
 
 

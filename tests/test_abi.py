@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = _declared()
     for want in ["mx_quantize", "mx_swiglu_quant", "mx_swiglu_quant_bwd", "mx_scaled_mm", "mx_grouped_mm",
                  "mx_bf16_wgrad", "mx_mlp_workspace_size", "mx_mlp_fwd", "mx_mlp_bwd",
-                 "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows"]:
+                 "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows",
+                 "mx_linear_workspace_size", "mx_linear_fwd", "mx_linear_bwd"]:
         assert want in names
 
 
@@ -94,6 +95,18 @@ def test_token_group_pad_rejects_bad_arguments(L):
     assert L.mx_gather_rows(p, 10, 12, p, 10, 1, p, None, None) == 4                      # cols % 8
     assert L.mx_gather_rows(p, 10, 16, p, 10, 0, p, None, None) == 1                      # div 0
     assert L.mx_gather_rows(ctypes.c_void_p(0x1008), 10, 16, p, 10, 1, p, None, None) == 2  # alignment
+
+
+def test_linear_rejects_bad_arguments(L):
+    p = _fake()
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.mx_linear_workspace_size(256, 384, 512, 0, ctypes.byref(c), ctypes.byref(s)) == 0
+    assert c.value >= 384 * 256 and s.value >= 256 * 384 + 512 * 384
+    assert L.mx_linear_workspace_size(256, 384, 500, 0, ctypes.byref(c), ctypes.byref(s)) == 4   # N % 128
+    assert L.mx_linear_fwd(p, p, 256, 384, 512, 7, p, p, p, None, None) == 1                     # recipe
+    assert L.mx_linear_fwd(p, None, 256, 384, 512, 0, p, p, p, None, None) == 1                  # no w
+    assert L.mx_linear_bwd(p, p, p, 0, 384, 512, 0, p, p, p, None, None) == 1                    # M = 0
+    assert L.mx_linear_bwd(p, p, ctypes.c_void_p(0x10008), 256, 384, 512, 0, p, p, p, None, None) == 2
 
 
 def test_python_binding_fails_loudly_without_cuda_tensors():
