@@ -328,6 +328,8 @@ def run_gpu(args, rank, world, dev):
     }
     if w["kind"] == "grouped":
         res["dispatch"] = dispatch_measure(mx, w, dev, peaks["hbm_gbs"])
+    if w["kind"] == "dense" and not args.no_quant_sweep and rank == 0:
+        res["linear_lm_head"] = linear_measure(mx, dev, mx_peak)
     if not args.no_quant_sweep and rank == 0:
         res["quant_sweep"] = quant_sweep_measure(mx, dev, peaks["hbm_gbs"])
     return res
@@ -385,6 +387,32 @@ def quant_sweep_measure(mx, dev, hbm_gbs, iters=5):
         del x
         torch.cuda.empty_cache()
     return out
+
+
+def linear_measure(mx, dev, mx_peak, iters=3):
+    """The per-linear MXFP8 path at a Llama-3 lm_head (8192 tokens, 4096 ->
+    128256), default recipe: forward + backward TFLOP/s (6 M K N FLOP)."""
+    M, K, N = 8192, 4096, 128256
+    x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+    wt = (torch.randn((N, K), device=dev) * 0.02).to(torch.bfloat16)
+    dout = torch.randn((M, N), device=dev).to(torch.bfloat16)
+    c, s = mx.ctypes.c_size_t(), mx.ctypes.c_size_t()
+    L, P = mx.lib(), mx._ptr
+    mx._check(L.mx_linear_workspace_size(M, K, N, mx.RECIPE_RCEIL, mx.ctypes.byref(c), mx.ctypes.byref(s)))
+    ctx = torch.empty(c.value, dtype=torch.uint8, device=dev)
+    scratch = torch.empty(s.value, dtype=torch.uint8, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dx, dw = torch.empty_like(x), torch.empty_like(wt)
+
+    def step():
+        mx._check(L.mx_linear_fwd(P(x), P(wt), M, K, N, mx.RECIPE_RCEIL, P(ctx), P(scratch), P(out), None,
+                                  mx._stream()))
+        mx._check(L.mx_linear_bwd(P(ctx), P(dout), P(wt), M, K, N, mx.RECIPE_RCEIL, P(scratch), P(dx), P(dw), None,
+                                  mx._stream()))
+    ms = _event_ms(step, iters)
+    tf = 6.0 * M * K * N / (ms * 1e-3) / 1e12
+    return {"shape_MKN": [M, K, N], "ms_fwd_bwd": round(ms, 3), "tflops": round(tf, 1),
+            "frac": round(tf / mx_peak, 4), "recipe": "rceil"}
 
 
 def kernel_breakdown(mx, w, t, offs, recipe, dev, steps):
