@@ -58,6 +58,13 @@ R12 Token-group padding ("[mxfp8] refactor model converter; use token group
     is the cumulative padded end of group e; padded rows past offs[E-1] up
     to the buffer's capacity (the tail) are zero as well.  A routed row's
     activations are those of token r // topk.
+R14 FLOOR scale mode (the pages name ScaleCalculationMode.RCEIL as one mode
+    of several, defining none): the shared exponent of the OCP MX v1.0
+    conversion, e = floor(log2(amax)) - 8 (8 = the exponent of E4M3's largest
+    power of two), clamped to [-127, 127], byte e + 127; zero and non-finite
+    blocks as in R1; elements as in R2, where saturation now binds (scaled
+    values in (448, 512) become +-448).  Recipes "floor" and
+    "floor_wgrad_hp" use it for every quantization of the MLP and linear.
 R13 Per-linear MXFP8 path ("TrainingWeightWrapperTensor base class ...",
     linear override; "Add MXFP8 fused-MLP overrides in torchtitan": non-MLP
     linears keep the per-linear MXFP8 path): out = x w^T with both operands
@@ -161,6 +168,20 @@ def e8m0_rceil(amax) -> np.ndarray:
     return out
 
 
+def e8m0_floor(amax) -> np.ndarray:
+    """Reading R14: e = floor(log2 amax) - 8, clamped; byte e + 127; zero
+    amax -> 0x00, non-finite -> 0xFF.  Pinned exhaustively over every
+    non-negative bf16 amax in tests/test_oracle_floor.py."""
+    amax = np.asarray(amax, dtype=np.float64)
+    out = np.full(amax.shape, 255, dtype=np.uint8)
+    fin = np.isfinite(amax)
+    a = amax[fin]
+    _, ex = np.frexp(a)                       # a = m 2^ex, m in [0.5, 1): floor(log2 a) = ex - 1
+    e = np.where(a > 0, ex - 1 - 8, -127)
+    out[fin] = (np.clip(e, -127, 127) + 127).astype(np.uint8)
+    return out
+
+
 def e4m3_encode(v) -> np.ndarray:
     """Reading R2: RNE onto the E4M3fn grid (bias 7, subnormal quantum 2^-9,
     max 448), saturating to +-448, sign of zero kept, NaN -> 0x7F.
@@ -217,8 +238,12 @@ def e4m3_decode(codes) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 
-def quantize_rows(bits):
-    """MX(R): 32-element blocks along the last axis.
+SCALE_RCEIL = "rceil"
+SCALE_FLOOR = "floor"
+
+
+def quantize_rows(bits, scale: str = SCALE_RCEIL):
+    """MX(R): 32-element blocks along the last axis (scale mode R1 or R14).
 
     bits: bf16 bit patterns [..., C] with C % 32 == 0.
     Returns (codes uint8 [..., C], scales uint8 [..., C/32]) in the linear
@@ -229,7 +254,7 @@ def quantize_rows(bits):
     assert C % BLOCK == 0
     v = bf16_to_f64(bits).reshape(bits.shape[:-1] + (C // BLOCK, BLOCK))
     amax = np.max(np.abs(v), axis=-1)        # NaN propagates
-    s = e8m0_rceil(amax)
+    s = e8m0_floor(amax) if scale == SCALE_FLOOR else e8m0_rceil(amax)
     e = s.astype(np.int64) - 127
     scaled = np.ldexp(v, -e[..., None])      # exact power-of-two scaling
     codes = e4m3_encode(scaled)
@@ -238,11 +263,11 @@ def quantize_rows(bits):
     return codes.reshape(bits.shape), s
 
 
-def quantize_cols(bits):
+def quantize_cols(bits, scale: str = SCALE_RCEIL):
     """MX(C) of X[R,C] = MX(R) of X^T (reading R3): codes [C,R], scales [C,R/32].
     Leading batch axes (experts) are kept."""
     bits = np.asarray(bits, dtype=np.uint16)
-    return quantize_rows(np.swapaxes(bits, -1, -2))
+    return quantize_rows(np.swapaxes(bits, -1, -2), scale)
 
 
 def dequantize(codes, scales) -> np.ndarray:
@@ -565,6 +590,17 @@ def bf16_grouped_mm_k(a_bits, b_bits, offs) -> np.ndarray:
 
 RECIPE_RCEIL = "rceil"
 RECIPE_RCEIL_WGRAD_HP = "wgrad_hp"
+RECIPE_FLOOR = "floor"
+RECIPE_FLOOR_WGRAD_HP = "floor_wgrad_hp"
+
+
+def recipe_hp(recipe) -> bool:
+    """Weight-gradient GEMMs in bf16 (wgrad_with_hp)."""
+    return recipe in (RECIPE_RCEIL_WGRAD_HP, RECIPE_FLOOR_WGRAD_HP)
+
+
+def recipe_scale(recipe) -> str:
+    return SCALE_FLOOR if recipe in (RECIPE_FLOOR, RECIPE_FLOOR_WGRAD_HP) else SCALE_RCEIL
 
 
 def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL):
@@ -579,10 +615,11 @@ def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL):
     """
     x = np.asarray(x, dtype=np.uint16)
     grouped = offs is not None
+    sc = recipe_scale(recipe)
     w13 = np.concatenate([w1, w3], axis=-2)          # [.., 2h, d]
-    xq, xs = quantize_rows(x)
-    w13q, w13s = quantize_rows(w13)
-    w2q, w2s = quantize_rows(w2)
+    xq, xs = quantize_rows(x, sc)
+    w13q, w13s = quantize_rows(w13, sc)
+    w2q, w2s = quantize_rows(w2, sc)
     if grouped:
         h13_f = mx_grouped_mm_m(xq, xs, w13q, w13s, offs)
     else:
@@ -590,7 +627,7 @@ def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL):
     h13 = round_to_bf16_bits(h13_f)
     g, u = split_h13(h13)
     y = swiglu_fwd(g, u)
-    yq, ys = quantize_rows(y)
+    yq, ys = quantize_rows(y, sc)
     if grouped:
         out_f = mx_grouped_mm_m(yq, ys, w2q, w2s, offs)
     else:
@@ -598,9 +635,9 @@ def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL):
     out = round_to_bf16_bits(out_f)
     res = dict(xq=xq, xs=xs, w13q=w13q, w13s=w13s, h13_f=h13_f, h13=h13, y=y,
                yq=yq, ys=ys, w2q=w2q, w2s=w2s, out_f=out_f, out=out)
-    if recipe == RECIPE_RCEIL:
-        res["yq_c"], res["ys_c"] = quantize_cols(y)
-        res["xq_c"], res["xs_c"] = quantize_cols(x)
+    if not recipe_hp(recipe):
+        res["yq_c"], res["ys_c"] = quantize_cols(y, sc)
+        res["xq_c"], res["xs_c"] = quantize_cols(x, sc)
     return res
 
 
@@ -620,9 +657,10 @@ def mlp_bwd(x, w1, w3, w2, dout, offs=None, recipe=RECIPE_RCEIL, fwd=None):
     dout = np.asarray(dout, dtype=np.uint16)
     w13 = np.concatenate([w1, w3], axis=-2)
     h = np.asarray(w1).shape[-2]
-    dq, ds = quantize_rows(dout)
-    w2q_c, w2s_c = quantize_cols(w2)                 # [.., h, d]
-    w13q_c, w13s_c = quantize_cols(w13)              # [.., d, 2h]
+    sc = recipe_scale(recipe)
+    dq, ds = quantize_rows(dout, sc)
+    w2q_c, w2s_c = quantize_cols(w2, sc)             # [.., h, d]
+    w13q_c, w13s_c = quantize_cols(w13, sc)          # [.., d, 2h]
     if grouped:
         dy_f = mx_grouped_mm_m(dq, ds, w2q_c, w2s_c, offs)
     else:
@@ -631,7 +669,7 @@ def mlp_bwd(x, w1, w3, w2, dout, offs=None, recipe=RECIPE_RCEIL, fwd=None):
     g, u = split_h13(fwd["h13"])
     dg, du = swiglu_bwd(dy, g, u)
     dh13 = np.concatenate([dg, du], axis=-1)
-    dhq, dhs = quantize_rows(dh13)
+    dhq, dhs = quantize_rows(dh13, sc)
     if grouped:
         dx_f = mx_grouped_mm_m(dhq, dhs, w13q_c, w13s_c, offs)
     else:
@@ -641,9 +679,9 @@ def mlp_bwd(x, w1, w3, w2, dout, offs=None, recipe=RECIPE_RCEIL, fwd=None):
                dy_f=dy_f, dy=dy, dg=dg, du=du, dh13=dh13, dhq=dhq, dhs=dhs,
                dx_f=dx_f, dx=dx)
     go = offs if grouped else np.array([x.shape[0]], dtype=np.int32)
-    if recipe == RECIPE_RCEIL:
-        dq_c, ds_c = quantize_cols(dout)             # [d, M]
-        dhq_c, dhs_c = quantize_cols(dh13)           # [2h, M]
+    if not recipe_hp(recipe):
+        dq_c, ds_c = quantize_cols(dout, sc)         # [d, M]
+        dhq_c, dhs_c = quantize_cols(dh13, sc)       # [2h, M]
         dw2_f = mx_grouped_mm_k(dq_c, ds_c, fwd["yq_c"], fwd["ys_c"], go)
         dw13_f = mx_grouped_mm_k(dhq_c, dhs_c, fwd["xq_c"], fwd["xs_c"], go)
         res.update(dq_c=dq_c, ds_c=ds_c, dhq_c=dhq_c, dhs_c=dhs_c)
@@ -690,13 +728,13 @@ def e4m3_code_distance(c1, c2) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 
-def linear_fwd(x, w, rounded: bool = True):
+def linear_fwd(x, w, rounded: bool = True, recipe=RECIPE_RCEIL):
     """out = RN_bf16(x . w^T) with x [M,K] and w [N,K] both quantized MX(R)
     along K (the per-linear MXFP8 path, reading R13); rounded=False returns
     the exact float64 product before the bf16 rounding.  Pinned in
     tests/test_oracle_linear.py."""
-    xq, xs = quantize_rows(np.asarray(x, dtype=np.uint16))
-    wq, ws = quantize_rows(np.asarray(w, dtype=np.uint16))
+    xq, xs = quantize_rows(np.asarray(x, dtype=np.uint16), recipe_scale(recipe))
+    wq, ws = quantize_rows(np.asarray(w, dtype=np.uint16), recipe_scale(recipe))
     out = mx_mm(xq, xs, wq, ws)
     return round_to_bf16_bits(out) if rounded else out
 
@@ -711,14 +749,15 @@ def linear_bwd(x, w, dout, recipe=RECIPE_RCEIL, rounded: bool = True):
     x = np.asarray(x, dtype=np.uint16)
     w = np.asarray(w, dtype=np.uint16)
     dout = np.asarray(dout, dtype=np.uint16)
-    dq, ds = quantize_rows(dout)
-    wq_c, ws_c = quantize_cols(w)                        # [K, N], blocks along N
+    sc = recipe_scale(recipe)
+    dq, ds = quantize_rows(dout, sc)
+    wq_c, ws_c = quantize_cols(w, sc)                    # [K, N], blocks along N
     dx = mx_mm(dq, ds, wq_c, ws_c)
-    if recipe == RECIPE_RCEIL_WGRAD_HP:
+    if recipe_hp(recipe):
         dw = bf16_mm(dout.T, x.T)
     else:
-        dq_c, ds_c = quantize_cols(dout)                 # [N, M], blocks along M
-        xq_c, xs_c = quantize_cols(x)                    # [K, M]
+        dq_c, ds_c = quantize_cols(dout, sc)             # [N, M], blocks along M
+        xq_c, xs_c = quantize_cols(x, sc)                # [K, M]
         dw = mx_mm(dq_c, ds_c, xq_c, xs_c)
     if rounded:
         return round_to_bf16_bits(dx), round_to_bf16_bits(dw)
