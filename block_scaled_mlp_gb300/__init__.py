@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "MxError", "lib", "library_path", "ROW", "COL", "BOTH", "SCALE_LINEAR", "SCALE_MMA",
-    "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "GROUP_M", "GROUP_K", "mma_scale_bytes",
+    "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "RECIPE_FLOOR", "RECIPE_FLOOR_WGRAD_HP", "SCALE_RCEIL", "SCALE_FLOOR", "GROUP_M", "GROUP_K", "mma_scale_bytes",
     "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
     "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
     "token_group_pad", "token_group_capacity", "gather_rows", "linear_fwd", "linear_bwd", "LinearContext",
@@ -30,7 +30,8 @@ __all__ = [
 
 ROW, COL, BOTH = 1, 2, 3
 SCALE_LINEAR, SCALE_MMA = 0, 1
-RECIPE_RCEIL, RECIPE_RCEIL_WGRAD_HP = 0, 1
+RECIPE_RCEIL, RECIPE_RCEIL_WGRAD_HP, RECIPE_FLOOR, RECIPE_FLOOR_WGRAD_HP = 0, 1, 2, 3
+SCALE_RCEIL, SCALE_FLOOR = 0, 1
 GROUP_M, GROUP_K = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -43,8 +44,11 @@ _SIGS = {
     "mx_status_string": ([_I], ctypes.c_char_p),
     "mx_last_error": ([], ctypes.c_char_p),
     "mx_quantize": ([_V, _I64, _I64, _I, _I, _V, _V, _V, _V, _V], _I),
+    "mx_quantize_mode": ([_V, _I64, _I64, _I, _I, _I, _V, _V, _V, _V, _V], _I),
     "mx_swiglu_quant": ([_V, _I64, _I64, _I, _I, _V, _V, _V, _V, _V], _I),
     "mx_swiglu_quant_bwd": ([_V, _V, _I64, _I64, _I, _I, _V, _V, _V, _V, _V, _V, _V], _I),
+    "mx_swiglu_quant_mode": ([_V, _I64, _I64, _I, _I, _I, _V, _V, _V, _V, _V], _I),
+    "mx_swiglu_quant_bwd_mode": ([_V, _V, _I64, _I64, _I, _I, _I, _V, _V, _V, _V, _V, _V, _V], _I),
     "mx_scaled_mm": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _V, _V], _I),
     "mx_grouped_mm": ([_I, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _V, _V, _V], _I),
     "mx_bf16_wgrad": ([_V, _V, _I64, _I64, _I64, _V, _I32, _I32, _V, _V, _V], _I),
@@ -143,7 +147,7 @@ class ErrorWord:
 # ---------------------------------------------------------------- per-op calls
 
 
-def quantize(x, axis=BOTH, layout=SCALE_MMA):
+def quantize(x, axis=BOTH, layout=SCALE_MMA, scale_mode=SCALE_RCEIL):
     """MXFP8 cast of a bf16 [rows, cols] matrix.  Returns a dict with
     q_row [rows, cols], s_row, q_col [cols, rows], s_col (absent axes None)."""
     _need(x, torch.bfloat16, "x")
@@ -156,12 +160,12 @@ def quantize(x, axis=BOTH, layout=SCALE_MMA):
     if axis & COL:
         out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
         out["s_col"] = _scales(cols, rows, layout, dev)
-    _check(lib().mx_quantize(_ptr(x), rows, cols, axis, layout, _ptr(out["q_row"]), _ptr(out["s_row"]),
-                             _ptr(out["q_col"]), _ptr(out["s_col"]), _stream()))
+    _check(lib().mx_quantize_mode(_ptr(x), rows, cols, axis, layout, scale_mode, _ptr(out["q_row"]),
+                                  _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]), _stream()))
     return out
 
 
-def swiglu_quant(h13, axis=BOTH, layout=SCALE_MMA):
+def swiglu_quant(h13, axis=BOTH, layout=SCALE_MMA, scale_mode=SCALE_RCEIL):
     """Fused SwiGLU of h13 [M, 2h] = [g | u] with dual MXFP8 quantization of
     y [M, h].  Returns dict(q_row [M,h], s_row, q_col [h,M], s_col)."""
     _need(h13, torch.bfloat16, "h13")
@@ -173,12 +177,12 @@ def swiglu_quant(h13, axis=BOTH, layout=SCALE_MMA):
     if axis & COL:
         out["q_col"] = torch.empty((h, M), dtype=torch.uint8, device=dev)
         out["s_col"] = _scales(h, M, layout, dev)
-    _check(lib().mx_swiglu_quant(_ptr(h13), M, h, axis, layout, _ptr(out["q_row"]), _ptr(out["s_row"]),
-                                 _ptr(out["q_col"]), _ptr(out["s_col"]), _stream()))
+    _check(lib().mx_swiglu_quant_mode(_ptr(h13), M, h, axis, layout, scale_mode, _ptr(out["q_row"]),
+                                      _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]), _stream()))
     return out
 
 
-def swiglu_quant_bwd(dy, h13, axis=BOTH, layout=SCALE_MMA, bf16_transposed=False):
+def swiglu_quant_bwd(dy, h13, axis=BOTH, layout=SCALE_MMA, bf16_transposed=False, scale_mode=SCALE_RCEIL):
     """Fused SwiGLU backward: dh13 = [dg | du] quantized rowwise (and
     columnwise with axis=BOTH).  With bf16_transposed=True (rowwise only) it
     also returns dh13_t [2h, M] and y_t [h, M] in bf16."""
@@ -194,9 +198,9 @@ def swiglu_quant_bwd(dy, h13, axis=BOTH, layout=SCALE_MMA, bf16_transposed=False
     if bf16_transposed:
         out["dh13_t"] = torch.empty((2 * h, M), dtype=torch.bfloat16, device=dev)
         out["y_t"] = torch.empty((h, M), dtype=torch.bfloat16, device=dev)
-    _check(lib().mx_swiglu_quant_bwd(_ptr(dy), _ptr(h13), M, h, axis, layout, _ptr(out["q_row"]),
-                                     _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]),
-                                     _ptr(out["dh13_t"]), _ptr(out["y_t"]), _stream()))
+    _check(lib().mx_swiglu_quant_bwd_mode(_ptr(dy), _ptr(h13), M, h, axis, layout, scale_mode, _ptr(out["q_row"]),
+                                          _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]),
+                                          _ptr(out["dh13_t"]), _ptr(out["y_t"]), _stream()))
     return out
 
 

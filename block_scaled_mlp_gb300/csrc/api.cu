@@ -76,6 +76,11 @@ namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// recipes: bit 0 = bf16 weight gradients (wgrad_with_hp), bit 1 = FLOOR scales
+inline bool valid_recipe(int r) { return r >= MX_RECIPE_RCEIL && r <= MX_RECIPE_FLOOR_WGRAD_HP; }
+inline bool recipe_hp(int r) { return r == MX_RECIPE_RCEIL_WGRAD_HP || r == MX_RECIPE_FLOOR_WGRAD_HP; }
+inline int recipe_floor(int r) { return r == MX_RECIPE_FLOOR || r == MX_RECIPE_FLOOR_WGRAD_HP; }
+
 inline int64_t mma_scale_bytes(int64_t rows, int64_t cols) {
   const int64_t S = cols / 32;
   return ((rows + 127) / 128) * ((S + 3) / 4) * 512;
@@ -117,7 +122,7 @@ struct MlpBuffers {
 
 MlpBuffers carve(void* ctx, void* scratch, int64_t M, int64_t d, int64_t h, int64_t Ew, int recipe) {
   MlpBuffers b{};
-  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  const bool hp = recipe_hp(recipe);
   Arena c(ctx);
   b.h13 = c.take(M * 2 * h * 2);
   if (hp) {
@@ -174,8 +179,7 @@ int check_mlp_args(const void* x, const void* w1, const void* w3, const void* w2
   if (M % 128 || d % 128 || h % 128)
     return fail(MX_ERR_UNSUPPORTED, "M_total, d and h must be multiples of 128 (got %lld, %lld, %lld)",
                 (long long)M, (long long)d, (long long)h);
-  if (recipe != MX_RECIPE_RCEIL && recipe != MX_RECIPE_RCEIL_WGRAD_HP)
-    return fail(MX_ERR_INVALID_ARG, "unknown recipe %d", recipe);
+  if (!valid_recipe(recipe)) return fail(MX_ERR_INVALID_ARG, "unknown recipe %d", recipe);
   if (offs) {
     if (E < 1 || E > 1024) return fail(MX_ERR_INVALID_ARG, "E must be in [1, 1024]");
     if (pad != 128) return fail(MX_ERR_UNSUPPORTED, "pad_multiple must be 128");
@@ -198,7 +202,7 @@ struct LinearBuffers {
 
 LinearBuffers carve_linear(void* ctx, void* scratch, int64_t M, int64_t K, int64_t N, int recipe) {
   LinearBuffers b{};
-  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  const bool hp = recipe_hp(recipe);
   Arena c(ctx);
   if (hp) {
     b.x_t = c.take(K * M * 2);
@@ -232,8 +236,7 @@ int check_linear_args(int64_t M, int64_t K, int64_t N, int recipe) {
   if (M % 128 || K % 128 || N % 128)
     return fail(MX_ERR_UNSUPPORTED, "M, K and N must be multiples of 128 (got %lld, %lld, %lld)", (long long)M,
                 (long long)K, (long long)N);
-  if (recipe != MX_RECIPE_RCEIL && recipe != MX_RECIPE_RCEIL_WGRAD_HP)
-    return fail(MX_ERR_INVALID_ARG, "unknown recipe %d", recipe);
+  if (!valid_recipe(recipe)) return fail(MX_ERR_INVALID_ARG, "unknown recipe %d", recipe);
   if (M > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "dimension too large");
   return MX_OK;
 }
@@ -262,6 +265,13 @@ const char* mx_last_error(void) { return g_msg; }
 
 int mx_quantize(const void* x, int64_t rows, int64_t cols, int axis, int layout, void* q_row, void* s_row,
                 void* q_col, void* s_col, void* stream) {
+  return mx_quantize_mode(x, rows, cols, axis, layout, MX_SCALE_RCEIL, q_row, s_row, q_col, s_col, stream);
+}
+
+int mx_quantize_mode(const void* x, int64_t rows, int64_t cols, int axis, int layout, int scale_mode,
+                     void* q_row, void* s_row, void* q_col, void* s_col, void* stream) {
+  if (scale_mode != MX_SCALE_RCEIL && scale_mode != MX_SCALE_FLOOR)
+    return fail(MX_ERR_INVALID_ARG, "unknown scale mode %d", scale_mode);
   if (!x) return fail(MX_ERR_INVALID_ARG, "x is null");
   if (rows <= 0 || cols <= 0) return fail(MX_ERR_INVALID_ARG, "rows and cols must be positive");
   if (axis < MX_ROW || axis > MX_BOTH) return fail(MX_ERR_INVALID_ARG, "axis must be MX_ROW, MX_COL or MX_BOTH");
@@ -283,11 +293,19 @@ int mx_quantize(const void* x, int64_t rows, int64_t cols, int axis, int layout,
   q.q_row = row ? q_row : nullptr; q.s_row = row ? s_row : nullptr;
   q.q_col = col ? q_col : nullptr; q.s_col = col ? s_col : nullptr;
   q.qc_ld = rows; q.qc_off = 0; q.qc_bs = 0; q.sc_bs = 0;
+  q.floor_scale = scale_mode == MX_SCALE_FLOOR;
   return launch_quant(q, st);
 }
 
 int mx_swiglu_quant(const void* h13, int64_t M, int64_t h, int axis, int layout, void* yq_row, void* ys_row,
                     void* yq_col, void* ys_col, void* stream) {
+  return mx_swiglu_quant_mode(h13, M, h, axis, layout, MX_SCALE_RCEIL, yq_row, ys_row, yq_col, ys_col, stream);
+}
+
+int mx_swiglu_quant_mode(const void* h13, int64_t M, int64_t h, int axis, int layout, int scale_mode,
+                         void* yq_row, void* ys_row, void* yq_col, void* ys_col, void* stream) {
+  if (scale_mode != MX_SCALE_RCEIL && scale_mode != MX_SCALE_FLOOR)
+    return fail(MX_ERR_INVALID_ARG, "unknown scale mode %d", scale_mode);
   if (!h13) return fail(MX_ERR_INVALID_ARG, "h13 is null");
   if (M <= 0 || h <= 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
   if (axis < MX_ROW || axis > MX_BOTH) return fail(MX_ERR_INVALID_ARG, "bad axis");
@@ -306,12 +324,22 @@ int mx_swiglu_quant(const void* h13, int64_t M, int64_t h, int axis, int layout,
   s.h13 = h13; s.M = M; s.h = h; s.layout = layout;
   s.q_row = yq_row; s.s_row = ys_row;
   s.q_col = col ? yq_col : nullptr; s.s_col = col ? ys_col : nullptr;
+  s.floor_scale = scale_mode == MX_SCALE_FLOOR;
   return launch_swiglu_fwd(s, st);
 }
 
 int mx_swiglu_quant_bwd(const void* dy, const void* h13, int64_t M, int64_t h, int axis, int layout,
                         void* dq_row, void* ds_row, void* dq_col, void* ds_col, void* dh13_t, void* y_t,
                         void* stream) {
+  return mx_swiglu_quant_bwd_mode(dy, h13, M, h, axis, layout, MX_SCALE_RCEIL, dq_row, ds_row, dq_col, ds_col,
+                                  dh13_t, y_t, stream);
+}
+
+int mx_swiglu_quant_bwd_mode(const void* dy, const void* h13, int64_t M, int64_t h, int axis, int layout,
+                             int scale_mode, void* dq_row, void* ds_row, void* dq_col, void* ds_col, void* dh13_t,
+                             void* y_t, void* stream) {
+  if (scale_mode != MX_SCALE_RCEIL && scale_mode != MX_SCALE_FLOOR)
+    return fail(MX_ERR_INVALID_ARG, "unknown scale mode %d", scale_mode);
   if (!dy || !h13) return fail(MX_ERR_INVALID_ARG, "dy or h13 is null");
   if (M <= 0 || h <= 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
   if (axis < MX_ROW || axis > MX_BOTH) return fail(MX_ERR_INVALID_ARG, "bad axis");
@@ -333,6 +361,7 @@ int mx_swiglu_quant_bwd(const void* dy, const void* h13, int64_t M, int64_t h, i
   s.q_row = dq_row; s.s_row = ds_row;
   s.q_col = col ? dq_col : nullptr; s.s_col = col ? ds_col : nullptr;
   s.dh13_t = dh13_t; s.y_t = y_t;
+  s.floor_scale = scale_mode == MX_SCALE_FLOOR;
   return launch_swiglu_bwd(s, st);
 }
 
@@ -397,7 +426,7 @@ int mx_mlp_workspace_size(int64_t M_total, int64_t d, int64_t h, int32_t E, int 
                           size_t* scratch_bytes) {
   if (!ctx_bytes || !scratch_bytes) return fail(MX_ERR_INVALID_ARG, "null output pointer");
   if (M_total <= 0 || d <= 0 || h <= 0 || E < 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
-  if (recipe != MX_RECIPE_RCEIL && recipe != MX_RECIPE_RCEIL_WGRAD_HP) return fail(MX_ERR_INVALID_ARG, "unknown recipe");
+  if (!valid_recipe(recipe)) return fail(MX_ERR_INVALID_ARG, "unknown recipe");
   const MlpBuffers b = carve(nullptr, nullptr, M_total, d, h, E > 0 ? E : 1, recipe);
   *ctx_bytes = b.ctx_bytes;
   *scratch_bytes = b.scratch_bytes;
@@ -412,13 +441,15 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
   if (!out || !aligned16(out)) return fail(out ? MX_ERR_ALIGNMENT : MX_ERR_INVALID_ARG, "bad out pointer");
   const bool grouped = offs != nullptr;
   const int64_t Ew = grouped ? E : 1;
-  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  const bool hp = recipe_hp(recipe);
+  const int fl = recipe_floor(recipe);
   cudaStream_t st = (cudaStream_t)stream;
   MlpBuffers b = carve(ctx, scratch, M, d, h, Ew, recipe);
 
   // F1: x -> rowwise MX (+ columnwise MX, or bf16 transpose for the HP recipe)
   {
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = x; q.rows = M; q.cols = d; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.xq_r; q.s_row = b.xs_r;
     if (hp) { q.t_col = b.x_t; q.tc_ld = M; }
@@ -428,6 +459,7 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
   // F2: w1, w3 -> packed w13 rowwise [2h, d] and columnwise [d, 2h], per expert
   for (int half = 0; half < 2; ++half) {
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = half ? w3 : w1; q.rows = h; q.cols = d; q.batch = (int32_t)Ew; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.w13q_r + half * h * d;
     q.s_row = b.w13s_r + half * (h / 128) * (d / 128) * 512;
@@ -448,6 +480,7 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
   // F4: y = SwiGLU(h13) -> rowwise MX (+ columnwise MX for the default recipe)
   {
     SwigluLaunch s{};
+    s.floor_scale = fl;
     s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
     s.q_row = b.yq_r; s.s_row = b.ys_r;
     if (!hp) { s.q_col = b.yq_c; s.s_col = b.ys_c; }
@@ -456,6 +489,7 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
   // F5: w2 -> rowwise [d, h] and columnwise [h, d], per expert
   {
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = w2; q.rows = d; q.cols = h; q.batch = (int32_t)Ew; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.w2q_r; q.s_row = b.w2s_r;
     q.q_col = b.w2q_c; q.s_col = b.w2s_c;
@@ -483,13 +517,15 @@ int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const void* w1,
     return fail(MX_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
   const bool grouped = offs != nullptr;
   const int64_t Ew = grouped ? E : 1;
-  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  const bool hp = recipe_hp(recipe);
+  const int fl = recipe_floor(recipe);
   cudaStream_t st = (cudaStream_t)stream;
   MlpBuffers b = carve(const_cast<void*>(ctx), scratch, M, d, h, Ew, recipe);
 
   // B1: dout -> rowwise MX (+ columnwise MX, or bf16 transpose for HP)
   {
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = dout; q.rows = M; q.cols = d; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.dq_r; q.s_row = b.ds_r;
     if (hp) { q.t_col = b.dout_t; q.tc_ld = M; }
@@ -508,6 +544,7 @@ int mx_mlp_bwd(const void* ctx, const void* dout, const void* x, const void* w1,
   // transposed dh13 and y for HP)
   {
     SwigluLaunch s{};
+    s.floor_scale = fl;
     s.dy = b.dy; s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
     s.q_row = b.dhq_r; s.s_row = b.dhs_r;
     if (hp) { s.dh13_t = b.dh13_t; s.y_t = b.y_t; }
@@ -566,11 +603,13 @@ int mx_linear_fwd(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
   if (!x || !w || !ctx || !scratch || !out) return fail(MX_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(x) || !aligned16(w) || !aligned16(ctx) || !aligned16(scratch) || !aligned16(out))
     return fail(MX_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
-  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  const bool hp = recipe_hp(recipe);
+  const int fl = recipe_floor(recipe);
   cudaStream_t st = (cudaStream_t)stream;
   LinearBuffers b = carve_linear(ctx, scratch, M, K, N, recipe);
   {  // x -> MX(R) along K; MX(C) along M (or bf16 x^T) saved for the weight gradient
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = x; q.rows = M; q.cols = K; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.xq_r; q.s_row = b.xs_r;
     if (hp) { q.t_col = b.x_t; q.tc_ld = M; }
@@ -579,6 +618,7 @@ int mx_linear_fwd(const void* x, const void* w, int64_t M, int64_t K, int64_t N,
   }
   {  // w -> MX(R) along K
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = w; q.rows = N; q.cols = K; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.wq_r; q.s_row = b.ws_r;
     if ((rc = launch_quant(q, st))) return rc;
@@ -598,11 +638,13 @@ int mx_linear_bwd(const void* ctx, const void* dout, const void* w, int64_t M, i
   if (!aligned16(ctx) || !aligned16(dout) || !aligned16(w) || !aligned16(scratch) || !aligned16(dx) ||
       !aligned16(dw))
     return fail(MX_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
-  const bool hp = recipe == MX_RECIPE_RCEIL_WGRAD_HP;
+  const bool hp = recipe_hp(recipe);
+  const int fl = recipe_floor(recipe);
   cudaStream_t st = (cudaStream_t)stream;
   LinearBuffers b = carve_linear(const_cast<void*>(ctx), scratch, M, K, N, recipe);
   {  // dout -> MX(R) along N; MX(C) along M (or bf16 dout^T)
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = dout; q.rows = M; q.cols = N; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_row = b.dq_r; q.s_row = b.ds_r;
     if (hp) { q.t_col = b.dout_t; q.tc_ld = M; }
@@ -611,6 +653,7 @@ int mx_linear_bwd(const void* ctx, const void* dout, const void* w, int64_t M, i
   }
   {  // w -> MX(C) along N: codes [K, N]
     QuantLaunch q{};
+    q.floor_scale = fl;
     q.x = w; q.rows = N; q.cols = K; q.batch = 1; q.layout = MX_SCALE_MMA; q.err = err_word;
     q.q_col = b.wq_c; q.s_col = b.ws_c; q.qc_ld = N;
     if ((rc = launch_quant(q, st))) return rc;

@@ -390,12 +390,14 @@ MX_DEVINL uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_
 // the smallest e with amax <= 448 * 2^e is E-8 when the significand is at
 // most 1.75 (mantissa field <= 0x60) and E-7 otherwise (E = exponent field
 // minus bias); clamped below at 2^-127; NaN/Inf -> 0xFF.
-MX_DEVINL uint32_t e8m0_from_amax_bits(uint32_t amax_bits) {
+MX_DEVINL uint32_t e8m0_from_amax_bits(uint32_t amax_bits, uint32_t rceil = 1u) {
   const uint32_t E = (amax_bits >> 7) & 0xFF;
   const uint32_t m = amax_bits & 0x7F;
   if (E == 0xFF) return 0xFF;
   if (E == 0) return 0;
-  int s = (int)E - 8 + (m > 0x60 ? 1 : 0);
+  // RCEIL rounds the exponent up when amax / 2^E exceeds 448/256 = 1.75;
+  // FLOOR (rceil = 0) keeps floor(log2 amax) - 8 and lets codes saturate
+  int s = (int)E - 8 + ((m > 0x60 && rceil) ? 1 : 0);
   return s < 0 ? 0u : (uint32_t)s;
 }
 

@@ -39,6 +39,7 @@ struct QuantLaunch {
   // t_col[c*tc_ld + tc_off + r] (+ b*tc_bs)
   void* t_col;
   int64_t tc_ld, tc_off, tc_bs;
+  int floor_scale;   // 1: FLOOR E8M0 scales; 0 (default): RCEIL
   int32_t* err;
 };
 int launch_quant(const QuantLaunch& q, cudaStream_t stream);
@@ -53,6 +54,7 @@ struct SwigluLaunch {
   void* q_col; void* s_col;   // fwd: y cols [h,M]; bwd: dh13 cols [2h,M]
   void* dh13_t;               // bwd, optional: [2h, M] bf16
   void* y_t;                  // bwd, optional: [h, M] bf16
+  int floor_scale;            // 1: FLOOR E8M0 scales; 0 (default): RCEIL
   int32_t* err;
 };
 int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream);

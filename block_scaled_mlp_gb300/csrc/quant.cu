@@ -39,6 +39,7 @@ struct QuantKParams {
   ScaleDst s_col; int64_t sc_off; int64_t sc_bs;
   // columnwise bf16 transpose: dest [cols, *] bf16
   uint16_t* t_col; int64_t tc_ld; int64_t tc_off; int64_t tc_bs;
+  uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
   int32_t* err;
 };
 
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           pk[4 * k] = v.x; pk[4 * k + 1] = v.y; pk[4 * k + 2] = v.z; pk[4 * k + 3] = v.w;
         }
         uint32_t codes[8];
-        const uint32_t s = quant_row32(pk, codes);
+        const uint32_t s = quant_row32(pk, codes, p.rceil);
         const int64_t r = r0 + rr;
         const int64_t c = c0 + box * 64 + jj * 32;
         if (r < p.rows && c < p.cols) {
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           ScaleDst sd = p.s_col;
           sd.base += b * p.sc_bs;
           uint32_t ca[8], cb[8], sa, sb;
-          quant_col32x2(v, ca, cb, sa, sb);
+          quant_col32x2(v, ca, cb, sa, sb, p.rceil);
           uint8_t* dst = qcol + cg * p.qc_ld + p.qc_off + rg;
           store16(dst, ca[0], ca[1], ca[2], ca[3]);
           store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
@@ -210,6 +211,7 @@ int launch_quant(const QuantLaunch& q, cudaStream_t stream) {
   p.s_col = ScaleDst{(uint8_t*)q.s_col, (S_col + 3) / 4, S_col, q.layout == MX_SCALE_MMA};
   p.sc_off = q.qc_off / 32; p.sc_bs = q.sc_bs;
   p.t_col = (uint16_t*)q.t_col; p.tc_ld = q.tc_ld; p.tc_off = q.tc_off; p.tc_bs = q.tc_bs;
+  p.rceil = q.floor_scale ? 0u : 1u;
   p.err = q.err;
 
   const int64_t n_tiles = p.row_tiles * p.col_tiles * q.batch;

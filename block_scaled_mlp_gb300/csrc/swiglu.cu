@@ -64,14 +64,14 @@ MX_DEVINL int tile_word(int r, int pc) { return r * 128 + ((((pc >> 2) ^ (r & 7)
 
 // Row quantization of one 32-element block of a result tile: the 64-byte
 // half jj of row rr.
-MX_DEVINL uint32_t quant_tile_block(const uint8_t* tile, int rr, int jj, uint32_t (&codes)[8]) {
+MX_DEVINL uint32_t quant_tile_block(const uint8_t* tile, int rr, int jj, uint32_t (&codes)[8], uint32_t rceil) {
   uint32_t pk[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint4 v = *reinterpret_cast<const uint4*>(tile + tile_chunk(rr, jj * 4 + k));
     pk[4 * k] = v.x; pk[4 * k + 1] = v.y; pk[4 * k + 2] = v.z; pk[4 * k + 3] = v.w;
   }
-  return quant_row32(pk, codes);
+  return quant_row32(pk, codes, rceil);
 }
 
 MX_DEVINL void store32(uint8_t* dst, const uint32_t (&c)[8]) {
@@ -91,6 +91,7 @@ struct SwiFwdParams {
   int64_t row_tiles, col_tiles;
   uint8_t* q_row; ScaleDst s_row;
   uint8_t* q_col; ScaleDst s_col;
+  uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
   int32_t* err;
 };
 
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int base = w * 16; base < SF_R; base += nw * 16) {
           const int rr = base + (lane >> 3) * 4 + ((lane & 7) >> 1);
           uint32_t codes[8];
-          const uint32_t sc = quant_tile_block(yt, rr, jj, codes);
+          const uint32_t sc = quant_tile_block(yt, rr, jj, codes, p.rceil);
           const int64_t r = r0 + rr;
           const int64_t c = c0 + jj * 32;
           if (r < p.M) {
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(yt + tile_word(rb * 32 + i, pc));
         uint32_t ca[8], cb[8], sa, sb;
-        quant_col32x2(v, ca, cb, sa, sb);
+        quant_col32x2(v, ca, cb, sa, sb, p.rceil);
         const int64_t rg = r0 + rb * 32;
         if (rg < p.M) {
           const int64_t col = c0 + 2 * pc;
@@ -288,6 +289,7 @@ struct SwiBwdParams {
   uint8_t* q_col; ScaleDst s_col;   // [2h, M]
   uint16_t* dh13_t;                 // [2h, M]
   uint16_t* y_t;                    // [h, M]
+  uint32_t rceil;                   // 1: RCEIL scales, 0: FLOOR
   int32_t* err;
 };
 
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           const int kk = base + (lane >> 3) * 4 + ((lane & 7) >> 1);
           const int which = kk / SB_R, rr = kk % SB_R;
           uint32_t codes[8];
-          const uint32_t sc = quant_tile_block(ot + which * SB_BOX, rr, jj, codes);
+          const uint32_t sc = quant_tile_block(ot + which * SB_BOX, rr, jj, codes, p.rceil);
           const int64_t r = r0 + rr;
           const int64_t c = (which ? p.h : 0) + c0 + jj * 32;
           if (r < p.M) {
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(src + tile_word(rb * 32 + i, pc));
         uint32_t ca[8], cb[8], sa, sb;
-        quant_col32x2(v, ca, cb, sa, sb);
+        quant_col32x2(v, ca, cb, sa, sb, p.rceil);
         const int64_t rg = r0 + rb * 32;
         if (rg < p.M) {
           const int64_t orow = (which ? p.h : 0) + c0 + 2 * pc;
@@ -567,6 +569,7 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   const int64_t Sr = s.h / 32, Sc = s.M / 32;
   p.q_row = (uint8_t*)s.q_row; p.s_row = ScaleDst{(uint8_t*)s.s_row, (Sr + 3) / 4, Sr, mma};
   p.q_col = (uint8_t*)s.q_col; p.s_col = ScaleDst{(uint8_t*)s.s_col, (Sc + 3) / 4, Sc, mma};
+  p.rceil = s.floor_scale ? 0u : 1u;
   p.err = s.err;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
   if (n_tiles == 0) return MX_OK;
@@ -611,6 +614,7 @@ int launch_swiglu_bwd(const SwigluLaunch& s, cudaStream_t stream) {
   p.q_row = (uint8_t*)s.q_row; p.s_row = ScaleDst{(uint8_t*)s.s_row, (Sr + 3) / 4, Sr, mma};
   p.q_col = (uint8_t*)s.q_col; p.s_col = ScaleDst{(uint8_t*)s.s_col, (Sc + 3) / 4, Sc, mma};
   p.dh13_t = (uint16_t*)s.dh13_t; p.y_t = (uint16_t*)s.y_t;
+  p.rceil = s.floor_scale ? 0u : 1u;
   p.err = s.err;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
   if (n_tiles == 0) return MX_OK;

@@ -62,11 +62,11 @@ MX_DEVINL uint64_t splat_f32x2(float f) {
 // Quantize one whole 32-element block held by one thread as 16 packed bf16
 // pairs (element 2i in the low half of p[i]).  Writes the 32 codes as 8
 // words (element 0 in the lowest byte) and returns the scale byte.
-MX_DEVINL uint32_t quant_row32(const uint32_t (&p)[16], uint32_t (&codes)[8]) {
+MX_DEVINL uint32_t quant_row32(const uint32_t (&p)[16], uint32_t (&codes)[8], uint32_t rceil = 1u) {
   uint32_t m2 = abs2(p[0]);
 #pragma unroll
   for (int i = 1; i < 16; ++i) m2 = max2(m2, abs2(p[i]));
-  const uint32_t s = e8m0_from_amax_bits(max_halves(m2));
+  const uint32_t s = e8m0_from_amax_bits(max_halves(m2), rceil);
   if (s == 0xFF) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
@@ -82,11 +82,11 @@ MX_DEVINL uint32_t quant_row32(const uint32_t (&p)[16], uint32_t (&codes)[8]) {
 // Quantize 8 elements (4 packed bf16 pairs, element 2i in the low half) of a
 // row block spread over 4 consecutive lanes.  Returns the 8 codes as two
 // 32-bit words (element 0 in the lowest byte) and the block scale byte.
-MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out) {
+MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out, uint32_t rceil = 1u) {
   uint32_t m2 = max2(max2(abs2(p[0]), abs2(p[1])), max2(abs2(p[2]), abs2(p[3])));
   m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
   m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 2));
-  const uint32_t s = e8m0_from_amax_bits(max_halves(m2));
+  const uint32_t s = e8m0_from_amax_bits(max_halves(m2), rceil);
   scale_out = s;
   uint2 out;
   if (s == 0xFF) {
@@ -107,13 +107,13 @@ MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out) {
 // words (row i of column A in the low half of v[i], column B in the high
 // half).  Writes 8 words of codes per column and returns both scales.
 MX_DEVINL void quant_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_t (&cb)[8], uint32_t& sa,
-                             uint32_t& sb) {
+                             uint32_t& sb, uint32_t rceil = 1u) {
   uint32_t m2 = abs2(v[0]);
 #pragma unroll
   for (int i = 1; i < 32; ++i) m2 = max2(m2, abs2(v[i]));
   const uint32_t la = m2 & 0xFFFFu, lb = m2 >> 16;
-  sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la);
-  sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb);
+  sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la, rceil);
+  sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb, rceil);
   // column A in the low lanes, column B in the high lanes: one packed
   // multiply scales an element of each column
   uint64_t iab;

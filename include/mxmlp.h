@@ -77,7 +77,21 @@ typedef enum { MX_SCALE_LINEAR = 0, MX_SCALE_MMA = 1 } mx_scale_layout;
  * ("wgrad_with_hp", pages "TrainingWeightWrapperTensor base class ..." and
  * "[mxfp8 training] unified MXFP8TrainingConfig ...", Autograd function
  * changes). */
-typedef enum { MX_RECIPE_RCEIL = 0, MX_RECIPE_RCEIL_WGRAD_HP = 1 } mx_recipe;
+typedef enum {
+  MX_RECIPE_RCEIL = 0,
+  MX_RECIPE_RCEIL_WGRAD_HP = 1,
+  /* The same two recipes with FLOOR scales for every quantization (see
+   * mx_scale_mode). */
+  MX_RECIPE_FLOOR = 2,
+  MX_RECIPE_FLOOR_WGRAD_HP = 3
+} mx_recipe;
+/* E8M0 scale rule.  MX_SCALE_RCEIL: the one above (amax/448 rounded up to a
+ * power of two; "ScaleCalculationMode.RCEIL" on the ao pages).
+ * MX_SCALE_FLOOR: 2^e with e = floor(log2(amax)) - 8, the shared exponent of
+ * the OCP Microscaling Formats v1.0 conversion, clamped likewise; scaled
+ * values in (448, 512) then saturate to +-448.  Zero and non-finite blocks
+ * as for RCEIL. */
+typedef enum { MX_SCALE_RCEIL = 0, MX_SCALE_FLOOR = 1 } mx_scale_mode;
 typedef enum { MX_GROUP_M = 0, MX_GROUP_K = 1 } mx_grouped_mode;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -106,6 +120,10 @@ MX_API const char* mx_last_error(void);
  */
 MX_API int mx_quantize(const void* x, int64_t rows, int64_t cols, int axis, int layout,
                 void* q_row, void* s_row, void* q_col, void* s_col, void* stream);
+
+/* mx_quantize with an explicit scale rule (mx_scale_mode). */
+MX_API int mx_quantize_mode(const void* x, int64_t rows, int64_t cols, int axis, int layout, int scale_mode,
+                            void* q_row, void* s_row, void* q_col, void* s_col, void* stream);
 
 /*
  * mx_swiglu_quant - fused SwiGLU forward with dual MXFP8 quantization; the
@@ -143,6 +161,14 @@ MX_API int mx_swiglu_quant(const void* h13, int64_t M, int64_t h, int axis, int 
 MX_API int mx_swiglu_quant_bwd(const void* dy, const void* h13, int64_t M, int64_t h, int axis,
                         int layout, void* dq_row, void* ds_row, void* dq_col, void* ds_col,
                         void* dh13_t, void* y_t, void* stream);
+
+/* mx_swiglu_quant and mx_swiglu_quant_bwd with an explicit scale rule
+ * (mx_scale_mode); the plain entry points use MX_SCALE_RCEIL. */
+MX_API int mx_swiglu_quant_mode(const void* h13, int64_t M, int64_t h, int axis, int layout, int scale_mode,
+                                void* yq_row, void* ys_row, void* yq_col, void* ys_col, void* stream);
+MX_API int mx_swiglu_quant_bwd_mode(const void* dy, const void* h13, int64_t M, int64_t h, int axis, int layout,
+                                    int scale_mode, void* dq_row, void* ds_row, void* dq_col, void* ds_col,
+                                    void* dh13_t, void* y_t, void* stream);
 
 /*
  * mx_scaled_mm - block-scaled MXFP8 GEMM on the tcgen05 tensor cores:

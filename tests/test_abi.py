@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     for want in ["mx_quantize", "mx_swiglu_quant", "mx_swiglu_quant_bwd", "mx_scaled_mm", "mx_grouped_mm",
                  "mx_bf16_wgrad", "mx_mlp_workspace_size", "mx_mlp_fwd", "mx_mlp_bwd",
                  "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows",
-                 "mx_linear_workspace_size", "mx_linear_fwd", "mx_linear_bwd"]:
+                 "mx_linear_workspace_size", "mx_linear_fwd", "mx_linear_bwd", "mx_quantize_mode",
+                 "mx_swiglu_quant_mode", "mx_swiglu_quant_bwd_mode"]:
         assert want in names
 
 
@@ -95,6 +96,18 @@ def test_token_group_pad_rejects_bad_arguments(L):
     assert L.mx_gather_rows(p, 10, 12, p, 10, 1, p, None, None) == 4                      # cols % 8
     assert L.mx_gather_rows(p, 10, 16, p, 10, 0, p, None, None) == 1                      # div 0
     assert L.mx_gather_rows(ctypes.c_void_p(0x1008), 10, 16, p, 10, 1, p, None, None) == 2  # alignment
+
+
+def test_scale_modes_and_recipes(L):
+    p = _fake()
+    assert L.mx_quantize_mode(p, 64, 64, 3, 1, 2, p, p, p, p, None) == 1                 # scale mode 2
+    assert L.mx_swiglu_quant_mode(p, 64, 64, 1, 1, 5, p, p, None, None, None) == 1
+    assert L.mx_swiglu_quant_bwd_mode(p, p, 64, 64, 1, 1, -1, p, p, None, None, None, None, None) == 1
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    for recipe in (2, 3):                                                                  # FLOOR recipes
+        assert L.mx_mlp_workspace_size(256, 256, 512, 0, recipe, ctypes.byref(c), ctypes.byref(s)) == 0
+        assert L.mx_linear_workspace_size(256, 256, 512, recipe, ctypes.byref(c), ctypes.byref(s)) == 0
+    assert L.mx_mlp_workspace_size(256, 256, 512, 0, 4, ctypes.byref(c), ctypes.byref(s)) == 1
 
 
 def test_linear_rejects_bad_arguments(L):

@@ -15,7 +15,8 @@ from tests.util import bits, to_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-3
-RECIPES = [(mx.RECIPE_RCEIL, o.RECIPE_RCEIL), (mx.RECIPE_RCEIL_WGRAD_HP, o.RECIPE_RCEIL_WGRAD_HP)]
+RECIPES = [(mx.RECIPE_RCEIL, o.RECIPE_RCEIL), (mx.RECIPE_RCEIL_WGRAD_HP, o.RECIPE_RCEIL_WGRAD_HP),
+           (mx.RECIPE_FLOOR, o.RECIPE_FLOOR), (mx.RECIPE_FLOOR_WGRAD_HP, o.RECIPE_FLOOR_WGRAD_HP)]
 
 
 def _run(x, w, dout, recipe):
@@ -33,7 +34,7 @@ def test_exact_inputs_bit_exact(recipe, orec):
     ints = lambda *s: synth.bf16_from_f32(rng.integers(-7, 8, s).astype(np.float32))
     x, w, dout = ints(256, 384), ints(512, 384), ints(256, 512)
     out, dx, dw = _run(x, w, dout, recipe)
-    r_out = o.linear_fwd(x, w)
+    r_out = o.linear_fwd(x, w, recipe=orec)
     r_dx, r_dw = o.linear_bwd(x, w, dout, orec)
     assert np.array_equal(out, r_out) and np.array_equal(dx, r_dx) and np.array_equal(dw, r_dw)
 
@@ -45,7 +46,7 @@ def test_matches_oracle(M, K, N, recipe, orec):
     w = synth.normal_bf16((N, K), 0.02, N + 1)
     dout = synth.normal_bf16((M, N), 1.0, N + 2)
     out, dx, dw = _run(x, w, dout, recipe)
-    r_out = o.linear_fwd(x, w, rounded=False)
+    r_out = o.linear_fwd(x, w, rounded=False, recipe=orec)
     r_dx, r_dw = o.linear_bwd(x, w, dout, orec, rounded=False)
     for got, ref in ((out, r_out), (dx, r_dx), (dw, r_dw)):
         assert o.normwise_rel_err(o.bf16_to_f64(got), ref) <= TOL

@@ -29,7 +29,7 @@ def _cat_tiles(sa, sb, rows, cols_each):
     return torch.cat([a, b], dim=1).reshape(-1)
 
 
-def _quant_weights(w1, w3, w2):
+def _quant_weights(w1, w3, w2, sm=0):
     """Per-expert MX quantization of the weights exactly as the composite
     lays them out: w13 rowwise [E,2h,d], w13 columnwise [E,d,2h], w2
     rowwise [E,d,h], w2 columnwise [E,h,d]."""
@@ -41,9 +41,9 @@ def _quant_weights(w1, w3, w2):
     h, d = W1.shape[1], W1.shape[2]
     r = dict(w13q=[], w13s=[], w13qc=[], w13sc=[], w2q=[], w2s=[], w2qc=[], w2sc=[])
     for e in range(E):
-        a = mx.quantize(W1[e].contiguous())
-        b = mx.quantize(W3[e].contiguous())
-        c = mx.quantize(W2[e].contiguous())
+        a = mx.quantize(W1[e].contiguous(), scale_mode=sm)
+        b = mx.quantize(W3[e].contiguous(), scale_mode=sm)
+        c = mx.quantize(W2[e].contiguous(), scale_mode=sm)
         r["w13q"].append(torch.cat([a["q_row"], b["q_row"]], 0))
         r["w13s"].append(torch.cat([a["s_row"], b["s_row"]], 0))
         r["w13qc"].append(torch.cat([a["q_col"], b["q_col"]], 1))
@@ -58,11 +58,12 @@ def _quant_weights(w1, w3, w2):
 
 def _chain(x, w1, w3, w2, dout, offs, recipe):
     """The MLP forward+backward as a chain of per-op entry points."""
-    hp = recipe == mx.RECIPE_RCEIL_WGRAD_HP
+    hp = recipe in (mx.RECIPE_RCEIL_WGRAD_HP, mx.RECIPE_FLOOR_WGRAD_HP)
+    sm = mx.SCALE_FLOOR if recipe in (mx.RECIPE_FLOOR, mx.RECIPE_FLOOR_WGRAD_HP) else mx.SCALE_RCEIL
     grouped = offs is not None
-    W = _quant_weights(w1, w3, w2)
+    W = _quant_weights(w1, w3, w2, sm)
     h = w1.shape[-2]
-    xq = mx.quantize(x, mx.BOTH)
+    xq = mx.quantize(x, mx.BOTH, scale_mode=sm)
 
     def mm(aq, as_, bq, bs):
         if grouped:
@@ -75,18 +76,18 @@ def _chain(x, w1, w3, w2, dout, offs, recipe):
         return mx.scaled_mm(aq, as_, bq, bs)
 
     h13 = mm(xq["q_row"], xq["s_row"], W["w13q"], W["w13s"])
-    y = mx.swiglu_quant(h13, mx.ROW if hp else mx.BOTH)
+    y = mx.swiglu_quant(h13, mx.ROW if hp else mx.BOTH, scale_mode=sm)
     out = mm(y["q_row"], y["s_row"], W["w2q"], W["w2s"])
-    dq = mx.quantize(dout, mx.BOTH)
+    dq = mx.quantize(dout, mx.BOTH, scale_mode=sm)
     dy = mm(dq["q_row"], dq["s_row"], W["w2qc"], W["w2sc"])
     if hp:
-        dh = mx.swiglu_quant_bwd(dy, h13, mx.ROW, bf16_transposed=True)
+        dh = mx.swiglu_quant_bwd(dy, h13, mx.ROW, bf16_transposed=True, scale_mode=sm)
         dout_t = dout.t().contiguous()
         x_t = x.t().contiguous()
         dw2 = mx.bf16_wgrad(dout_t, dh["y_t"], offs)
         dw13 = mx.bf16_wgrad(dh["dh13_t"], x_t, offs)
     else:
-        dh = mx.swiglu_quant_bwd(dy, h13, mx.BOTH)
+        dh = mx.swiglu_quant_bwd(dy, h13, mx.BOTH, scale_mode=sm)
         dw2 = wg(dq["q_col"], dq["s_col"], y["q_col"], y["s_col"])
         dw13 = wg(dh["q_col"], dh["s_col"], xq["q_col"], xq["s_col"])
     dx = mm(dh["q_row"], dh["s_row"], W["w13qc"], W["w13sc"])
@@ -110,7 +111,11 @@ CASES = [
     ("dense", mx.RECIPE_RCEIL_WGRAD_HP),
     ("grouped", mx.RECIPE_RCEIL),
     ("grouped", mx.RECIPE_RCEIL_WGRAD_HP),
+    ("dense", mx.RECIPE_FLOOR),
+    ("grouped", mx.RECIPE_FLOOR_WGRAD_HP),
 ]
+ORACLE_RECIPE = {mx.RECIPE_RCEIL: o.RECIPE_RCEIL, mx.RECIPE_RCEIL_WGRAD_HP: o.RECIPE_RCEIL_WGRAD_HP,
+                 mx.RECIPE_FLOOR: o.RECIPE_FLOOR, mx.RECIPE_FLOOR_WGRAD_HP: o.RECIPE_FLOOR_WGRAD_HP}
 
 
 def _setup(kind):
@@ -137,7 +142,9 @@ def test_composite_equals_op_chain(kind, recipe):
 @pytest.mark.parametrize("kind,recipe", CASES)
 def test_op_chain_stagewise_vs_oracle(kind, recipe):
     inp, t, offs = _setup(kind)
-    hp = recipe == mx.RECIPE_RCEIL_WGRAD_HP
+    orc = ORACLE_RECIPE[recipe]
+    hp = o.recipe_hp(orc)
+    sc = o.recipe_scale(orc)
     ch = _chain(t["x"], t["w1"], t["w3"], t["w2"], t["dout"], offs, recipe)
     torch.cuda.synchronize()
     offs_h = inp.get("offs")
@@ -146,13 +153,13 @@ def test_op_chain_stagewise_vs_oracle(kind, recipe):
     h = w1.shape[-2]
     M, d = x.shape
     # F1/F2/F5: quantization bit-exact
-    xq, xs = o.quantize_rows(x)
+    xq, xs = o.quantize_rows(x, sc)
     assert np.array_equal(u8(ch["xq"]["q_row"]), xq)
     w13 = np.concatenate([w1, w3], axis=-2)
-    w13q, w13s = o.quantize_rows(w13)
+    w13q, w13s = o.quantize_rows(w13, sc)
     assert np.array_equal(u8(ch["W"]["w13q"]), w13q)
     assert np.array_equal(u8(ch["W"]["w13s"]), o.scales_to_mma(w13s))
-    w13qc, w13sc = o.quantize_cols(w13)
+    w13qc, w13sc = o.quantize_cols(w13, sc)
     assert np.array_equal(u8(ch["W"]["w13qc"]), w13qc)
     assert np.array_equal(u8(ch["W"]["w13sc"]), o.scales_to_mma(w13sc))
     # F3: h13 from the (bit-exact) quantized operands
@@ -161,27 +168,27 @@ def test_op_chain_stagewise_vs_oracle(kind, recipe):
     assert o.normwise_rel_err(o.bf16_to_f64(h13), ref) <= TOL
     # F4: SwiGLU of the GPU's h13, bit-exact codes
     y = o.swiglu_fwd(*o.split_h13(h13))
-    yq, ys = o.quantize_rows(y)
+    yq, ys = o.quantize_rows(y, sc)
     assert np.array_equal(u8(ch["y"]["q_row"]), yq)
     assert np.array_equal(u8(ch["y"]["s_row"]), o.scales_to_mma(ys))
     if not hp:
-        yqc, ysc = o.quantize_cols(y)
+        yqc, ysc = o.quantize_cols(y, sc)
         assert np.array_equal(u8(ch["y"]["q_col"]), yqc)
     # F6
-    w2q, w2s = o.quantize_rows(w2)
+    w2q, w2s = o.quantize_rows(w2, sc)
     ref = o.mx_grouped_mm_m(yq, ys, w2q, w2s, offs_h) if grouped else o.mx_mm(yq, ys, w2q, w2s)
     assert o.normwise_rel_err(o.bf16_to_f64(bits(ch["out"])), ref) <= TOL
     # B2: dy
-    dq, ds = o.quantize_rows(dout)
+    dq, ds = o.quantize_rows(dout, sc)
     assert np.array_equal(u8(ch["dq"]["q_row"]), dq)
-    w2qc, w2sc = o.quantize_cols(w2)
+    w2qc, w2sc = o.quantize_cols(w2, sc)
     ref = o.mx_grouped_mm_m(dq, ds, w2qc, w2sc, offs_h) if grouped else o.mx_mm(dq, ds, w2qc, w2sc)
     dy = bits(ch["dy"])
     assert o.normwise_rel_err(o.bf16_to_f64(dy), ref) <= TOL
     # B4: SwiGLU backward of the GPU's dy and h13, bit-exact
     dg, du = o.swiglu_bwd(dy, *o.split_h13(h13))
     dh13 = np.concatenate([dg, du], axis=-1)
-    dhq, dhs = o.quantize_rows(dh13)
+    dhq, dhs = o.quantize_rows(dh13, sc)
     assert np.array_equal(u8(ch["dh"]["q_row"]), dhq)
     # B5: dx
     ref = (o.mx_grouped_mm_m(dhq, dhs, w13qc, w13sc, offs_h) if grouped
@@ -195,10 +202,10 @@ def test_op_chain_stagewise_vs_oracle(kind, recipe):
         ref2 = o.bf16_grouped_mm_k(dout.T, y.T, go)
         ref13 = o.bf16_grouped_mm_k(dh13.T, x.T, go)
     else:
-        dqc, dsc = o.quantize_cols(dout)
-        dhqc, dhsc = o.quantize_cols(dh13)
+        dqc, dsc = o.quantize_cols(dout, sc)
+        dhqc, dhsc = o.quantize_cols(dh13, sc)
         assert np.array_equal(u8(ch["dh"]["q_col"]), dhqc)
-        xqc, xsc = o.quantize_cols(x)
+        xqc, xsc = o.quantize_cols(x, sc)
         ref2 = o.mx_grouped_mm_k(dqc, dsc, yqc, ysc, go)
         ref13 = o.mx_grouped_mm_k(dhqc, dhsc, xqc, xsc, go)
     if not grouped:
@@ -219,7 +226,7 @@ def test_end_to_end_vs_oracle(kind, recipe):
     dx, dw1, dw3, dw2 = mx.mlp_bwd(ctx, t["dout"])
     torch.cuda.synchronize()
     offs_h = inp.get("offs")
-    orc = "wgrad_hp" if recipe == mx.RECIPE_RCEIL_WGRAD_HP else "rceil"
+    orc = ORACLE_RECIPE[recipe]
     f = o.mlp_fwd(inp["x"], inp["w1"], inp["w3"], inp["w2"], offs=offs_h, recipe=orc)
     b = o.mlp_bwd(inp["x"], inp["w1"], inp["w3"], inp["w2"], inp["dout"], offs=offs_h, recipe=orc, fwd=f)
     h = inp["w1"].shape[-2]

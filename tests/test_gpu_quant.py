@@ -12,8 +12,8 @@ from tests.util import bits, to_dev, u8
 pytestmark = pytest.mark.gpu
 
 
-def _check_rows(res, x, layout, rows=None):
-    q, s = o.quantize_rows(x if rows is None else x[rows])
+def _check_rows(res, x, layout, rows=None, scale=o.SCALE_RCEIL):
+    q, s = o.quantize_rows(x if rows is None else x[rows], scale)
     got_q = u8(res["q_row"]) if rows is None else u8(res["q_row"])[rows]
     assert np.array_equal(got_q, q)
     R, C = x.shape
@@ -27,9 +27,9 @@ def _check_rows(res, x, layout, rows=None):
     assert np.array_equal(sl if rows is None else sl[rows], s)
 
 
-def _check_cols(res, x, layout, cols=None):
+def _check_cols(res, x, layout, cols=None, scale=o.SCALE_RCEIL):
     xt = x.T if cols is None else x[:, cols].T
-    q, s = o.quantize_rows(np.ascontiguousarray(xt))
+    q, s = o.quantize_rows(np.ascontiguousarray(xt), scale)
     got_q = u8(res["q_col"]) if cols is None else u8(res["q_col"])[cols]
     assert np.array_equal(got_q, q)
     R, C = x.shape
@@ -75,7 +75,24 @@ def test_quantize_ragged_rows_rowwise():
     _check_rows(res, x, mx.SCALE_LINEAR)
 
 
-def test_quantize_every_bf16_amax():
+@pytest.mark.parametrize("layout", [mx.SCALE_MMA, mx.SCALE_LINEAR])
+@pytest.mark.parametrize("shape", [(256, 256), (384, 640), (96, 160)])
+def test_quantize_floor_matches_oracle(shape, layout):
+    """FLOOR scales (reading R14) on the sweep recipe and on blocks whose
+    amax mantissa exceeds 1.75, where saturation binds."""
+    R, C = shape
+    x = synth.quant_sweep_tensor(R, C, seed=R + 2 * C)
+    v = o.bf16_to_f64(x)
+    sat = synth.bf16_from_f32((np.sign(v) * 1.9 * 2.0 ** np.round(np.log2(np.abs(v) + 1e-30))).astype(np.float32))
+    x[::3] = sat[::3]                 # every third row: magnitudes 1.9 * 2^k
+    res = mx.quantize(to_dev(x), mx.BOTH, layout, mx.SCALE_FLOOR)
+    torch.cuda.synchronize()
+    _check_rows(res, x, layout, scale=o.SCALE_FLOOR)
+    _check_cols(res, x, layout, scale=o.SCALE_FLOOR)
+
+
+@pytest.mark.parametrize("scale", [o.SCALE_RCEIL, o.SCALE_FLOOR])
+def test_quantize_every_bf16_amax(scale):
     """One block per non-negative bf16 amax value (plus NaN/Inf/-0 blocks):
     exhaustive E8M0 + E4M3 coverage of the kernel's scale path."""
     amax = np.arange(0, 0x7F81, dtype=np.uint32).astype(np.uint16)      # incl. +Inf
@@ -92,9 +109,10 @@ def test_quantize_every_bf16_amax():
     blocks[amax.size] = 0x7FC0        # NaN block
     blocks[amax.size + 1, 3] = 0x8000  # -0 block
     x = blocks.reshape(-1, 128)        # 4 blocks per row
-    res = mx.quantize(to_dev(x), mx.ROW, mx.SCALE_LINEAR)
+    mode = mx.SCALE_FLOOR if scale == o.SCALE_FLOOR else mx.SCALE_RCEIL
+    res = mx.quantize(to_dev(x), mx.ROW, mx.SCALE_LINEAR, mode)
     torch.cuda.synchronize()
-    _check_rows(res, x, mx.SCALE_LINEAR)
+    _check_rows(res, x, mx.SCALE_LINEAR, scale=scale)
 
 
 def test_quantize_golden_blocks():
