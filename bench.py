@@ -617,6 +617,17 @@ def run_profile_case(args):
             offs, dst, src = mx.token_group_pad(ids, E, m_cap)
             mx.gather_rows(x, src, div=k)
         work, unit = (T * k + m_cap) * d * 2, "B"
+    elif c == "gemm_group_k":  # MoE 16E dW13: [E=16] x [2h=16384, d=5120] over 33536 padded routed rows
+        w = synth.WORKLOADS["moe_16e"]
+        counts = synth.zipf_group_counts(w["E"], w["tokens"], w["s"], w["seed"], w["n_empty"])
+        offs = torch.as_tensor(synth.offsets_from_counts(synth.pad_counts(counts)), device=dev)
+        Mt, N, K = int(offs[-1]), 2 * w["h"], w["d"]
+        codes = lambda *sh: torch.randint(0, 126, sh, generator=g, device=dev, dtype=torch.uint8)
+        aq, bq = codes(N, Mt), codes(K, Mt)
+        as_ = torch.full((mx.mma_scale_bytes(N, Mt),), 127, dtype=torch.uint8, device=dev)
+        bs = torch.full((mx.mma_scale_bytes(K, Mt),), 120, dtype=torch.uint8, device=dev)
+        fn = lambda: mx.grouped_mm(mx.GROUP_K, aq, as_, bq, bs, offs)
+        work, unit = 2.0 * Mt * N * K, "FLOP"
     elif c in ("gemm_mx", "gemm_bf16"):
         N, K = 8192, 4096
         if c == "gemm_mx":
@@ -657,7 +668,7 @@ def main():
     ap.add_argument("--no-quant-sweep", action="store_true", help="skip the quantize-sweep GB/s object")
     ap.add_argument("--profile-case", default=None,
                     choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
-                             "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "dispatch"])
+                             "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

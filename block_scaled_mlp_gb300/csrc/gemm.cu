@@ -109,8 +109,15 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
     const int64_t e = u / per_e;
     const int64_t rem = u - e * per_e;
     ti.e = (int32_t)e;
-    ti.m_blk = CL == 2 ? 2 * (rem % mt) + rank : rem % mt;
-    ti.n_blk = rem / mt;
+    if (CL == 1 && p.M > p.N) {
+      // columns fastest: the smaller operand (B, N x tokens) is the one
+      // re-read for every row of tiles and stays in L2; A streams once
+      ti.m_blk = rem / p.n_tiles;
+      ti.n_blk = rem % p.n_tiles;
+    } else {
+      ti.m_blk = CL == 2 ? 2 * (rem % mt) + rank : rem % mt;
+      ti.n_blk = rem / mt;
+    }
     ti.store = ti.m_blk < p.m_tiles;
     const int64_t s = e == 0 ? 0 : g.ends[e - 1];
     const int64_t en = g.ends[e];
@@ -152,8 +159,13 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
       const int64_t tiles_e = (g.ends[lo] - start) / BM;
       const int64_t r = u - (lo == 0 ? 0 : g.unit_end[lo - 1]);
       ti.e = lo;
-      ti.n_blk = r / tiles_e;
-      ti.m_blk = start / BM + r % tiles_e;
+      if (tiles_e * BM <= p.N) {  // the group's rows are the smaller operand: re-read them
+        ti.n_blk = r / tiles_e;
+        ti.m_blk = start / BM + r % tiles_e;
+      } else {                    // the expert's weights are smaller: columns fastest
+        ti.m_blk = start / BM + r / p.n_tiles;
+        ti.n_blk = r % p.n_tiles;
+      }
       return ti;
     }
     // dense: bands of p.band tile rows (sized so that a band of A stays in
