@@ -70,6 +70,7 @@ struct GemmParams {
   int64_t split;              // row split of C between tmC0 / tmC1 (0: none)
   int64_t msub;               // GROUP_K: rows per expert in the output maps
   int64_t band;               // DENSE: tile rows per band of the tile order
+  int32_t cols_fast;          // DENSE: columns fastest (B re-read from L2, A streamed once)
   int32_t* err;
 };
 
@@ -166,6 +167,11 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
         ti.m_blk = start / BM + r / p.n_tiles;
         ti.n_blk = r % p.n_tiles;
       }
+      return ti;
+    }
+    if (p.cols_fast) {  // dense, B the smaller operand: columns fastest
+      ti.m_blk = u / p.n_tiles;
+      ti.n_blk = u % p.n_tiles;
       return ti;
     }
     // dense: bands of p.band tile rows (sized so that a band of A stays in
@@ -596,6 +602,9 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
     int64_t band = (int64_t)(48ll << 20) / (row_bytes > 0 ? row_bytes : 1);
     if (row_bytes * p.m_tiles <= (96ll << 20)) band = p.m_tiles;
     p.band = band < 1 ? 1 : (band > p.m_tiles ? p.m_tiles : band);
+    // B smaller than A and resident in L2: re-read B, stream A once
+    const int64_t a_bytes = row_bytes * p.m_tiles, b_bytes = p.N * p.K * (MX ? 1 : 2);
+    p.cols_fast = b_bytes < a_bytes && b_bytes <= (96ll << 20);
   }
   p.m_pairs = (p.m_tiles + 1) / 2;
   const int64_t experts = g.mode == GEMM_GROUP_K ? g.E : 1;
