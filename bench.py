@@ -223,7 +223,9 @@ def run_gpu(args, rank, world, dev):
         torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
     ms_max = float(ms_t.item())
     value = w["flops"] * world / (ms_max * 1e-3) / 1e12
-    launches_per_step = 13 if E == 0 else 13
+    # own kernels per step: 13, or 12 when the w13 GEMM carries the SwiGLU
+    # (wgrad_with_hp recipes)
+    launches_per_step = 12 if recipe in (mx.RECIPE_RCEIL_WGRAD_HP, mx.RECIPE_FLOOR_WGRAD_HP) else 13
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs (x, dout) in from pinned host memory and its results

@@ -469,22 +469,33 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
     q.qc_ld = 2 * h; q.qc_off = half * h; q.qc_bs = d * 2 * h; q.sc_bs = mma_scale_bytes(d, 2 * h);
     if ((rc = launch_quant(q, st))) return rc;
   }
-  // F3: h13 = x . w13^T
-  {
+  if (hp) {
+    // F3 + F4 in one kernel: the w13 GEMM stores h13 and, in its epilogue,
+    // the rowwise MXFP8 y = SwiGLU(h13) (the HP recipe needs no columnwise y)
     GemmLaunch g{};
     g.mx = 1; g.mode = grouped ? GEMM_GROUP_M : GEMM_DENSE;
     g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.w13q_r; g.sfb = b.w13s_r;
     g.M = M; g.N = 2 * h; g.K = d; g.offs = offs; g.E = (int32_t)Ew; g.c0 = b.h13; g.err = err_word;
+    g.fuse_swiglu = 1; g.yq = b.yq_r; g.ys = b.ys_r; g.floor_scale = fl;
     if ((rc = launch_gemm(g, st))) return rc;
-  }
-  // F4: y = SwiGLU(h13) -> rowwise MX (+ columnwise MX for the default recipe)
-  {
-    SwigluLaunch s{};
-    s.floor_scale = fl;
-    s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
-    s.q_row = b.yq_r; s.s_row = b.ys_r;
-    if (!hp) { s.q_col = b.yq_c; s.s_col = b.ys_c; }
-    if ((rc = launch_swiglu_fwd(s, st))) return rc;
+  } else {
+    // F3: h13 = x . w13^T
+    {
+      GemmLaunch g{};
+      g.mx = 1; g.mode = grouped ? GEMM_GROUP_M : GEMM_DENSE;
+      g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.w13q_r; g.sfb = b.w13s_r;
+      g.M = M; g.N = 2 * h; g.K = d; g.offs = offs; g.E = (int32_t)Ew; g.c0 = b.h13; g.err = err_word;
+      if ((rc = launch_gemm(g, st))) return rc;
+    }
+    // F4: y = SwiGLU(h13) -> rowwise MX (+ columnwise MX for the default recipe)
+    {
+      SwigluLaunch s{};
+      s.floor_scale = fl;
+      s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
+      s.q_row = b.yq_r; s.s_row = b.ys_r;
+      if (!hp) { s.q_col = b.yq_c; s.s_col = b.ys_c; }
+      if ((rc = launch_swiglu_fwd(s, st))) return rc;
+    }
   }
   // F5: w2 -> rowwise [d, h] and columnwise [h, d], per expert
   {

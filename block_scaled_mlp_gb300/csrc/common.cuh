@@ -117,6 +117,15 @@ MX_DEVINL void tma_load_4d(void* dst, const CUtensorMap* m, int32_t x, int32_t y
       : "memory");
 }
 
+MX_DEVINL void tma_load_5d(void* dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z, int32_t w, int32_t v,
+                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // The same tile delivered to the shared memory of every CTA in ctaMask (at
 // this CTA's offsets), each CTA's mbarrier at the same offset receiving the
 // byte count.

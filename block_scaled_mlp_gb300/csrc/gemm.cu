@@ -19,6 +19,8 @@
 // group writes zeros).  Group offsets are read on the device.
 #include "common.cuh"
 #include "kernels.h"
+#include "swiglu_math.cuh"
+#include "tile_quant.cuh"
 
 namespace mx {
 
@@ -71,8 +73,20 @@ struct GemmParams {
   int64_t msub;               // GROUP_K: rows per expert in the output maps
   int64_t band;               // DENSE: tile rows per band of the tile order
   int32_t cols_fast;          // DENSE: columns fastest (B re-read from L2, A streamed once)
+  // fused SwiGLU epilogue (the w13 GEMM of the MLP forward): tile n covers
+  // hidden units [128n, 128n+128) of g (accumulator columns 0-127) and of u
+  // (128-255); C (h13) is stored and y = SwiGLU(h13) quantized by rows
+  uint8_t* yq;                // [M, hy] codes
+  ScaleDst ys;                // [M, hy/32] scales
+  int64_t hy;                 // h
+  uint32_t rceil;             // 1: RCEIL scales, 0: FLOOR
   int32_t* err;
 };
+
+MX_DEVINL void store32g(uint8_t* dst, const uint32_t (&c)[8]) {
+  store16(dst, c[0], c[1], c[2], c[3]);
+  store16(dst + 16, c[4], c[5], c[6], c[7]);
+}
 
 struct TileInfo {
   int64_t m_blk, n_blk;
@@ -214,13 +228,14 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
   return ti;
 }
 
-template <bool MX, int BN, int CL, int SUB>
+template <bool MX, int BN, int CL, int SUB, bool FUSE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 GemmParams p) {
   using C = Cfg<MX, BN, SUB, CL>;
+  static_assert(!FUSE || (MX && CL == 1 && SUB == 1 && BN == 256), "fused SwiGLU: MXFP8, one CTA, 128x256 tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -348,7 +363,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t bytes = C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? 512 : 0) + C::SFB_BYTES : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * C::TM), &full[stage]);
-          if (p.mode == GEMM_GROUP_M)
+          if (FUSE) {  // rows 128n.. of w1 and of w3 in one copy ([2][128] rows)
+            if (p.mode == GEMM_GROUP_M)
+              tma_load_4d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * 128), 0, ti.e, &full[stage]);
+            else
+              tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * 128), 0, &full[stage]);
+          } else if (p.mode == GEMM_GROUP_M)
             tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
           else
             tma_load_2d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), &full[stage]);
@@ -358,7 +378,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         &full[stage]);
             // all of the tile's B scale tiles (BN/128 tile rows) in one copy;
             // rows past N are zero-filled and counted
-            if (p.mode == GEMM_GROUP_M)
+            if (FUSE && p.mode == GEMM_GROUP_M)
+              tma_load_5d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)ti.n_blk, 0, ti.e,
+                          &full[stage]);
+            else if (FUSE)
+              tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)ti.n_blk, 0, &full[stage]);
+            else if (p.mode == GEMM_GROUP_M)
               tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)), ti.e,
                           &full[stage]);
             else
@@ -467,8 +492,42 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (p.mode == GEMM_GROUP_K) mrow += (int64_t)ti.e * p.msub;
         return mrow;
       };
+      // stage one 32x32 chunk of bf16 words (one row per lane) with the 64-byte
+      // swizzle and TMA-store it
+      auto store_chunk = [&](const uint32_t (&w)[16], const CUtensorMap* tmC, int64_t col, int64_t mrow) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        uint8_t* row = stg + lane * 64;
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
+              make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmC, stg, (int32_t)col, (int32_t)mrow);
+          bulk_commit();
+        }
+      };
+      auto pack = [](const uint32_t (&r)[32], uint32_t (&w)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+      };
       if (ti.num_kb == 0) {
         if (!ti.store) continue;
+        if (FUSE) {  // rows with no group: y codes and scales are zero too
+          const int64_t ycol = ti.n_blk * 128 + half * 64;
+          const int64_t row = ti.m_blk * BM + q * 32 + lane;
+          const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          store32g(p.yq + row * p.hy + ycol, z);
+          store32g(p.yq + row * p.hy + ycol + 32, z);
+          p.ys.put(row, ycol >> 5, 0);
+          p.ys.put(row, (ycol >> 5) + 1, 0);
+        }
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         uint4* row = reinterpret_cast<uint4*>(stg + lane * 64);
@@ -496,31 +555,73 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
         continue;
       }
-      // stage one 32x32 chunk of bf16 words (one row per lane) with the 64-byte
-      // swizzle and TMA-store it
-      auto store_chunk = [&](const uint32_t (&w)[16], const CUtensorMap* tmC, int64_t col, int64_t mrow) {
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-        uint8_t* row = stg + lane * 64;
-        const int sw = (lane >> 1) & 3;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(row + ((j ^ sw) * 16)) =
-              make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(tmC, stg, (int32_t)col, (int32_t)mrow);
-          bulk_commit();
+      if constexpr (FUSE) {
+        // this warp: rows 32q.. of the tile, hidden units ycol..ycol+63;
+        // g in accumulator columns 64*half.., u in 128 + 64*half..
+        const int64_t ycol = ti.n_blk * 128 + half * 64;
+        const int64_t mrow = ti.m_blk * BM + q * 32;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
+        uint32_t gw[2][16], uw[2][16];   // RN bf16 pairs: the stored h13 values
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32cols(tb, r0);
+          tmem_ld_32cols(tb + 32, r1);
+          tmem_ld_wait();
+          pack(r0, gw[0]);
+          pack(r1, gw[1]);
+          tmem_ld_32cols(tb + 128, r0);
+          tmem_ld_32cols(tb + 160, r1);
+          tmem_ld_wait();
+          pack(r0, uw[0]);
+          pack(r1, uw[1]);
         }
-      };
-      auto pack = [](const uint32_t (&r)[32], uint32_t (&w)[16]) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release_acc(acc);
+        store_chunk(gw[0], &tmC0, ycol, mrow);
+        store_chunk(gw[1], &tmC0, ycol + 32, mrow);
+        store_chunk(uw[0], &tmC0, p.hy + ycol, mrow);
+        store_chunk(uw[1], &tmC0, p.hy + ycol + 32, mrow);
+        // y = SwiGLU(g, u) of this thread's row, the same certified fast path
+        // and exact tiers as the standalone SwiGLU kernel, then rows quantized
+        const int64_t row = mrow + lane;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        for (int b = 0; b < 2; ++b) {
+          uint32_t yw[16];
+          uint32_t slow = 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t G = f2_from_bf16x2(gw[b][i]);
+            const uint64_t P = f2_mul(G, swiglu_math::sig_fast2(G).S);
+            float g0, g1, p0, p1;
+            f2_unpack(G, g0, g1);
+            f2_unpack(P, p0, p1);
+            slow |= (fabsf(g0) <= 64.0f && swiglu_math::clear_of_midpoint(p0, 16) ? 0u : 1u) << (2 * i);
+            slow |= (fabsf(g1) <= 64.0f && swiglu_math::clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
+            yw[i] = f2_to_bf16x2(f2_mul(f2_from_bf16x2(f2_to_bf16x2(P)), f2_from_bf16x2(uw[b][i])));
+          }
+          if (slow) {  // exact tiers for the uncertain elements (static indices: registers stay registers)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                if ((slow >> (2 * i + hh)) & 1u) {
+                  const float g = hh ? bf16_hi(gw[b][i]) : bf16_lo(gw[b][i]);
+                  const float uu = hh ? bf16_hi(uw[b][i]) : bf16_lo(uw[b][i]);
+                  const uint32_t y = f32_to_bf16_bits(__fmul_rn(bf16_lo(swiglu_math::silu_bits_slow(g)), uu));
+                  yw[i] = hh ? ((yw[i] & 0xFFFFu) | (y << 16)) : ((yw[i] & 0xFFFF0000u) | y);
+                }
+              }
+            }
+          }
+          uint32_t codes[8];
+          const uint32_t sc = quant_row32(yw, codes, p.rceil);
+          store32g(p.yq + row * p.hy + ycol + 32 * b, codes);
+          p.ys.put(row, (ycol >> 5) + b, sc);
         }
-      };
+        if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
+        continue;
+      }
       if (SUB == 1) {
         // drain this warp's whole share into registers (as bf16), hand the
         // accumulator back, then store: the next tile's MMAs overlap the stores
@@ -587,7 +688,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-template <bool MX, int BN, int CL, int SUB>
+template <bool MX, int BN, int CL, int SUB, bool FUSE = false>
 int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC0,
                const CUtensorMap& tC1, const CUtensorMap& tSFA, const CUtensorMap& tSFB, GemmParams& p,
                cudaStream_t stream) {
@@ -615,7 +716,7 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   p.tiles = units;
   if (units == 0) return MX_OK;
   if (units > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "gemm: too many tiles");
-  auto k = gemm_kernel<MX, BN, CL, SUB>;
+  auto k = gemm_kernel<MX, BN, CL, SUB, FUSE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
   if (CL == 1) {
@@ -688,7 +789,16 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     rc = make_tmap(&tA, dt, 2, const_cast<void*>(g.a), dims, strides, box, opswz);
     if (rc) return rc;
   }
-  if (g.mode == GEMM_GROUP_M) {
+  const bool fuse = g.fuse_swiglu != 0;
+  if (fuse) {
+    // w13 [(E,) 2h, K] viewed as [(E,) 2, h, K]: one box = rows 128n.. of w1
+    // and the same rows of w3
+    const uint64_t hh = (uint64_t)(g.N / 2);
+    uint64_t dims[4] = {(uint64_t)g.K, hh, 2, (uint64_t)g.E};
+    uint64_t strides[3] = {(uint64_t)g.K, (uint64_t)g.K * hh, (uint64_t)g.K * g.N};
+    uint32_t box[4] = {bk, 128, 2, 1};
+    rc = make_tmap(&tB, dt, g.mode == GEMM_GROUP_M ? 4 : 3, const_cast<void*>(g.b), dims, strides, box, opswz);
+  } else if (g.mode == GEMM_GROUP_M) {
     uint64_t dims[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
     uint64_t strides[2] = {(uint64_t)g.K * esz, (uint64_t)g.K * g.N * esz};
     uint32_t box[3] = {bk, BROWS, 1};
@@ -730,12 +840,29 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   p.sfb_expert_stride = (g.N / 128) * (g.K / 128) * 512;
   p.split = g.split;
   p.msub = g.split > 0 ? g.split : g.M;
+  p.yq = (uint8_t*)g.yq;
+  p.hy = g.N / 2;
+  {
+    const int64_t S = p.hy / 32;
+    p.ys = ScaleDst{(uint8_t*)g.ys, (S + 3) / 4, S, 1};
+  }
+  p.rceil = g.floor_scale ? 0u : 1u;
   p.err = g.err;
   // B scales viewed as 32-bit words: one 512-byte tile = 128 words; tile
   // (row rb, column cb) of a [R, S] scale matrix at word (rb*ceil(S/4) + cb)*128.
   // Box: one column tile of each of the BN/128 tile rows.
   CUtensorMap tSFB = tB;
-  if (mx) {
+  if (mx && fuse) {
+    // the scale tile rows of w1 block n and w3 block n: [(E,) 2, h/128, K/128, 128 words]
+    const uint64_t col_tiles = (uint64_t)(g.K / 128);
+    const uint64_t hrows = (uint64_t)(g.N / 256);
+    uint64_t dims[5] = {128, col_tiles, hrows, 2, (uint64_t)g.E};
+    uint64_t strides[4] = {512, col_tiles * 512, col_tiles * 512 * hrows, col_tiles * 512 * hrows * 2};
+    uint32_t box[5] = {128, 1, 1, 2, 1};
+    rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.mode == GEMM_GROUP_M ? 5 : 4, const_cast<void*>(g.sfb),
+                   dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  } else if (mx) {
     const uint64_t col_tiles = (uint64_t)(g.K / 128);
     const uint64_t tile_rows = (uint64_t)(g.N / 128);
     if (g.mode == GEMM_GROUP_M) {
@@ -763,6 +890,11 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     rc = make_tmap(&tSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(g.sfa), dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
+  }
+  if (fuse) {
+    if (!mx || BN != 256 || g.mode == GEMM_GROUP_K || g.N % 256 || !g.yq || !g.ys)
+      return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: MXFP8 forward form, 2h a multiple of 256");
+    return launch_cfg<true, 256, 1, 1, true>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
   }
   if (mx) {
     if (pair) return launch_cfg<true, BN, 2, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);

@@ -80,6 +80,13 @@ struct GemmLaunch {
   void* c0;
   void* c1;
   int64_t split;
+  // fused SwiGLU epilogue (MXFP8, DENSE or GROUP_M): B = w13 [(E,) 2h, K]
+  // with w1 rows first; c0 receives h13 [M, 2h] and yq/ys the rowwise MXFP8
+  // y = SwiGLU(h13) [M, h] (scales in the MMA layout)
+  int fuse_swiglu;
+  void* yq;
+  void* ys;
+  int floor_scale;   // 1: FLOOR E8M0 scales for y
   int32_t* err;
 };
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream);

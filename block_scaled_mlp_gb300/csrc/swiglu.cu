@@ -202,22 +202,21 @@ __global__ void __launch_bounds__(THREADS, 2)
             slow |= (fabsf(g1) <= 64.0f && clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
             yp[i] = f2_to_bf16x2(f2_mul(f2_from_bf16x2(f2_to_bf16x2(P)), f2_from_bf16x2(up[i])));
           }
+          *reinterpret_cast<uint4*>(yt + tile_chunk(rr, seg)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
           while (slow) {
             const int j = __ffs(slow) - 1;
             slow &= slow - 1;
             const int slot = atomicAdd(&s_qn[buf], 1);
             if (slot < QCAP) {
               q[slot] = (uint16_t)(rr * SF_C + seg * 8 + j);
-            } else {  // queue full: resolve here
-              const uint32_t gw = gp[j >> 1], uw = up[j >> 1];
-              const float g = (j & 1) ? bf16_hi(gw) : bf16_lo(gw);
-              const float u = (j & 1) ? bf16_hi(uw) : bf16_lo(uw);
-              const uint32_t y = f32_to_bf16_bits(__fmul_rn(bf16_lo(silu_bits_slow(g)), u));
-              uint32_t& w = yp[j >> 1];
-              w = (j & 1) ? ((w & 0xFFFFu) | (y << 16)) : ((w & 0xFFFF0000u) | y);
+            } else {  // queue full: resolve here, over this thread's own store above
+              const int off = rr * 128 + (seg * 8 + j) * 2;
+              const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off));
+              const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off));
+              *reinterpret_cast<uint16_t*>(yt + tile_off(rr, seg * 8 + j)) =
+                  (uint16_t)f32_to_bf16_bits(__fmul_rn(bf16_lo(silu_bits_slow(g)), u));
             }
           }
-          *reinterpret_cast<uint4*>(yt + tile_chunk(rr, seg)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
         }
       }
       if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
