@@ -35,23 +35,30 @@ constexpr int MAX_GROUPS = 1024;
 // two 128x256 fp32 accumulators then fill TMEM; MXFP8 needs TMEM columns for
 // its scales).  CL = 2: CTA pairs, each CTA holding its 128 rows of A and
 // half of the B rows, the MMA (M = 256) issued by the even CTA.
-template <bool MX, int BN, int SUB = 1, int CL = 1>
+// KA: 128-byte K atoms per stage (2 only for MXFP8 on one CTA: eight MMAs
+// per stage instead of four, because a stage's fixed latency is what limits
+// the four-MMA pipeline; two stages of 99 KB then fill shared memory).
+template <bool MX, int BN, int SUB = 1, int CL = 1, int KA = 1>
 struct Cfg {
   static_assert(SUB == 1 || (!MX && BN == 256), "two sub-tiles only for the bf16 kernel");
   static_assert(CL == 1 || SUB == 1, "CTA pairs only with single sub-tiles");
+  static_assert(KA == 1 || (MX && CL == 1 && SUB == 1 && BN == 256), "two K atoms only for the MXFP8 1-CTA tile");
   static constexpr int TM = SUB * BM;                      // tile rows
-  static constexpr int BK = MX ? 128 : 64;                 // elements per stage (128 bytes of K)
-  static constexpr int A_BYTES = TM * 128;
-  static constexpr int B_BYTES = (BN / CL) * 128;           // this CTA's rows of the B tile
-  static constexpr int SFA_BYTES = MX ? 512 : 0;           // one scale tile of A per stage
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;  // all of the tile's B scales
-  static constexpr int STAGES = CL == 2 ? 6 : SUB == 2 ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int BK = KA * (MX ? 128 : 64);          // elements per stage (KA x 128 bytes of K)
+  static constexpr int ATOM_A = TM * 128;                  // one 128-byte K atom of the A tile
+  static constexpr int ATOM_B = (BN / CL) * 128;
+  static constexpr int A_BYTES = KA * ATOM_A;
+  static constexpr int B_BYTES = KA * ATOM_B;               // this CTA's rows of the B tile
+  static constexpr int SFA_BYTES = MX ? KA * 512 : 0;      // one scale tile of A per atom
+  static constexpr int SFB_BYTES = MX ? KA * (BN / 128) * 512 : 0;  // all of the tile's B scales
+  static constexpr int STAGES = KA == 2 ? 2 : CL == 2 ? 6 : SUB == 2 ? 3 : (BN == 256 ? 4 : 6);
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // bytes one CTA loads
   static constexpr int NUM_ACC = (BN == 256 || SUB == 2) ? 1 : 2;
   static constexpr int EPI_BYTES = EPI_WARPS * 32 * 64;    // one 32x32 bf16 buffer per warp
   static constexpr int TMEM_COLS = 512;
   static constexpr int SF_COL = NUM_ACC * BN;               // per-stage scale slots from here
-  static constexpr int SF_SLOT = 4 + 4 * (BN / 128);       // TMEM columns of one stage's scales
+  static constexpr int SF_ATOM = 4 + 4 * (BN / 128);       // TMEM columns of one atom's scales
+  static constexpr int SF_SLOT = KA * SF_ATOM;               // TMEM columns of one stage's scales
   static constexpr size_t SMEM = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES +
                                  MAX_GROUPS * 4 * (CL == 1 ? 2 : 1) + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr uint32_t IDESC =
@@ -228,13 +235,13 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
   return ti;
 }
 
-template <bool MX, int BN, int CL, int SUB, bool FUSE>
+template <bool MX, int BN, int CL, int SUB, bool FUSE, int KA>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 GemmParams p) {
-  using C = Cfg<MX, BN, SUB, CL>;
+  using C = Cfg<MX, BN, SUB, CL, KA>;
   static_assert(!FUSE || (MX && CL == 1 && SUB == 1 && BN == 256), "fused SwiGLU: MXFP8, one CTA, 128x256 tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -360,21 +367,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
             continue;
           }
-          const uint32_t bytes = C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? 512 : 0) + C::SFB_BYTES : 0);
+          const uint32_t bytes =
+              C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? C::SFA_BYTES : 0) + C::SFB_BYTES : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sA + stage * C::A_BYTES, &tmA, (int32_t)k, (int32_t)(ti.m_blk * C::TM), &full[stage]);
-          if (FUSE) {  // rows 128n.. of w1 and of w3 in one copy ([2][128] rows)
-            if (p.mode == GEMM_GROUP_M)
-              tma_load_4d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * 128), 0, ti.e, &full[stage]);
+#pragma unroll
+          for (int at = 0; at < KA; ++at) {
+            const int32_t ka = (int32_t)(k + at * 128);
+            uint8_t* dA = sA + stage * C::A_BYTES + at * C::ATOM_A;
+            uint8_t* dB = sB + stage * C::B_BYTES + at * C::ATOM_B;
+            tma_load_2d(dA, &tmA, ka, (int32_t)(ti.m_blk * C::TM), &full[stage]);
+            if (FUSE) {  // rows 128n.. of w1 and of w3 in one copy ([2][128] rows)
+              if (p.mode == GEMM_GROUP_M)
+                tma_load_4d(dB, &tmB, ka, (int32_t)(ti.n_blk * 128), 0, ti.e, &full[stage]);
+              else
+                tma_load_3d(dB, &tmB, ka, (int32_t)(ti.n_blk * 128), 0, &full[stage]);
+            } else if (p.mode == GEMM_GROUP_M)
+              tma_load_3d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
             else
-              tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * 128), 0, &full[stage]);
-          } else if (p.mode == GEMM_GROUP_M)
-            tma_load_3d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
-          else
-            tma_load_2d(sB + stage * C::B_BYTES, &tmB, (int32_t)k, (int32_t)(ti.n_blk * BN), &full[stage]);
+              tma_load_2d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), &full[stage]);
+          }
           if (MX) {
+            // the KA scale tiles of A are adjacent; B's come in one box of
+            // [tile rows][KA atoms][512 B]
             if (ti.store)
-              bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, 512,
+              bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, C::SFA_BYTES,
                         &full[stage]);
             // all of the tile's B scale tiles (BN/128 tile rows) in one copy;
             // rows past N are zero-filled and counted
@@ -418,25 +434,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT;
+#pragma unroll
+          for (int at = 0; at < KA; ++at) {
+          const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT + at * C::SF_ATOM;
           if (MX) {
-            const uint64_t sfa = sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES) >> 4);
+            const uint64_t sfa = sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES + at * 512) >> 4);
             if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col, sfa);
             else tmem_cp_32x128b_x4(sf_col, sfa);
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j) {
-              const uint64_t sfb = sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + j * 512) >> 4);
+              const uint64_t sfb = sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + (j * KA + at) * 512) >> 4);
               if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col + 4 + 4 * j, sfb);
               else tmem_cp_32x128b_x4(sf_col + 4 + 4 * j, sfb);
             }
           }
-          const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES) >> 4);
-          const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES) >> 4);
+          const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES + at * C::ATOM_A) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES + at * C::ATOM_B) >> 4);
 #pragma unroll
           for (int sub = 0; sub < SUB; ++sub) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+              const uint32_t accum = (kb > 0 || at > 0 || k > 0) ? 1u : 0u;
               const uint64_t a = ad + (uint64_t)((sub * BM * 128) >> 4) + 2 * k;
               const uint32_t sf_ids = ((uint32_t)k << 4) | ((uint32_t)k << 29);
               if (MX && CL == 2)
@@ -449,6 +467,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 mma_bf16(d_tmem + (uint32_t)(sub * BN), a, bd + 2 * k, C::IDESC, accum);
             }
           }
+          }  // K atoms of the stage
           // the stage is free (in both CTAs of a pair) once these MMAs are done
           if (CL == 2) tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
           else tc_commit(&empty[stage]);
@@ -688,11 +707,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-template <bool MX, int BN, int CL, int SUB, bool FUSE = false>
+template <bool MX, int BN, int CL, int SUB, bool FUSE = false, int KA = 1>
 int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC0,
                const CUtensorMap& tC1, const CUtensorMap& tSFA, const CUtensorMap& tSFB, GemmParams& p,
                cudaStream_t stream) {
-  using C = Cfg<MX, BN, SUB, CL>;
+  using C = Cfg<MX, BN, SUB, CL, KA>;
   p.m_tiles = (p.M + C::TM - 1) / C::TM;
   p.n_tiles = (p.N + BN - 1) / BN;
   {
@@ -716,7 +735,7 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   p.tiles = units;
   if (units == 0) return MX_OK;
   if (units > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "gemm: too many tiles");
-  auto k = gemm_kernel<MX, BN, CL, SUB, FUSE>;
+  auto k = gemm_kernel<MX, BN, CL, SUB, FUSE, KA>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
   if (CL == 1) {
@@ -763,6 +782,9 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
 // MXFP8 on CTA pairs (cta_group::2, 256x256 tiles, six stages): exact, but
 // slower than single CTAs on GB300 (2.54 vs 2.82 PFLOP/s at 8192x8192x4096),
 // so built only on request.
+#ifndef MX_GEMM_KA2
+#define MX_GEMM_KA2 0  // MXFP8: stages of two 128-byte K atoms (eight MMAs)
+#endif
 #ifndef MX_GEMM_PAIR
 #define MX_GEMM_PAIR 0
 #endif
@@ -775,6 +797,8 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // grouped forward form).
   const bool pair = mx && MX_GEMM_PAIR && BN == 256;
   const bool two_sub = !mx && BN == 256 && g.mode != GEMM_GROUP_M;
+  // MXFP8 on one CTA: two K atoms per stage where K allows it
+  const int ka = (mx && !pair && BN == 256 && g.mode != GEMM_GROUP_K && g.K % 256 == 0 && MX_GEMM_KA2) ? 2 : 1;
   const uint32_t BROWS = pair ? BN / 2 : BN;  // rows of one B load
   const int esz = mx ? 1 : 2;
   const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -858,7 +882,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     const uint64_t hrows = (uint64_t)(g.N / 256);
     uint64_t dims[5] = {128, col_tiles, hrows, 2, (uint64_t)g.E};
     uint64_t strides[4] = {512, col_tiles * 512, col_tiles * 512 * hrows, col_tiles * 512 * hrows * 2};
-    uint32_t box[5] = {128, 1, 1, 2, 1};
+    uint32_t box[5] = {128, (uint32_t)ka, 1, 2, 1};
     rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.mode == GEMM_GROUP_M ? 5 : 4, const_cast<void*>(g.sfb),
                    dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
@@ -868,13 +892,13 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (g.mode == GEMM_GROUP_M) {
       uint64_t dims[4] = {128, col_tiles, tile_rows, (uint64_t)g.E};
       uint64_t strides[3] = {512, col_tiles * 512, col_tiles * 512 * tile_rows};
-      uint32_t box[4] = {128, 1, (uint32_t)(BN / 128), 1};
+      uint32_t box[4] = {128, (uint32_t)ka, (uint32_t)(BN / 128), 1};
       rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(g.sfb), dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
     } else {
       uint64_t dims[3] = {128, col_tiles, tile_rows};
       uint64_t strides[2] = {512, col_tiles * 512};
-      uint32_t box[3] = {128, 1, (uint32_t)(BN / 128)};
+      uint32_t box[3] = {128, (uint32_t)ka, (uint32_t)(BN / 128)};
       rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(g.sfb), dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -894,10 +918,12 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (fuse) {
     if (!mx || BN != 256 || g.mode == GEMM_GROUP_K || g.N % 256 || !g.yq || !g.ys)
       return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: MXFP8 forward form, 2h a multiple of 256");
-    return launch_cfg<true, 256, 1, 1, true>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+    if (ka == 2) return launch_cfg<true, 256, 1, 1, true, 2>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+    return launch_cfg<true, 256, 1, 1, true, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
   }
   if (mx) {
     if (pair) return launch_cfg<true, BN, 2, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+    if (ka == 2) return launch_cfg<true, 256, 1, 1, false, 2>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
     return launch_cfg<true, BN, 1, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
   }
   if (two_sub) return launch_cfg<false, BN, 1, 2>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
