@@ -110,6 +110,20 @@ def bind_to_gpu_cpus(dev):
     return None
 
 
+def max_over_ranks(ms: float, world: int, dev) -> float:
+    """The slowest rank's time (ms per step): every rank contributes its own
+    CUDA-event time and all of them get the maximum (replicas: N independent
+    copies of the step, whole-job throughput = N x work / this time)."""
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def to_dev(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
@@ -218,11 +232,8 @@ def run_gpu(args, rank, world, dev):
     clk = clocks.stop()
     err.check()
     ms = e0.elapsed_time(e1) / args.steps
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = w["flops"] * world / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, world, dev)
+    value = whole_job_tflops(w["flops"], world, ms_max)
     # own kernels per step: 13, or 12 when the w13 GEMM carries the SwiGLU
     # (wgrad_with_hp recipes)
     launches_per_step = 12 if recipe in (mx.RECIPE_RCEIL_WGRAD_HP, mx.RECIPE_FLOOR_WGRAD_HP) else 13
@@ -279,11 +290,8 @@ def run_gpu(args, rank, world, dev):
     a1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    ms_e2e = a0.elapsed_time(a1) / args.steps
-    et = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(et, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = w["flops"] * world / (float(et.item()) * 1e-3) / 1e12
+    ms_e2e = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
+    e2e_value = whole_job_tflops(w["flops"], world, ms_e2e)
     h2d = (hx.numel() + hd.numel()) * 2
     d2h = (ho[0].numel() + hdx[0].numel()) * 2
 
