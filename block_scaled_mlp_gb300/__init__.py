@@ -65,6 +65,7 @@ _SIGS = {
     "mx_linear_bwd": ([_V, _V, _V, _I64, _I64, _I64, _I, _V, _V, _V, _V, _V], _I),
     "mx_token_group_pad": ([_V, _I64, _I32, _I32, _I64, _V, _V, _V, _V, _V, _V], _I),
     "mx_gather_rows": ([_V, _I64, _I64, _V, _I64, _I32, _V, _V, _V], _I),
+    "mx_selftest_wait_timeout": ([_V, _V], _I),
 }
 
 

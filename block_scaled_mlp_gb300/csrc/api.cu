@@ -764,3 +764,28 @@ extern "C" int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const vo
   return mx_mlp_fwd(x, w1, w3, w2, M_total, d, h, offs, E, pad_multiple, recipe, ctx, scratch, out, err_word,
                     stream);
 }
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded pipeline waits (failure detection without a GPU
+// fault): a 256x256x256 MXFP8 GEMM on library-owned buffers whose producer
+// issues no copies, so the MMA and epilogue waits run out of their bound.
+
+namespace {
+constexpr size_t kSelftestBytes = 256 * 256 * 2 + 2 * 2048 + 256 * 256 * 2;  // A, B codes; scales; C
+static __device__ __align__(256) uint8_t g_selftest[kSelftestBytes];
+}  // namespace
+
+extern "C" int mx_selftest_wait_timeout(int32_t* err_word, void* stream) {
+  if (!err_word) return fail(MX_ERR_INVALID_ARG, "err_word is required");
+  uint8_t* base = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&base), g_selftest);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(self-test buffers)");
+  GemmLaunch g{};
+  g.mx = 1; g.mode = GEMM_DENSE;
+  g.a = base; g.b = base + 256 * 256;
+  g.sfa = base + 2 * 256 * 256; g.sfb = base + 2 * 256 * 256 + 2048;
+  g.c0 = base + 2 * 256 * 256 + 2 * 2048;
+  g.M = 256; g.N = 256; g.K = 256; g.E = 1;
+  g.starve = 1; g.err = err_word;
+  return launch_gemm(g, (cudaStream_t)stream);
+}

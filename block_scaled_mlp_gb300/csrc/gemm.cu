@@ -87,6 +87,7 @@ struct GemmParams {
   ScaleDst ys;                // [M, hy/32] scales
   int64_t hy;                 // h
   uint32_t rceil;             // 1: RCEIL scales, 0: FLOOR
+  int32_t starve;             // self-test only: the producer issues nothing, so waits expire
   int32_t* err;
 };
 
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !p.starve) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       if (MX) prefetch_tmap(&tmSFB);
@@ -871,6 +872,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.ys = ScaleDst{(uint8_t*)g.ys, (S + 3) / 4, S, 1};
   }
   p.rceil = g.floor_scale ? 0u : 1u;
+  p.starve = g.starve;
   p.err = g.err;
   // B scales viewed as 32-bit words: one 512-byte tile = 128 words; tile
   // (row rb, column cb) of a [R, S] scale matrix at word (rb*ceil(S/4) + cb)*128.

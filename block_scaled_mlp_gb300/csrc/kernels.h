@@ -87,6 +87,7 @@ struct GemmLaunch {
   void* yq;
   void* ys;
   int floor_scale;   // 1: FLOOR E8M0 scales for y
+  int starve;        // self-test of the bounded waits: the producer issues nothing
   int32_t* err;
 };
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream);

@@ -361,6 +361,17 @@ MX_API int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const void* 
                                      int32_t E, int32_t pad_multiple, int recipe, void* ctx,
                                      void* out, int32_t* err_word, void* stream);
 
+/*
+ * mx_selftest_wait_timeout - test entry of the failure detection: launches a
+ * 256x256x256 MXFP8 GEMM on library-owned device buffers whose load stage
+ * issues nothing, so that the MMA and epilogue pipeline waits run past their
+ * 2 s bound.  The kernel then records MX_ERR_TIMEOUT in *err_word (device
+ * memory, required), releases its tensor memory and returns: no trap, no
+ * hang, and the CUDA context stays usable.  It exists for tests (no
+ * counterpart on the pages); the call takes about 2 s of GPU time.
+ */
+MX_API int mx_selftest_wait_timeout(int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

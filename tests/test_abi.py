@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
                  "mx_bf16_wgrad", "mx_mlp_workspace_size", "mx_mlp_fwd", "mx_mlp_bwd",
                  "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows",
                  "mx_linear_workspace_size", "mx_linear_fwd", "mx_linear_bwd", "mx_quantize_mode",
-                 "mx_swiglu_quant_mode", "mx_swiglu_quant_bwd_mode"]:
+                 "mx_swiglu_quant_mode", "mx_swiglu_quant_bwd_mode", "mx_mlp_fwd_static_scratch",
+                 "mx_selftest_wait_timeout"]:
         assert want in names
 
 
