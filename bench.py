@@ -236,7 +236,7 @@ def run_gpu(args, rank, world, dev):
     value = whole_job_tflops(w["flops"], world, ms_max)
     # own kernels per step: 13, or 12 when the w13 GEMM carries the SwiGLU
     # (wgrad_with_hp recipes)
-    launches_per_step = 12 if recipe in (mx.RECIPE_RCEIL_WGRAD_HP, mx.RECIPE_FLOOR_WGRAD_HP) else 13
+    launches_per_step = 12  # the w13 GEMM carries SwiGLU and the quantization of y under every recipe
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs (x, dout) in from pinned host memory and its results

@@ -24,7 +24,7 @@ __all__ = [
     "MxError", "lib", "library_path", "ROW", "COL", "BOTH", "SCALE_LINEAR", "SCALE_MMA",
     "RECIPE_RCEIL", "RECIPE_RCEIL_WGRAD_HP", "RECIPE_FLOOR", "RECIPE_FLOOR_WGRAD_HP", "SCALE_RCEIL", "SCALE_FLOOR", "GROUP_M", "GROUP_K", "mma_scale_bytes",
     "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
-    "mlp_workspace_size", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
+    "mlp_workspace_size", "mlp_ctx_layout", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
     "token_group_pad", "token_group_capacity", "gather_rows", "linear_fwd", "linear_bwd", "LinearContext",
 ]
 
@@ -54,6 +54,8 @@ _SIGS = {
     "mx_bf16_wgrad": ([_V, _V, _I64, _I64, _I64, _V, _I32, _I32, _V, _V, _V], _I),
     "mx_mlp_workspace_size": ([_I64, _I64, _I64, _I32, _I, ctypes.POINTER(ctypes.c_size_t),
                                ctypes.POINTER(ctypes.c_size_t)], _I),
+    "mx_mlp_ctx_layout": ([_I64, _I64, _I64, _I32, _I, _I, ctypes.POINTER(ctypes.c_size_t),
+                           ctypes.POINTER(ctypes.c_size_t)], _I),
     "mx_mlp_fwd": ([_V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V], _I),
     "mx_mlp_bwd": ([_V, _V, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _I, _V, _V, _V, _V, _V,
                     _V, _V], _I),
@@ -260,6 +262,18 @@ def mlp_workspace_size(M_total, d, h, E=0, recipe=RECIPE_RCEIL):
     return c.value, s.value
 
 
+CTX_TENSORS = ("h13", "xq_col", "xs_col", "yq_col", "ys_col", "x_t", "w13q_col", "w13s_col", "w2q_col",
+               "w2s_col")
+
+
+def mlp_ctx_layout(M_total, d, h, E, recipe, name):
+    """(byte offset, bytes) of a saved tensor inside the mlp_fwd context."""
+    off, n = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().mx_mlp_ctx_layout(M_total, d, h, E, recipe, CTX_TENSORS.index(name), ctypes.byref(off),
+                                   ctypes.byref(n)))
+    return off.value, n.value
+
+
 class MlpContext:
     """What mlp_fwd saves for mlp_bwd (a caller-owned device buffer plus the
     call's arguments)."""
@@ -272,6 +286,14 @@ class MlpContext:
         """The saved w13 GEMM output [M_total, 2h] (bf16), first in the context."""
         M, h = self.args["M"], self.args["h"]
         return self.buf[: M * 2 * h * 2].view(torch.bfloat16).view(M, 2 * h)
+
+    def tensor(self, name: str):
+        """A saved tensor as a flat uint8 view of the context: one of "h13",
+        "xq_col", "xs_col", "yq_col", "ys_col", "x_t", "w13q_col", "w13s_col",
+        "w2q_col", "w2s_col" (MxError if the recipe keeps no such tensor)."""
+        a = self.args
+        off, n = mlp_ctx_layout(a["M"], a["d"], a["h"], a["E"], a["recipe"], name)
+        return self.buf[off:off + n]
 
 
 def mlp_fwd(x, w1, w3, w2, offs=None, recipe=RECIPE_RCEIL, pad_multiple=128, scratch=None,

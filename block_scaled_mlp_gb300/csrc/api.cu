@@ -433,6 +433,35 @@ int mx_mlp_workspace_size(int64_t M_total, int64_t d, int64_t h, int32_t E, int 
   return MX_OK;
 }
 
+int mx_mlp_ctx_layout(int64_t M_total, int64_t d, int64_t h, int32_t E, int recipe, int tensor, size_t* offset,
+                      size_t* bytes) {
+  if (!offset || !bytes) return fail(MX_ERR_INVALID_ARG, "null output pointer");
+  if (M_total <= 0 || d <= 0 || h <= 0 || E < 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
+  if (!valid_recipe(recipe)) return fail(MX_ERR_INVALID_ARG, "unknown recipe");
+  const int64_t Ew = E > 0 ? E : 1;
+  uint8_t* const base = reinterpret_cast<uint8_t*>(uintptr_t(1) << 40);  // any non-null base: offsets only
+  const MlpBuffers b = carve(base, nullptr, M_total, d, h, Ew, recipe);
+  const uint8_t* p = nullptr;
+  int64_t n = 0;
+  switch (tensor) {
+    case MX_CTX_H13: p = b.h13; n = M_total * 2 * h * 2; break;
+    case MX_CTX_XQ_COL: p = b.xq_c; n = d * M_total; break;
+    case MX_CTX_XS_COL: p = b.xs_c; n = mma_scale_bytes(d, M_total); break;
+    case MX_CTX_YQ_COL: p = b.yq_c; n = h * M_total; break;
+    case MX_CTX_YS_COL: p = b.ys_c; n = mma_scale_bytes(h, M_total); break;
+    case MX_CTX_X_T: p = b.x_t; n = d * M_total * 2; break;
+    case MX_CTX_W13Q_COL: p = b.w13q_c; n = Ew * d * 2 * h; break;
+    case MX_CTX_W13S_COL: p = b.w13s_c; n = Ew * mma_scale_bytes(d, 2 * h); break;
+    case MX_CTX_W2Q_COL: p = b.w2q_c; n = Ew * h * d; break;
+    case MX_CTX_W2S_COL: p = b.w2s_c; n = Ew * mma_scale_bytes(h, d); break;
+    default: return fail(MX_ERR_INVALID_ARG, "unknown context tensor %d", tensor);
+  }
+  if (!p) return fail(MX_ERR_UNSUPPORTED, "this recipe keeps no context tensor %d", tensor);
+  *offset = (size_t)(p - base);
+  *bytes = (size_t)n;
+  return MX_OK;
+}
+
 int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, int64_t M, int64_t d, int64_t h,
                const int32_t* offs, int32_t E, int32_t pad_multiple, int recipe, void* ctx, void* scratch, void* out,
                int32_t* err_word, void* stream) {
@@ -469,33 +498,17 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
     q.qc_ld = 2 * h; q.qc_off = half * h; q.qc_bs = d * 2 * h; q.sc_bs = mma_scale_bytes(d, 2 * h);
     if ((rc = launch_quant(q, st))) return rc;
   }
-  if (hp) {
-    // F3 + F4 in one kernel: the w13 GEMM stores h13 and, in its epilogue,
-    // the rowwise MXFP8 y = SwiGLU(h13) (the HP recipe needs no columnwise y)
+  // F3 + F4 in one kernel: the w13 GEMM stores h13 and, in its epilogue,
+  // y = SwiGLU(h13) as rowwise MXFP8 (+ columnwise for the default recipe,
+  // whose weight gradient of w2 contracts y over tokens)
+  {
     GemmLaunch g{};
     g.mx = 1; g.mode = grouped ? GEMM_GROUP_M : GEMM_DENSE;
     g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.w13q_r; g.sfb = b.w13s_r;
     g.M = M; g.N = 2 * h; g.K = d; g.offs = offs; g.E = (int32_t)Ew; g.c0 = b.h13; g.err = err_word;
     g.fuse_swiglu = 1; g.yq = b.yq_r; g.ys = b.ys_r; g.floor_scale = fl;
+    if (!hp) { g.yq_col = b.yq_c; g.ys_col = b.ys_c; }
     if ((rc = launch_gemm(g, st))) return rc;
-  } else {
-    // F3: h13 = x . w13^T
-    {
-      GemmLaunch g{};
-      g.mx = 1; g.mode = grouped ? GEMM_GROUP_M : GEMM_DENSE;
-      g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.w13q_r; g.sfb = b.w13s_r;
-      g.M = M; g.N = 2 * h; g.K = d; g.offs = offs; g.E = (int32_t)Ew; g.c0 = b.h13; g.err = err_word;
-      if ((rc = launch_gemm(g, st))) return rc;
-    }
-    // F4: y = SwiGLU(h13) -> rowwise MX (+ columnwise MX for the default recipe)
-    {
-      SwigluLaunch s{};
-      s.floor_scale = fl;
-      s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
-      s.q_row = b.yq_r; s.s_row = b.ys_r;
-      if (!hp) { s.q_col = b.yq_c; s.s_col = b.ys_c; }
-      if ((rc = launch_swiglu_fwd(s, st))) return rc;
-    }
   }
   // F5: w2 -> rowwise [d, h] and columnwise [h, d], per expert
   {

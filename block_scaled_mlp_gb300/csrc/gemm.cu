@@ -83,8 +83,11 @@ struct GemmParams {
   // fused SwiGLU epilogue (the w13 GEMM of the MLP forward): tile n covers
   // hidden units [128n, 128n+128) of g (accumulator columns 0-127) and of u
   // (128-255); C (h13) is stored and y = SwiGLU(h13) quantized by rows
+  // and, when yqc is set, by columns (32-row blocks of the tile)
   uint8_t* yq;                // [M, hy] codes
   ScaleDst ys;                // [M, hy/32] scales
+  uint8_t* yqc;               // [hy, M] columnwise codes, or NULL
+  ScaleDst ysc;               // [hy, M/32] columnwise scales
   int64_t hy;                 // h
   uint32_t rceil;             // 1: RCEIL scales, 0: FLOOR
   int32_t starve;             // self-test only: the producer issues nothing, so waits expire
@@ -547,6 +550,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           store32g(p.yq + row * p.hy + ycol + 32, z);
           p.ys.put(row, ycol >> 5, 0);
           p.ys.put(row, (ycol >> 5) + 1, 0);
+          if (p.yqc) {  // columns ycol + 2 lane, +1: one 32-row block each
+            const int64_t r0 = ti.m_blk * BM + q * 32;
+            const int64_t c = ycol + 2 * lane;
+            store32g(p.yqc + c * p.M + r0, z);
+            store32g(p.yqc + (c + 1) * p.M + r0, z);
+            p.ysc.put(c, r0 >> 5, 0);
+            p.ysc.put(c + 1, r0 >> 5, 0);
+          }
         }
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
@@ -638,6 +649,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t sc = quant_row32(yw, codes, p.rceil);
           store32g(p.yq + row * p.hy + ycol + 32 * b, codes);
           p.ys.put(row, (ycol >> 5) + b, sc);
+          if (p.yqc) {
+            // columns: the warp's 32 rows are one 32-row block of each of
+            // the 32 columns.  Transpose through the staging buffer: row r
+            // in slot r ^ (r >> 4 & 1), its 16-byte chunk j at j ^ (r >> 1 & 3)
+            // (no bank conflicts on the row writes or the column reads);
+            // lanes l and l ^ 16 take column pair l & 15, 16 rows each.
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            {
+              uint8_t* dst = stg + (lane ^ ((lane >> 4) & 1)) * 64;
+              const int sw = (lane >> 1) & 3;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(dst + ((j ^ sw) * 16)) =
+                    make_uint4(yw[4 * j], yw[4 * j + 1], yw[4 * j + 2], yw[4 * j + 3]);
+            }
+            __syncwarp();
+            const int pc = lane & 15, rh = lane >> 4;
+            auto col_word = [&](int r) {
+              const int rr = rh * 16 + r;
+              return *reinterpret_cast<const volatile uint32_t*>(stg + (rr ^ rh) * 64 +
+                                                                 (((pc >> 2) ^ ((rr >> 1) & 3)) << 4) + ((pc & 3) << 2));
+            };
+            uint32_t ca[4], cb[4], sa, sb;
+            quant_col16x2(col_word, ca, cb, sa, sb, p.rceil);
+            __syncwarp();  // the staging buffer is free for the next store
+            const int64_t c = ycol + 32 * b + 2 * pc;
+            uint8_t* dst = p.yqc + c * p.M + mrow + 16 * rh;
+            store16(dst, ca[0], ca[1], ca[2], ca[3]);
+            store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
+            if (rh == 0) {
+              p.ysc.put(c, mrow >> 5, sa);
+              p.ysc.put(c + 1, mrow >> 5, sb);
+            }
+          }
         }
         if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
         continue;
@@ -870,6 +916,9 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   {
     const int64_t S = p.hy / 32;
     p.ys = ScaleDst{(uint8_t*)g.ys, (S + 3) / 4, S, 1};
+    const int64_t Sc = g.M / 32;
+    p.yqc = (uint8_t*)g.yq_col;
+    p.ysc = ScaleDst{(uint8_t*)g.ys_col, (Sc + 3) / 4, Sc, 1};
   }
   p.rceil = g.floor_scale ? 0u : 1u;
   p.starve = g.starve;
@@ -920,6 +969,8 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (fuse) {
     if (!mx || BN != 256 || g.mode == GEMM_GROUP_K || g.N % 256 || !g.yq || !g.ys)
       return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: MXFP8 forward form, 2h a multiple of 256");
+    if (!g.yq_col != !g.ys_col || (g.yq_col && g.M % 128))
+      return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: columnwise y needs both buffers and M a multiple of 128");
     if (ka == 2) return launch_cfg<true, 256, 1, 1, true, 2>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
     return launch_cfg<true, 256, 1, 1, true, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
   }

@@ -86,6 +86,8 @@ struct GemmLaunch {
   int fuse_swiglu;
   void* yq;
   void* ys;
+  void* yq_col;      // optional columnwise y: codes [h, M] and MMA-layout scales [h, M/32]
+  void* ys_col;
   int floor_scale;   // 1: FLOOR E8M0 scales for y
   int starve;        // self-test of the bounded waits: the producer issues nothing
   int32_t* err;

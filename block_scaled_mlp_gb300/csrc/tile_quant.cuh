@@ -143,6 +143,44 @@ MX_DEVINL void quant_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_
     for (int i = 0; i < 8; ++i) cb[i] = 0x7F7F7F7Fu;
 }
 
+// Two 32-element column blocks split over lanes l and l ^ 16: each lane
+// reads 16 rows of both columns as packed words through ld(i) (column A in
+// the low halves, twice: once for the block maximum, which is combined
+// across the lane pair, once to convert, so that few registers stay live
+// inside a GEMM epilogue).  Writes this lane's 16 codes per column as 4
+// words and returns both scales (the same in both lanes of the pair).
+template <class Ld>
+MX_DEVINL void quant_col16x2(const Ld& ld, uint32_t (&ca)[4], uint32_t (&cb)[4], uint32_t& sa, uint32_t& sb,
+                             uint32_t rceil = 1u) {
+  uint32_t m2 = abs2(ld(0));
+#pragma unroll
+  for (int i = 1; i < 16; ++i) m2 = max2(m2, abs2(ld(i)));
+  m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 16));
+  const uint32_t la = m2 & 0xFFFFu, lb = m2 >> 16;
+  sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la, rceil);
+  sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb, rceil);
+  uint64_t iab;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(iab) : "f"(inv_scale_from_e8m0(sa)), "f"(inv_scale_from_e8m0(sb)));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = ld(4 * i + k);
+      uint64_t x, r;
+      asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(iab));
+      asm("mov.b64 {%0, %1}, %2;" : "=r"(lo[k]), "=r"(hi[k]) : "l"(r));
+    }
+    const uint32_t a01 = cvt_e4m3x2(__uint_as_float(lo[0]), __uint_as_float(lo[1]));
+    const uint32_t a23 = cvt_e4m3x2(__uint_as_float(lo[2]), __uint_as_float(lo[3]));
+    const uint32_t b01 = cvt_e4m3x2(__uint_as_float(hi[0]), __uint_as_float(hi[1]));
+    const uint32_t b23 = cvt_e4m3x2(__uint_as_float(hi[2]), __uint_as_float(hi[3]));
+    ca[i] = sa == 0xFF ? 0x7F7F7F7Fu : (a01 | (a23 << 16));
+    cb[i] = sb == 0xFF ? 0x7F7F7F7Fu : (b01 | (b23 << 16));
+  }
+}
+
 MX_DEVINL void store16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
 }

@@ -234,6 +234,26 @@ MX_API int mx_mlp_workspace_size(int64_t M_total, int64_t d, int64_t h, int32_t 
                           size_t* ctx_bytes, size_t* scratch_bytes);
 
 /*
+ * mx_mlp_ctx_layout - where one saved tensor lives inside the context
+ * buffer of mx_mlp_fwd, for callers that inspect or checkpoint it.
+ *   tensor     one of mx_ctx_tensor
+ *   offset     out: byte offset from the start of ctx (256-byte aligned)
+ *   bytes      out: its size in bytes
+ * Returns MX_ERR_UNSUPPORTED when the recipe keeps no such tensor (the
+ * columnwise x and y exist under the MXFP8 weight-gradient recipes, the
+ * bf16 x^T under the wgrad_with_hp recipes).  Layouts: H13 [M_total, 2h]
+ * bf16; XQ_COL [d, M_total] and YQ_COL [h, M_total] codes with MMA-layout
+ * scales XS_COL / YS_COL; X_T [d, M_total] bf16; W13Q_COL [E, d, 2h] and
+ * W2Q_COL [E, h, d] codes with per-expert MMA-layout scales.
+ */
+typedef enum {
+  MX_CTX_H13 = 0, MX_CTX_XQ_COL = 1, MX_CTX_XS_COL = 2, MX_CTX_YQ_COL = 3, MX_CTX_YS_COL = 4,
+  MX_CTX_X_T = 5, MX_CTX_W13Q_COL = 6, MX_CTX_W13S_COL = 7, MX_CTX_W2Q_COL = 8, MX_CTX_W2S_COL = 9
+} mx_ctx_tensor;
+MX_API int mx_mlp_ctx_layout(int64_t M_total, int64_t d, int64_t h, int32_t E, int recipe, int tensor,
+                             size_t* offset, size_t* bytes);
+
+/*
  * mx_mlp_fwd - forward of the MXFP8 SwiGLU MLP (torchtitan page, Summary):
  *   out = (silu(x . w1^T) * (x . w3^T)) . w2^T with every GEMM in MXFP8.
  *   x [M_total, d] bf16; dense: w1, w3 [h, d], w2 [d, h]; grouped (offs not

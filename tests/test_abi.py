@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
                  "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows",
                  "mx_linear_workspace_size", "mx_linear_fwd", "mx_linear_bwd", "mx_quantize_mode",
                  "mx_swiglu_quant_mode", "mx_swiglu_quant_bwd_mode", "mx_mlp_fwd_static_scratch",
-                 "mx_selftest_wait_timeout"]:
+                 "mx_selftest_wait_timeout", "mx_mlp_ctx_layout"]:
         assert want in names
 
 
@@ -128,3 +128,35 @@ def test_python_binding_fails_loudly_without_cuda_tensors():
     import block_scaled_mlp_gb300 as mx
     with pytest.raises(mx.MxError):
         mx.quantize(torch.zeros(64, 64, dtype=torch.bfloat16))
+
+
+def test_mlp_context_layout(L):
+    """Saved tensors tile the context without overlap, 256-byte aligned, and
+    exist exactly under the recipes that keep them."""
+    import block_scaled_mlp_gb300 as mx
+    M, d, h = 1024, 256, 384
+    for E in (0, 4):
+        for recipe in (mx.RECIPE_RCEIL, mx.RECIPE_RCEIL_WGRAD_HP, mx.RECIPE_FLOOR, mx.RECIPE_FLOOR_WGRAD_HP):
+            ctx_bytes, _ = mx.mlp_workspace_size(M, d, h, E, recipe)
+            hp = recipe in (mx.RECIPE_RCEIL_WGRAD_HP, mx.RECIPE_FLOOR_WGRAD_HP)
+            spans = []
+            for name in mx.CTX_TENSORS:
+                cols = name in ("xq_col", "xs_col", "yq_col", "ys_col")
+                if (name == "x_t" and not hp) or (cols and hp):
+                    with pytest.raises(mx.MxError):
+                        mx.mlp_ctx_layout(M, d, h, E, recipe, name)
+                    continue
+                off, n = mx.mlp_ctx_layout(M, d, h, E, recipe, name)
+                assert off % 256 == 0 and off + n <= ctx_bytes
+                spans.append((off, n, name))
+            spans.sort()
+            assert spans[0][0] == 0 and spans[0][2] == "h13" and spans[0][1] == M * 2 * h * 2
+            for (o0, n0, _), (o1, _, _) in zip(spans, spans[1:]):
+                assert o0 + n0 <= o1
+            Ew = max(E, 1)
+            sizes = {nm: n for _, n, nm in spans}
+            assert sizes["w13q_col"] == Ew * d * 2 * h and sizes["w2q_col"] == Ew * h * d
+            if not hp:
+                assert sizes["yq_col"] == h * M and sizes["ys_col"] == mx.mma_scale_bytes(h, M)
+    off, n = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.mx_mlp_ctx_layout(M, d, h, 0, 0, 10, ctypes.byref(off), ctypes.byref(n)) == 1

@@ -118,9 +118,21 @@ ORACLE_RECIPE = {mx.RECIPE_RCEIL: o.RECIPE_RCEIL, mx.RECIPE_RCEIL_WGRAD_HP: o.RE
                  mx.RECIPE_FLOOR: o.RECIPE_FLOOR, mx.RECIPE_FLOOR_WGRAD_HP: o.RECIPE_FLOOR_WGRAD_HP}
 
 
+def _inputs_grouped_tail(counts, d, h, seed, tail):
+    """Grouped inputs with `tail` rows past the last group whose x values are
+    not zero (the tail must stay inert whatever it holds)."""
+    inp = synth.grouped_mlp_inputs(np.array(counts), d, h, seed, tail_rows=tail)
+    end = int(inp["offs"][-1])
+    inp["x"][end:] = synth.normal_bf16((tail, d), 1.0, seed * 1000 + 9)
+    dev = {k: to_dev(inp[k]) for k in ("x", "w1", "w3", "w2", "dout")}
+    return inp, dev, to_dev(inp["offs"], torch.int32)
+
+
 def _setup(kind):
     if kind == "dense":
         return _inputs_dense(256, 256, 512, seed=0)           # the tiny dense config
+    if kind == "grouped_tail":
+        return _inputs_grouped_tail([100, 0, 300, 28], 256, 384, seed=4, tail=128)
     return _inputs_grouped([100, 0, 300, 28], 256, 384, seed=4)
 
 
@@ -238,3 +250,31 @@ def test_end_to_end_vs_oracle(kind, recipe):
     assert max(errs.values()) <= 2.5e-3, errs
     if offs_h is not None:
         assert not bits(out)[~inp["real_rows"]].any(), "padding rows must stay zero"
+
+
+@pytest.mark.parametrize("kind,recipe", [("dense", mx.RECIPE_RCEIL), ("grouped_tail", mx.RECIPE_RCEIL),
+                                         ("grouped_tail", mx.RECIPE_FLOOR)])
+def test_saved_columnwise_operands_vs_oracle(kind, recipe):
+    """Under the MXFP8 weight-gradient recipes the w13 GEMM's epilogue also
+    quantizes y by columns (each 32-row block of its tile); those codes and
+    the columnwise x that the forward saves equal the oracle bit for bit,
+    including the rows past the last group (zero codes, scale 0x00)."""
+    inp, t, offs = _setup(kind)
+    sc = o.recipe_scale(ORACLE_RECIPE[recipe])
+    err = mx.ErrorWord()
+    out, ctx = mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], offs=offs, recipe=recipe, err=err)
+    torch.cuda.synchronize()
+    err.check()
+    M, d = inp["x"].shape
+    h = inp["w1"].shape[-2]
+    h13 = bits(ctx.h13())
+    if offs is not None:
+        end = int(inp["offs"][-1])
+        assert not h13[end:].any() and not bits(out)[end:].any(), "tail rows must be zero"
+    y = o.swiglu_fwd(*o.split_h13(h13))
+    yqc, ysc = o.quantize_cols(y, sc)
+    assert np.array_equal(u8(ctx.tensor("yq_col")).reshape(h, M), yqc)
+    assert np.array_equal(u8(ctx.tensor("ys_col")), o.scales_to_mma(ysc))
+    xqc, xsc = o.quantize_cols(inp["x"], sc)
+    assert np.array_equal(u8(ctx.tensor("xq_col")).reshape(d, M), xqc)
+    assert np.array_equal(u8(ctx.tensor("xs_col")), o.scales_to_mma(xsc))
