@@ -384,17 +384,43 @@ def dispatch_measure(mx, w, dev, hbm_gbs, iters=10):
 
 def quant_sweep_measure(mx, dev, hbm_gbs, iters=5):
     """The quantize sweep (N x N bf16, N(0,1) with 1% outliers x100) by axis:
-    algorithmic GB/s of mx_quantize against the HBM peak."""
+    algorithmic GB/s of mx_quantize against the HBM peak.  Outputs are
+    allocated once; every timed launch follows a write of a 256 MB buffer
+    (L2 flushed, so the smaller sizes read from HBM too) and is bracketed by
+    its own CUDA events on the launching stream."""
     out = {}
+    L, P = mx.lib(), mx._ptr
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
     for n in (4096, 8192, 16384, 32768):
         x = torch.randn((n, n), device=dev, dtype=torch.float32)
         x = torch.where(torch.rand_like(x) < 0.01, x * 100, x).to(torch.bfloat16)
+        q_row = torch.empty((n, n), dtype=torch.uint8, device=dev)
+        q_col = torch.empty((n, n), dtype=torch.uint8, device=dev)
+        s_row = torch.zeros(mx.mma_scale_bytes(n, n), dtype=torch.uint8, device=dev)
+        s_col = torch.zeros(mx.mma_scale_bytes(n, n), dtype=torch.uint8, device=dev)
         for name, ax, per in (("row", mx.ROW, 2 + 1.03125), ("col", mx.COL, 2 + 1.03125),
                               ("both", mx.BOTH, 2 + 2 * 1.03125)):
-            ms = _event_ms(lambda: mx.quantize(x, ax), iters)
+            qr, sr = (P(q_row), P(s_row)) if ax & mx.ROW else (None, None)
+            qc, sc = (P(q_col), P(s_col)) if ax & mx.COL else (None, None)
+
+            def launch():
+                mx._check(L.mx_quantize_mode(P(x), n, n, ax, mx.SCALE_MMA, mx.SCALE_RCEIL, qr, sr, qc, sc,
+                                             stream.cuda_stream))
+            launch()
+            times = []
+            for _ in range(iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = sum(times) / len(times)
             gbs = n * n * per / (ms * 1e-3) / 1e9
             out[f"{n}_{name}"] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4)}
-        del x
+        del x, q_row, q_col, s_row, s_col
         torch.cuda.empty_cache()
     return out
 
@@ -638,6 +664,11 @@ def run_profile_case(args):
         bs = torch.full((mx.mma_scale_bytes(K, Mt),), 120, dtype=torch.uint8, device=dev)
         fn = lambda: mx.grouped_mm(mx.GROUP_K, aq, as_, bq, bs, offs)
         work, unit = 2.0 * Mt * N * K, "FLOP"
+    elif c == "mlp_fwd_dense":   # default-recipe forward, M=8192, d=4096, h=8192: the fused w13 GEMM
+        d, h = 4096, 8192        # (h13 + rowwise and columnwise MXFP8 y) is its first gemm_kernel launch
+        x, w1, w3, w2 = rnd(M, d), rnd(h, d, std=0.02), rnd(h, d, std=0.02), rnd(d, h, std=0.02)
+        fn = lambda: mx.mlp_fwd(x, w1, w3, w2, recipe=mx.RECIPE_RCEIL)
+        work, unit = 6.0 * M * d * h, "FLOP"
     elif c in ("gemm_mx", "gemm_bf16"):
         N, K = 8192, 4096
         if c == "gemm_mx":
@@ -678,7 +709,8 @@ def main():
     ap.add_argument("--no-quant-sweep", action="store_true", help="skip the quantize-sweep GB/s object")
     ap.add_argument("--profile-case", default=None,
                     choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
-                             "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch"])
+                             "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch",
+                             "mlp_fwd_dense"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
