@@ -85,6 +85,22 @@ MX_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   }
 }
 
+// The same wait by every lane of a warp, with one verdict for all of them
+// (a lane that saw the bound expire makes the whole warp give up).
+MX_DEVINL bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+  const bool ok = mbar_wait(bar, parity, err);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// True in exactly one lane of the (converged) warp.
+MX_DEVINL bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xFFFFFFFF;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r));
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 
 MX_DEVINL void prefetch_tmap(const CUtensorMap* m) {

@@ -332,21 +332,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !p.starve) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
-      if (MX) prefetch_tmap(&tmSFB);
-      if (MX && CL == 2) prefetch_tmap(&tmSFA);
+    // as the MMA issuer: the warp runs the loop, one elected lane issues
+    if (!p.starve) {
+      const bool leader = elect_one();
+      if (leader) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (MX) prefetch_tmap(&tmSFB);
+        if (MX && CL == 2) prefetch_tmap(&tmSFA);
+      }
       int stage = 0; uint32_t phase = 0;
       const int64_t sfa_row_tiles = p.K / 128;  // scale tiles per 128-row block of A
       for (int64_t u = unit0; u < n_units; u += ustep) {
         const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
         bool ok = true;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.err)) { ok = false; break; }
+          if (!warp_wait(&empty[stage], phase ^ 1, p.err)) { ok = false; break; }
           const int64_t k = ti.k0 + (int64_t)kb * C::BK;
           const int64_t kt = k / 128;
-          if (CL == 2) {
+          if (CL == 2 && leader) {
             // both CTAs' copies complete on the even CTA's barrier, which
             // expects the bytes of the pair; a filler tile's rows and scales
             // past the end read as zeros
@@ -368,48 +372,48 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tma_load_3d_pair(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)),
                                  bar);
             }
-            if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-            continue;
-          }
-          const uint32_t bytes =
-              C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? C::SFA_BYTES : 0) + C::SFB_BYTES : 0);
-          mbar_arrive_expect_tx(&full[stage], bytes);
+          } else if (CL == 1 && leader) {
+            const uint32_t bytes =
+                C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? C::SFA_BYTES : 0) + C::SFB_BYTES : 0);
+            mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
-          for (int at = 0; at < KA; ++at) {
-            const int32_t ka = (int32_t)(k + at * 128);
-            uint8_t* dA = sA + stage * C::A_BYTES + at * C::ATOM_A;
-            uint8_t* dB = sB + stage * C::B_BYTES + at * C::ATOM_B;
-            tma_load_2d(dA, &tmA, ka, (int32_t)(ti.m_blk * C::TM), &full[stage]);
-            if (FUSE) {  // rows 128n.. of w1 and of w3 in one copy ([2][128] rows)
-              if (p.mode == GEMM_GROUP_M)
-                tma_load_4d(dB, &tmB, ka, (int32_t)(ti.n_blk * 128), 0, ti.e, &full[stage]);
+            for (int at = 0; at < KA; ++at) {
+              const int32_t ka = (int32_t)(k + at * 128);
+              uint8_t* dA = sA + stage * C::A_BYTES + at * C::ATOM_A;
+              uint8_t* dB = sB + stage * C::B_BYTES + at * C::ATOM_B;
+              tma_load_2d(dA, &tmA, ka, (int32_t)(ti.m_blk * C::TM), &full[stage]);
+              if (FUSE) {  // rows 128n.. of w1 and of w3 in one copy ([2][128] rows)
+                if (p.mode == GEMM_GROUP_M)
+                  tma_load_4d(dB, &tmB, ka, (int32_t)(ti.n_blk * 128), 0, ti.e, &full[stage]);
+                else
+                  tma_load_3d(dB, &tmB, ka, (int32_t)(ti.n_blk * 128), 0, &full[stage]);
+              } else if (p.mode == GEMM_GROUP_M)
+                tma_load_3d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
               else
-                tma_load_3d(dB, &tmB, ka, (int32_t)(ti.n_blk * 128), 0, &full[stage]);
-            } else if (p.mode == GEMM_GROUP_M)
-              tma_load_3d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), ti.e, &full[stage]);
-            else
-              tma_load_2d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), &full[stage]);
-          }
-          if (MX) {
-            // the KA scale tiles of A are adjacent; B's come in one box of
-            // [tile rows][KA atoms][512 B]
-            if (ti.store)
-              bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, C::SFA_BYTES,
-                        &full[stage]);
-            // all of the tile's B scale tiles (BN/128 tile rows) in one copy;
-            // rows past N are zero-filled and counted
-            if (FUSE && p.mode == GEMM_GROUP_M)
-              tma_load_5d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)ti.n_blk, 0, ti.e,
+                tma_load_2d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), &full[stage]);
+            }
+            if (MX) {
+              // the KA scale tiles of A are adjacent; B's come in one box of
+              // [tile rows][KA atoms][512 B]
+              if (ti.store)
+                bulk_load(sSFA + stage * C::SFA_BYTES, p.sfa + (ti.m_blk * sfa_row_tiles + kt) * 512, C::SFA_BYTES,
                           &full[stage]);
-            else if (FUSE)
-              tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)ti.n_blk, 0, &full[stage]);
-            else if (p.mode == GEMM_GROUP_M)
-              tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)), ti.e,
-                          &full[stage]);
-            else
-              tma_load_3d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)),
-                          &full[stage]);
-          }
+              // all of the tile's B scale tiles (BN/128 tile rows) in one copy;
+              // rows past N are zero-filled and counted
+              if (FUSE && p.mode == GEMM_GROUP_M)
+                tma_load_5d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)ti.n_blk, 0, ti.e,
+                            &full[stage]);
+              else if (FUSE)
+                tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)ti.n_blk, 0, &full[stage]);
+              else if (p.mode == GEMM_GROUP_M)
+                tma_load_4d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)), ti.e,
+                            &full[stage]);
+              else
+                tma_load_3d(sSFB + stage * C::SFB_BYTES, &tmSFB, 0, (int32_t)kt, (int32_t)(ti.n_blk * (BN / 128)),
+                            &full[stage]);
+            }
+          }  // elected lane
+          __syncwarp();
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -418,10 +422,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop (warp-uniform control flow, so the
+    // descriptors and TMEM addresses stay in uniform registers) and one
+    // elected lane issues the tcgen05 instructions; a lane-0-only loop costs
+    // about 70 cycles per tcgen05 instruction, which starves the tensor pipe.
     // Descriptors are formed once and advanced by adding the byte offset
     // (>> 4) to their start-address field.  With CTA pairs only the even CTA
     // issues; its MMAs and scale copies act on both CTAs.
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
+      const bool leader = elect_one();
       const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, 2);
       const uint64_t sfa_desc0 = smem_desc(smem_u32(sSFA), 128, 128, 0);
@@ -432,59 +441,69 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int64_t u = unit0; u < n_units && ok; u += ustep) {
         const TileInfo ti = tile_info<C::BK, CL>(p, grp, u, rank);
         if (ti.num_kb == 0) continue;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, p.err)) { ok = false; break; }
+        if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
         for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, p.err)) { ok = false; break; }
+          if (!warp_wait(&full[stage], phase, p.err)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int at = 0; at < KA; ++at) {
-          const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT + at * C::SF_ATOM;
-          if (MX) {
-            const uint64_t sfa = sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES + at * 512) >> 4);
-            if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col, sfa);
-            else tmem_cp_32x128b_x4(sf_col, sfa);
+            const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT + at * C::SF_ATOM;
+            if (MX && leader) {
+              const uint64_t sfa = sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES + at * 512) >> 4);
+              if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col, sfa);
+              else tmem_cp_32x128b_x4(sf_col, sfa);
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j) {
-              const uint64_t sfb = sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + (j * KA + at) * 512) >> 4);
-              if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col + 4 + 4 * j, sfb);
-              else tmem_cp_32x128b_x4(sf_col + 4 + 4 * j, sfb);
+              for (int j = 0; j < BN / 128; ++j) {
+                const uint64_t sfb = sfb_desc0 + (uint64_t)((stage * C::SFB_BYTES + (j * KA + at) * 512) >> 4);
+                if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col + 4 + 4 * j, sfb);
+                else tmem_cp_32x128b_x4(sf_col + 4 + 4 * j, sfb);
+              }
             }
-          }
-          const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES + at * C::ATOM_A) >> 4);
-          const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES + at * C::ATOM_B) >> 4);
+            const uint64_t ad = a_desc0 + (uint64_t)((stage * C::A_BYTES + at * C::ATOM_A) >> 4);
+            const uint64_t bd = b_desc0 + (uint64_t)((stage * C::B_BYTES + at * C::ATOM_B) >> 4);
 #pragma unroll
-          for (int sub = 0; sub < SUB; ++sub) {
+            for (int sub = 0; sub < SUB; ++sub) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t accum = (kb > 0 || at > 0 || k > 0) ? 1u : 0u;
-              const uint64_t a = ad + (uint64_t)((sub * BM * 128) >> 4) + 2 * k;
-              const uint32_t sf_ids = ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              if (MX && CL == 2)
-                mma_mxf8_pair(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
-              else if (MX)
-                mma_mxf8(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
-              else if (CL == 2)
-                mma_bf16_pair(d_tmem, a, bd + 2 * k, C::IDESC, accum);
-              else
-                mma_bf16(d_tmem + (uint32_t)(sub * BN), a, bd + 2 * k, C::IDESC, accum);
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t accum = (kb > 0 || at > 0 || k > 0) ? 1u : 0u;
+                const uint64_t a = ad + (uint64_t)((sub * BM * 128) >> 4) + 2 * k;
+                const uint32_t sf_ids = ((uint32_t)k << 4) | ((uint32_t)k << 29);
+                if (!leader) continue;
+                if (MX && CL == 2)
+                  mma_mxf8_pair(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
+                else if (MX)
+                  mma_mxf8(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
+                else if (CL == 2)
+                  mma_bf16_pair(d_tmem, a, bd + 2 * k, C::IDESC, accum);
+                else
+                  mma_bf16(d_tmem + (uint32_t)(sub * BN), a, bd + 2 * k, C::IDESC, accum);
+              }
             }
-          }
           }  // K atoms of the stage
           // the stage is free (in both CTAs of a pair) once these MMAs are done
-          if (CL == 2) tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
-          else tc_commit(&empty[stage]);
+          if (leader) {
+            if (CL == 2) tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
+            else tc_commit(&empty[stage]);
+          }
+          __syncwarp();
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        if (CL == 2) tc_commit_pair_mc(&acc_full[acc], (uint16_t)0x3);
-        else tc_commit(&acc_full[acc]);
+        if (leader) {
+          if (CL == 2) tc_commit_pair_mc(&acc_full[acc], (uint16_t)0x3);
+          else tc_commit(&acc_full[acc]);
+        }
+        __syncwarp();
         if (++acc == C::NUM_ACC) { acc = 0; acc_phase ^= 1; }
       }
       // all issued MMAs complete before TMEM is released
-      if (CL == 2) tc_commit_pair_mc(done_bar, (uint16_t)0x1);
-      else tc_commit(done_bar);
+      if (leader) {
+        if (CL == 2) tc_commit_pair_mc(done_bar, (uint16_t)0x1);
+        else tc_commit(done_bar);
+      }
+      __syncwarp();
       mbar_wait(done_bar, 0, p.err);
     }
     __syncwarp();
