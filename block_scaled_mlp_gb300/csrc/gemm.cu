@@ -845,23 +845,24 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
 #ifndef MX_GEMM_BN
 #define MX_GEMM_BN 256
 #endif
-// MXFP8 on CTA pairs (cta_group::2, 256x256 tiles, six stages): exact, but
-// slower than single CTAs on GB300 (2.54 vs 2.82 PFLOP/s at 8192x8192x4096),
-// so built only on request.
+// Dense MXFP8 GEMMs on CTA pairs (cta_group::2, 256x256 tiles, six stages):
+// 3.23-3.51 against 3.17-3.46 PFLOP/s on single CTAs at the MLP's shapes.
+// The grouped forms stay on single CTAs (pairs pad odd groups and measured
+// slower there).  Build with -DMX_GEMM_PAIR=0 for single CTAs everywhere.
 #ifndef MX_GEMM_KA2
 #define MX_GEMM_KA2 0  // MXFP8: stages of two 128-byte K atoms (eight MMAs)
 #endif
 #ifndef MX_GEMM_PAIR
-#define MX_GEMM_PAIR 0
+#define MX_GEMM_PAIR 1
 #endif
 
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   constexpr int BN = MX_GEMM_BN;
   const bool mx = g.mx != 0;
-  // MXFP8: 128x256 tiles (256x256 on CTA pairs when built so).  bf16:
+  // MXFP8: 128x256 tiles, 256x256 on CTA pairs for the dense form.  bf16:
   // 256x256 tiles on one CTA as two 128-row sub-tiles (128-row tiles for the
   // grouped forward form).
-  const bool pair = mx && MX_GEMM_PAIR && BN == 256;
+  const bool pair = mx && MX_GEMM_PAIR && BN == 256 && g.mode == GEMM_DENSE && !g.fuse_swiglu;
   const bool two_sub = !mx && BN == 256 && g.mode != GEMM_GROUP_M;
   // MXFP8 on one CTA: two K atoms per stage where K allows it
   const int ka = (mx && !pair && BN == 256 && g.mode != GEMM_GROUP_K && g.K % 256 == 0 && MX_GEMM_KA2) ? 2 : 1;
