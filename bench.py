@@ -669,11 +669,16 @@ def run_profile_case(args):
         x, w1, w3, w2 = rnd(M, d), rnd(h, d, std=0.02), rnd(h, d, std=0.02), rnd(d, h, std=0.02)
         fn = lambda: mx.mlp_fwd(x, w1, w3, w2, recipe=mx.RECIPE_RCEIL)
         work, unit = 6.0 * M * d * h, "FLOP"
-    elif c in ("gemm_mx", "gemm_bf16"):
+    elif c in ("gemm_mx", "gemm_bf16", "gemm_mx_cublas"):
         N, K = 8192, 4096
         if c == "gemm_mx":
             a, b = mx.quantize(rnd(M, K), mx.ROW), mx.quantize(rnd(N, K, std=0.02), mx.ROW)
             fn = lambda: mx.scaled_mm(a["q_row"], a["s_row"], b["q_row"], b["s_row"])
+        elif c == "gemm_mx_cublas":   # the library MXFP8 GEMM on the same operands, for comparison only
+            a, b = mx.quantize(rnd(M, K), mx.ROW), mx.quantize(rnd(N, K, std=0.02), mx.ROW)
+            A, B = a["q_row"].view(torch.float8_e4m3fn), b["q_row"].view(torch.float8_e4m3fn)
+            sa, sb = a["s_row"].view(torch.float8_e8m0fnu), b["s_row"].view(torch.float8_e8m0fnu)
+            fn = lambda: torch._scaled_mm(A, B.t(), sa, sb, out_dtype=torch.bfloat16)
         else:
             at, bt = rnd(N, M), rnd(K, M, std=0.02)   # bf16 wgrad: [N, tokens] x [K, tokens]
             fn = lambda: mx.bf16_wgrad(at, bt)
@@ -710,7 +715,7 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
                              "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch",
-                             "mlp_fwd_dense"])
+                             "mlp_fwd_dense", "gemm_mx_cublas"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
