@@ -236,7 +236,9 @@ def run_gpu(args, rank, world, dev):
     value = whole_job_tflops(w["flops"], world, ms_max)
     # own kernels per step: 13, or 12 when the w13 GEMM carries the SwiGLU
     # (wgrad_with_hp recipes)
-    launches_per_step = 12  # the w13 GEMM carries SwiGLU and the quantization of y under every recipe
+    # the w13 GEMM carries SwiGLU and the quantization of y, except for the
+    # MXFP8-wgrad recipes at d < 5120 (a separate SwiGLU launch)
+    launches_per_step = 12 if (w["recipe"] == "wgrad_hp" or d >= 5120) else 13
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs (x, dout) in from pinned host memory and its results

@@ -499,16 +499,32 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
     if ((rc = launch_quant(q, st))) return rc;
   }
   // F3 + F4 in one kernel: the w13 GEMM stores h13 and, in its epilogue,
-  // y = SwiGLU(h13) as rowwise MXFP8 (+ columnwise for the default recipe,
-  // whose weight gradient of w2 contracts y over tokens)
+  // y = SwiGLU(h13) as rowwise MXFP8 (+ columnwise for the MXFP8-wgrad
+  // recipes, whose weight gradient of w2 contracts y over tokens).  The
+  // epilogue overlaps the next tile's main loop; with both quantizations it
+  // outlasts a main loop of d < kFuseDualMinK (measured at d = 4096: 511 us
+  // fused against 325 + 126 us for the GEMM and the SwiGLU kernel), so
+  // shorter contractions run the two kernels instead (bit-identical).
+  constexpr int64_t kFuseDualMinK = 5120;
+  const bool fuse = hp || d >= kFuseDualMinK;
   {
     GemmLaunch g{};
     g.mx = 1; g.mode = grouped ? GEMM_GROUP_M : GEMM_DENSE;
     g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.w13q_r; g.sfb = b.w13s_r;
     g.M = M; g.N = 2 * h; g.K = d; g.offs = offs; g.E = (int32_t)Ew; g.c0 = b.h13; g.err = err_word;
-    g.fuse_swiglu = 1; g.yq = b.yq_r; g.ys = b.ys_r; g.floor_scale = fl;
-    if (!hp) { g.yq_col = b.yq_c; g.ys_col = b.ys_c; }
+    if (fuse) {
+      g.fuse_swiglu = 1; g.yq = b.yq_r; g.ys = b.ys_r; g.floor_scale = fl;
+      if (!hp) { g.yq_col = b.yq_c; g.ys_col = b.ys_c; }
+    }
     if ((rc = launch_gemm(g, st))) return rc;
+  }
+  if (!fuse) {
+    SwigluLaunch s{};
+    s.floor_scale = fl;
+    s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
+    s.q_row = b.yq_r; s.s_row = b.ys_r;
+    s.q_col = b.yq_c; s.s_col = b.ys_c;
+    if ((rc = launch_swiglu_fwd(s, st))) return rc;
   }
   // F5: w2 -> rowwise [d, h] and columnwise [h, d], per expert
   {

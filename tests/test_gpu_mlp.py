@@ -133,6 +133,12 @@ def _setup(kind):
         return _inputs_dense(256, 256, 512, seed=0)           # the tiny dense config
     if kind == "grouped_tail":
         return _inputs_grouped_tail([100, 0, 300, 28], 256, 384, seed=4, tail=128)
+    # d = 5120: long enough a contraction that the w13 GEMM also carries the
+    # columnwise quantization of y under the MXFP8-wgrad recipes
+    if kind == "dense_wide":
+        return _inputs_dense(256, 5120, 256, seed=6)
+    if kind == "grouped_tail_wide":
+        return _inputs_grouped_tail([100, 0, 300, 28], 5120, 256, seed=7, tail=128)
     return _inputs_grouped([100, 0, 300, 28], 256, 384, seed=4)
 
 
@@ -253,12 +259,15 @@ def test_end_to_end_vs_oracle(kind, recipe):
 
 
 @pytest.mark.parametrize("kind,recipe", [("dense", mx.RECIPE_RCEIL), ("grouped_tail", mx.RECIPE_RCEIL),
-                                         ("grouped_tail", mx.RECIPE_FLOOR)])
+                                         ("grouped_tail", mx.RECIPE_FLOOR), ("dense_wide", mx.RECIPE_RCEIL),
+                                         ("grouped_tail_wide", mx.RECIPE_RCEIL),
+                                         ("grouped_tail_wide", mx.RECIPE_FLOOR)])
 def test_saved_columnwise_operands_vs_oracle(kind, recipe):
-    """Under the MXFP8 weight-gradient recipes the w13 GEMM's epilogue also
-    quantizes y by columns (each 32-row block of its tile); those codes and
-    the columnwise x that the forward saves equal the oracle bit for bit,
-    including the rows past the last group (zero codes, scale 0x00)."""
+    """Under the MXFP8 weight-gradient recipes the forward saves y and x
+    quantized by columns; at d >= 5120 the w13 GEMM's epilogue writes the
+    columnwise y (each 32-row block of its tile), below it the SwiGLU kernel
+    does.  Both equal the oracle bit for bit, including the rows past the
+    last group (zero codes, scale 0x00)."""
     inp, t, offs = _setup(kind)
     sc = o.recipe_scale(ORACLE_RECIPE[recipe])
     err = mx.ErrorWord()
@@ -278,3 +287,21 @@ def test_saved_columnwise_operands_vs_oracle(kind, recipe):
     xqc, xsc = o.quantize_cols(inp["x"], sc)
     assert np.array_equal(u8(ctx.tensor("xq_col")).reshape(d, M), xqc)
     assert np.array_equal(u8(ctx.tensor("xs_col")), o.scales_to_mma(xsc))
+
+
+@pytest.mark.parametrize("kind,recipe", [("dense_wide", mx.RECIPE_RCEIL), ("grouped_tail_wide", mx.RECIPE_FLOOR),
+                                         ("dense_wide", mx.RECIPE_RCEIL_WGRAD_HP)])
+def test_fused_forward_equals_op_chain(kind, recipe):
+    """At d >= 5120 the composite's w13 GEMM carries SwiGLU and both
+    quantizations of y; its outputs equal the per-op chain bit for bit."""
+    inp, t, offs = _setup(kind)
+    err = mx.ErrorWord()
+    out, ctx = mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], offs=offs, recipe=recipe, err=err)
+    dx, dw1, dw3, dw2 = mx.mlp_bwd(ctx, t["dout"], err=err)
+    ch = _chain(t["x"], t["w1"], t["w3"], t["w2"], t["dout"], offs, recipe)
+    torch.cuda.synchronize()
+    err.check()
+    assert torch.equal(ctx.h13(), ch["h13"])
+    for name, a, b in [("out", out, ch["out"]), ("dx", dx, ch["dx"]), ("dw1", dw1, ch["dw1"]),
+                       ("dw3", dw3, ch["dw3"]), ("dw2", dw2, ch["dw2"])]:
+        assert torch.equal(a, b), name
