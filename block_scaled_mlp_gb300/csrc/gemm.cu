@@ -209,8 +209,21 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
     return ti;
   }
   if (p.mode == GEMM_DENSE) {
-    ti.m_blk = 2 * (u % p.m_pairs) + rank;
-    ti.n_blk = u / p.m_pairs;
+    // as for single CTAs, in units of tile-row pairs: columns fastest when B
+    // is the smaller operand and stays in L2, otherwise bands of pair rows
+    int64_t mp;
+    if (p.cols_fast) {
+      mp = u / p.n_tiles;
+      ti.n_blk = u % p.n_tiles;
+    } else {
+      const int64_t pb = p.band >= p.m_tiles ? p.m_pairs : (p.band / 2 > 0 ? p.band / 2 : 1);
+      const int64_t per_band = pb * p.n_tiles;
+      const int64_t b = u / per_band, r = u - b * per_band;
+      const int64_t bm = p.m_pairs - b * pb < pb ? p.m_pairs - b * pb : pb;
+      ti.n_blk = r / bm;
+      mp = b * pb + r % bm;
+    }
+    ti.m_blk = 2 * mp + rank;
     ti.store = ti.m_blk < p.m_tiles;
     return ti;
   }
