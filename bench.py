@@ -44,6 +44,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "source": "fallback"}
 MXFP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 L2_BYTES = 129 * 1024 * 1024
+# dram__bytes_read.sum + dram__bytes_write.sum of the MXFP8 GEMM launches of
+# one step (w13 with SwiGLU, w2, dy, dx), from one ncu capture of the current
+# kernels, next to the bytes those launches must move (operands read once,
+# outputs written once); workloads without a capture report null
+MXFP8_GEMM_TRAFFIC = {"llama3_8b_ffn": 2.9386e9}
+MXFP8_GEMM_ALGO_BYTES = {"llama3_8b_ffn": 1.745e9}
 
 
 def load_peaks():
@@ -305,7 +311,9 @@ def run_gpu(args, rank, world, dev):
     achieved = g["flops"] / (g["ms"] * 1e-3) / 1e12
     roofline = {"kernel": "gemm_kernel<MXFP8,BN=256> (tcgen05 block-scaled)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": round(mx_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / mx_peak, 4), "traffic": None,
+                "frac": round(achieved / mx_peak, 4), "traffic": MXFP8_GEMM_TRAFFIC.get(args.workload),
+                "traffic_unit": "DRAM bytes per step over the step's MXFP8 GEMM launches (ncu)",
+                "algorithmic_bytes": MXFP8_GEMM_ALGO_BYTES.get(args.workload),
                 "peak_source": f"{peaks['source']} bf16 sustained x {MXFP8_OVER_BF16} (nominal fp8/bf16 ratio)"}
     mem = kern["mem"]
     mem_gbs = mem["bytes"] / (mem["ms"] * 1e-3) / 1e9
