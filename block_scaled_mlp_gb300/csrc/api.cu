@@ -86,9 +86,6 @@ inline int64_t mma_scale_bytes(int64_t rows, int64_t cols) {
   return ((rows + 127) / 128) * ((S + 3) / 4) * 512;
 }
 
-inline int64_t scale_bytes(int layout, int64_t rows, int64_t cols) {
-  return layout == MX_SCALE_MMA ? mma_scale_bytes(rows, cols) : rows * (cols / 32);
-}
 
 // MMA-layout padding bytes must read 0x00: clear the buffer first when the
 // matrix does not fill whole tiles.
