@@ -86,7 +86,6 @@ inline int64_t mma_scale_bytes(int64_t rows, int64_t cols) {
   return ((rows + 127) / 128) * ((S + 3) / 4) * 512;
 }
 
-
 // MMA-layout padding bytes must read 0x00: clear the buffer first when the
 // matrix does not fill whole tiles.
 int clear_padding(int layout, void* s, int64_t rows, int64_t cols, cudaStream_t st) {
