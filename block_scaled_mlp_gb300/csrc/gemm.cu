@@ -109,14 +109,15 @@ struct TileInfo {
 
 // Group data in shared memory; ok == false if the offsets break the contract.
 //   ends[e]     cumulative group ends (CL == 1, and GROUP_K with clusters)
-//   pair_end[e] cumulative 128-row tile pairs of groups 0..e (GROUP_M with
-//               clusters; the offsets themselves are then read from global)
+//   pair_end[e] cumulative work units (tile pairs x tile columns) of groups
+//               0..e (GROUP_M with clusters; the offsets themselves are then
+//               read from global)
 struct Groups {
   const int32_t* ends;
   const int32_t* pair_end;
   const int32_t* unit_end;  // GROUP_M without clusters: work units of groups 0..e
   int32_t E;
-  int64_t units_per_n;  // GROUP_M with clusters: tile pairs in one 128-row column
+  int64_t tail_pairs;   // GROUP_M with clusters: tile pairs past the last group
   bool ok;
 };
 
@@ -227,28 +228,39 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
     ti.store = ti.m_blk < p.m_tiles;
     return ti;
   }
-  // GROUP_M with clusters
-  const int64_t P = u % g.units_per_n;
-  ti.n_blk = u / g.units_per_n;
-  const int64_t last_end = g.ok ? (int64_t)p.offs[g.E - 1] : 0;
-  const int64_t groups_pairs = g.ok ? g.pair_end[g.E - 1] : 0;
-  if (P >= groups_pairs) {  // tail (or every tile, for invalid offsets): zeros
-    ti.m_blk = last_end / BM + 2 * (P - groups_pairs) + rank;
+  // GROUP_M with clusters, expert-major like the single-CTA form: all tile
+  // pairs of group e (rows fastest if its rows are the smaller operand, else
+  // columns fastest) before group e+1, then the tail pairs as zero tiles
+  const int64_t grouped = g.ok ? g.pair_end[g.E - 1] : 0;
+  if (u >= grouped) {
+    const int64_t first = g.ok ? (int64_t)p.offs[g.E - 1] / BM : 0;
+    const int64_t r = u - grouped;
+    ti.n_blk = r / g.tail_pairs;
+    ti.m_blk = first + 2 * (r % g.tail_pairs) + rank;
     ti.num_kb = 0;
     ti.store = ti.m_blk < p.m_tiles;
     return ti;
   }
-  int lo = 0, hi = g.E - 1;  // first group whose pair_end is > P
+  int lo = 0, hi = g.E - 1;  // first group whose pair_end is > u
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (g.pair_end[mid] > P) hi = mid; else lo = mid + 1;
+    if (g.pair_end[mid] > u) hi = mid; else lo = mid + 1;
   }
-  const int64_t p_in = P - (lo == 0 ? 0 : g.pair_end[lo - 1]);
+  const int64_t r = u - (lo == 0 ? 0 : g.pair_end[lo - 1]);
   const int64_t start = lo == 0 ? 0 : (int64_t)p.offs[lo - 1];
-  const int64_t mb = ((int64_t)p.offs[lo] - start) / BM;
+  const int64_t mb = ((int64_t)p.offs[lo] - start) / BM;  // tiles of the group
+  const int64_t pe = (mb + 1) / 2;                         // tile pairs of the group
+  int64_t pi;
+  if (mb * BM <= p.N) {
+    ti.n_blk = r / pe;
+    pi = r % pe;
+  } else {
+    pi = r / p.n_tiles;
+    ti.n_blk = r % p.n_tiles;
+  }
   ti.e = lo;
-  ti.m_blk = start / BM + 2 * p_in + rank;
-  ti.store = 2 * p_in + rank < mb;
+  ti.m_blk = start / BM + 2 * pi + rank;
+  ti.store = 2 * pi + rank < mb;
   return ti;
 }
 
@@ -276,7 +288,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* done_bar = acc_empty + C::NUM_ACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
   __shared__ int s_groups_ok;
-  __shared__ long long s_units_per_n;
+  __shared__ long long s_tail_pairs, s_pair_units;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
@@ -316,19 +328,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   if (pairs_m && threadIdx.x == 0) {
     int64_t acc = 0;
+    int32_t prev = 0;
     if (s_groups_ok) {
-      int32_t prev = 0;
       for (int e = 0; e < p.E; ++e) {
         const int32_t v = p.offs[e];
-        acc += ((v - prev) / BM + 1) / 2;
+        acc += ((v - prev) / BM + 1) / 2 * p.n_tiles;
         sGroups[e] = (int32_t)acc;
         prev = v;
       }
-      const int64_t tail = p.m_tiles - prev / BM;
-      s_units_per_n = acc + (tail + 1) / 2;
-    } else {
-      s_units_per_n = p.m_pairs;
     }
+    const int64_t tail = p.m_tiles - prev / BM;  // every tile, for invalid offsets
+    s_tail_pairs = (tail + 1) / 2;
+    s_pair_units = acc + s_tail_pairs * p.n_tiles;
   }
   if (warp == 1) {
     if (CL == 2) { tmem_alloc_pair(tmem_holder, C::TMEM_COLS); tmem_relinquish_pair(); }
@@ -339,9 +350,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
   const uint32_t tmem = *tmem_holder;
-  Groups grp{sGroups, sGroups, sUnitEnd, p.E, pairs_m ? s_units_per_n : 0, s_groups_ok != 0};
+  Groups grp{sGroups, sGroups, sUnitEnd, p.E, pairs_m ? s_tail_pairs : 0, s_groups_ok != 0};
   if (!grp.ok && threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, MX_ERR_BAD_OFFSETS);
-  const int64_t n_units = pairs_m ? grp.units_per_n * p.n_tiles : p.tiles;
+  const int64_t n_units = pairs_m ? s_pair_units : p.tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -858,10 +869,11 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
 #ifndef MX_GEMM_BN
 #define MX_GEMM_BN 256
 #endif
-// Dense MXFP8 GEMMs on CTA pairs (cta_group::2, 256x256 tiles, six stages):
-// 3.23-3.51 against 3.17-3.46 PFLOP/s on single CTAs at the MLP's shapes.
-// The grouped forms stay on single CTAs (pairs pad odd groups and measured
-// slower there).  Build with -DMX_GEMM_PAIR=0 for single CTAs everywhere.
+// Dense and M-grouped MXFP8 GEMMs on CTA pairs (cta_group::2, 256x256
+// tiles, six stages): 3.23-3.51 against 3.17-3.46 PFLOP/s on single CTAs at
+// the MLP's dense shapes, 2-3% less GEMM time in the MoE steps.  The
+// K-grouped weight gradients and the fused w13 GEMM stay on single CTAs.
+// Build with -DMX_GEMM_PAIR=0 for single CTAs everywhere.
 #ifndef MX_GEMM_KA2
 #define MX_GEMM_KA2 0  // MXFP8: stages of two 128-byte K atoms (eight MMAs)
 #endif
@@ -872,10 +884,11 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   constexpr int BN = MX_GEMM_BN;
   const bool mx = g.mx != 0;
-  // MXFP8: 128x256 tiles, 256x256 on CTA pairs for the dense form.  bf16:
+  // MXFP8: 128x256 tiles, 256x256 on CTA pairs for the dense and M-grouped
+  // forms.  bf16:
   // 256x256 tiles on one CTA as two 128-row sub-tiles (128-row tiles for the
   // grouped forward form).
-  const bool pair = mx && MX_GEMM_PAIR && BN == 256 && g.mode == GEMM_DENSE && !g.fuse_swiglu;
+  const bool pair = mx && MX_GEMM_PAIR && BN == 256 && g.mode != GEMM_GROUP_K && !g.fuse_swiglu;
   const bool two_sub = !mx && BN == 256 && g.mode != GEMM_GROUP_M;
   // MXFP8 on one CTA: two K atoms per stage where K allows it
   const int ka = (mx && !pair && BN == 256 && g.mode != GEMM_GROUP_K && g.K % 256 == 0 && MX_GEMM_KA2) ? 2 : 1;
