@@ -24,7 +24,7 @@ Sources, by the pages' titles:
   scale, FP8 E4M3 elements) is the one of the OCP Microscaling Formats v1.0
   specification, which the pages name by "MXFP8" only.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 R1  RCEIL: the block scale is 2^e with e the smallest integer such that
     amax <= 448 * 2^e, clamped to [-127, 127]; the E8M0 byte is e + 127.
