@@ -160,3 +160,9 @@ def test_mlp_context_layout(L):
                 assert sizes["yq_col"] == h * M and sizes["ys_col"] == mx.mma_scale_bytes(h, M)
     off, n = ctypes.c_size_t(), ctypes.c_size_t()
     assert L.mx_mlp_ctx_layout(M, d, h, 0, 0, 10, ctypes.byref(off), ctypes.byref(n)) == 1
+
+
+def test_selftest_needs_an_error_word(L):
+    """The wait-timeout self-test rejects a missing error word on the host,
+    before touching the device."""
+    assert L.mx_selftest_wait_timeout(None, None) == 1  # MX_ERR_INVALID_ARG
