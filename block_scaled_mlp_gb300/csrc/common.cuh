@@ -142,26 +142,6 @@ MX_DEVINL void tma_load_5d(void* dst, const CUtensorMap* m, int32_t x, int32_t y
       : "memory");
 }
 
-// The same tile delivered to the shared memory of every CTA in ctaMask (at
-// this CTA's offsets), each CTA's mbarrier at the same offset receiving the
-// byte count.
-MX_DEVINL void tma_load_2d_mc(void* dst, const CUtensorMap* m, int32_t x, int32_t y, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-MX_DEVINL void tma_load_3d_mc(void* dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z, uint64_t* bar,
-                              uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 MX_DEVINL uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -278,16 +258,6 @@ MX_DEVINL void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As tc_commit, arriving on the mbarrier at the same offset in every CTA of
-// ctaMask.
-MX_DEVINL void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
       : "memory");
 }
 

@@ -123,8 +123,9 @@ struct Groups {
 
 // Work unit -> the tile this CTA (cluster rank `rank`) computes.  Without
 // clusters a unit is one tile.  With 2-CTA clusters a unit is a pair of
-// vertically adjacent tiles sharing one B tile (multicast), the same expert
-// and the same K range; a group with an odd number of 128-row tiles pads its
+// vertically adjacent tiles that one pair MMA (M = 256) computes together:
+// each CTA loads its own 128 rows of A and half of the B tile's rows, both
+// with the same expert and the same K range; a group with an odd number of 128-row tiles pads its
 // last pair with a filler tile that is computed but not stored.
 template <int BK, int CL>
 MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, int rank) {
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
+  if (CL == 2) cluster_sync();  // the peer's barriers exist before any remote arrive or pair copy
   const uint32_t tmem = *tmem_holder;
   Groups grp{sGroups, sGroups, sUnitEnd, p.E, pairs_m ? s_tail_pairs : 0, s_groups_ok != 0};
   if (!grp.ok && threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, MX_ERR_BAD_OFFSETS);
