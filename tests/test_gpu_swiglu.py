@@ -84,12 +84,13 @@ def test_swiglu_bwd_dual_matches_oracle(M, h):
     q, s = o.quantize_rows(dh13)
     qc, sc = o.quantize_cols(dh13)
     got_q, got_qc = u8(res["q_row"]), u8(res["q_col"])
-    # du half bit-exact; dg codes within one E4M3 step, fraction reported
-    assert np.array_equal(got_q[:, h:], q[:, h:])
+    # du and dg halves bit-exact (dg is rounded once from its exact value,
+    # so the one-code fraction the pages allow is 0 here; it is reported)
     dist = o.e4m3_code_distance(got_q[:, :h], q[:, :h])
-    assert dist.max() <= 1
     frac = float((dist > 0).mean())
     print(f"dg one-code fraction (rowwise): {frac:.3e}")
+    assert np.array_equal(got_q[:, h:], q[:, h:])
+    assert np.array_equal(got_q[:, :h], q[:, :h])
     assert np.array_equal(u8(res["s_row"]), o.scales_to_mma(s))
     assert np.array_equal(got_qc, qc)
     assert np.array_equal(u8(res["s_col"]), o.scales_to_mma(sc))
