@@ -40,8 +40,9 @@ R4  SwiGLU forward ("standalone-cast" reading): sigma = RN_f32(1/(1+e^-g))
 R5  SwiGLU backward: du = RN_bf16(RN_f32(dy*a)); dg = RN_bf16 of the exact
     real dy*u*sigma(g)*(1+g*(1-sigma(g))), one rounding; non-finite g gives
     NaN; the sign of a zero result follows IEEE multiplication of the signs.
-R6  GEMMs: C = deq(A) deq(B)^T accumulated exactly (fp64 of exact products),
-    then RN_bf16 for the stored result.  Grouped forward/dgrad: rows of group
+R6  GEMMs: C = deq(A) deq(B)^T, every product exact in float64 and summed
+    in float64 (BLAS order: not exact, but its error is far below the 2e-3
+    normwise bar), then RN_bf16 for the stored result.  Grouped forward/dgrad: rows of group
     e are [offs[e-1], offs[e]); rows past offs[E-1] (the tail) are zero.
     Grouped wgrad: dW[e] sums over group e's rows only; an empty group gives
     exact zeros.
@@ -65,6 +66,16 @@ R14 FLOOR scale mode (the pages name ScaleCalculationMode.RCEIL as one mode
     blocks as in R1; elements as in R2, where saturation now binds (scaled
     values in (448, 512) become +-448).  Recipes "floor" and
     "floor_wgrad_hp" use it for every quantization of the MLP and linear.
+R15 FP8 per-tensor ("tensorwise") grouped MM ("[mxfp8 training] unified
+    MXFP8TrainingConfig and MXFP8TrainingTensor": FP8 GroupedMM is the
+    non-MX FP8 recipe, its workflow temporarily removed there, arithmetic
+    not given).  One fp32 scale per tensor (per expert for [E, ...] weight
+    tensors): amax = max |x| (NaN propagates), s = RN_f32(448 /
+    max(amax, 2^-40)) by IEEE fp32 division (the floor keeps an all-zero
+    tensor finite); code = E4M3 of RN_f32(x * s), RNE and saturating as in
+    R2.  Dequantized value code / s.  GEMMs as in R6 on the dequantized
+    operands: M-grouped with one activation scale and one scale per expert
+    weight, K-grouped (weight gradient) with one scale per operand.
 R13 Per-linear MXFP8 path ("TrainingWeightWrapperTensor base class ...",
     linear override; "Add MXFP8 fused-MLP overrides in torchtitan": non-MLP
     linears keep the per-linear MXFP8 path): out = x w^T with both operands
@@ -564,6 +575,80 @@ def mx_grouped_mm_k(aq, as_, bq, bs, offs) -> np.ndarray:
     an empty group gives exact zeros."""
     A = dequantize(aq, as_)
     B = dequantize(bq, bs)
+    offs = np.asarray(offs)
+    C = np.zeros((len(offs), A.shape[0], B.shape[0]), dtype=np.float64)
+    for e, (s, t) in enumerate(group_bounds(offs)):
+        if t > s:
+            C[e] = A[:, s:t] @ B[:, s:t].T
+    return C
+
+
+# --------------------------------------------------------------------------
+# FP8 per-tensor scaling and its grouped GEMMs (reading R15)
+# --------------------------------------------------------------------------
+
+FP8_AMAX_FLOOR = 2.0 ** -40
+
+
+def fp8_tensor_amax(bits, batch_axes: int = 0) -> np.ndarray:
+    """max |x| over each tensor: over everything (batch_axes=0) or over all
+    but the leading batch axis (batch_axes=1, one amax per expert).  Exact
+    (bf16 values); NaN propagates.  Returned as float32."""
+    v = np.abs(bf16_to_f64(bits))
+    if batch_axes:
+        return v.reshape(v.shape[0], -1).max(axis=1).astype(np.float32)
+    return np.float32(v.max())
+
+
+def fp8_tensor_scale(amax) -> np.ndarray:
+    """Reading R15: s = RN_f32(448 / max(amax, 2^-40)), IEEE fp32 division
+    (numpy float32 arithmetic is correctly rounded).  Pinned on hand-worked
+    values (tests/golden/fp8_tensorwise.json)."""
+    a = np.maximum(np.asarray(amax, dtype=np.float32), np.float32(FP8_AMAX_FLOOR))
+    with np.errstate(invalid="ignore", divide="ignore"):
+        return (np.float32(E4M3_MAX) / a).astype(np.float32)
+
+
+def fp8_quantize_tensor(bits, batch_axes: int = 0):
+    """Reading R15: codes of RN_f32(x * s), s from the tensor's (or each
+    expert's) amax.  Returns (codes uint8, s float32 scalar or [E], amax)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    amax = fp8_tensor_amax(bits, batch_axes)
+    s = fp8_tensor_scale(amax)
+    x = bf16_to_f64(bits).astype(np.float32)             # exact
+    sb = s.reshape((-1,) + (1,) * (bits.ndim - 1)) if batch_axes else s
+    with np.errstate(invalid="ignore", over="ignore"):
+        prod = (x * sb).astype(np.float32)               # one fp32 rounding
+    return e4m3_encode(prod.astype(np.float64)), s, amax
+
+
+def fp8_dequantize(codes, s) -> np.ndarray:
+    """code / s in float64 (s per tensor, or per leading index when s has one
+    entry per row of the leading axis)."""
+    v = e4m3_decode(codes)
+    s = np.asarray(s, dtype=np.float64)
+    if s.ndim == 1:
+        s = s.reshape((-1,) + (1,) * (v.ndim - 1))
+    return v / s
+
+
+def fp8_grouped_mm_m(aq, sa, bq, sb, offs) -> np.ndarray:
+    """M-grouped: A [M_total, K] with one scale; B [E, N, K] with one scale per
+    expert; rows of group e use B[e]; tail rows are zero (as R6)."""
+    A = fp8_dequantize(aq, sa)
+    B = fp8_dequantize(bq, sb)
+    C = np.zeros((A.shape[0], B.shape[1]), dtype=np.float64)
+    for e, (s, t) in enumerate(group_bounds(offs)):
+        if t > s:
+            C[s:t] = A[s:t] @ B[e].T
+    return C
+
+
+def fp8_grouped_mm_k(aq, sa, bq, sb, offs) -> np.ndarray:
+    """K-grouped (weight gradient): A [N, M_total], B [K, M_total], one scale
+    each; C[e] = A[:, group e] . B[:, group e]^T; an empty group is zero."""
+    A = fp8_dequantize(aq, sa)
+    B = fp8_dequantize(bq, sb)
     offs = np.asarray(offs)
     C = np.zeros((len(offs), A.shape[0], B.shape[0]), dtype=np.float64)
     for e, (s, t) in enumerate(group_bounds(offs)):
