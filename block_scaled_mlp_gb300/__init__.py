@@ -26,6 +26,7 @@ __all__ = [
     "quantize", "swiglu_quant", "swiglu_quant_bwd", "scaled_mm", "grouped_mm", "bf16_wgrad",
     "mlp_workspace_size", "mlp_ctx_layout", "mlp_fwd", "mlp_bwd", "mlp_fwd_static_scratch", "MlpContext", "ErrorWord",
     "token_group_pad", "token_group_capacity", "gather_rows", "linear_fwd", "linear_bwd", "LinearContext",
+    "KERNEL_FAMILIES", "launch_counts", "fp8_amax", "fp8_quantize", "fp8_grouped_mm",
 ]
 
 ROW, COL, BOTH = 1, 2, 3
@@ -68,6 +69,10 @@ _SIGS = {
     "mx_token_group_pad": ([_V, _I64, _I32, _I32, _I64, _V, _V, _V, _V, _V, _V], _I),
     "mx_gather_rows": ([_V, _I64, _I64, _V, _I64, _I32, _V, _V, _V], _I),
     "mx_selftest_wait_timeout": ([_V, _V], _I),
+    "mx_launch_counts": ([ctypes.POINTER(ctypes.c_int64), _I], _I),
+    "mx_fp8_amax": ([_V, _I64, _I64, _V, _V], _I),
+    "mx_fp8_quantize": ([_V, _I64, _I64, _I64, _V, _I, _V, _V, _V], _I),
+    "mx_fp8_grouped_mm": ([_I, _V, _V, _V, _V, _I64, _I64, _I64, _V, _I32, _I32, _V, _V, _V], _I),
 }
 
 
@@ -115,6 +120,20 @@ def _need(t, dtype, name):
         raise MxError(1, f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise MxError(1, f"{name} must be contiguous")
+
+
+KERNEL_FAMILIES = ("quant", "swiglu_fwd", "swiglu_bwd", "gemm", "gemm_swiglu", "dispatch", "memset")
+
+
+def launch_counts() -> dict:
+    """The library's launch counters by kernel family (totals since load;
+    take differences around the calls of interest)."""
+    n = len(KERNEL_FAMILIES)
+    buf = (ctypes.c_int64 * n)()
+    got = lib().mx_launch_counts(buf, n)
+    if got != n:
+        raise MxError(got, f"library reports {got} kernel families, binding knows {n}")
+    return {k: int(buf[i]) for i, k in enumerate(KERNEL_FAMILIES)}
 
 
 def mma_scale_bytes(rows: int, cols: int) -> int:
@@ -249,6 +268,56 @@ def bf16_wgrad(a, b, offs=None, pad_multiple=128, err: ErrorWord | None = None):
     c = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
     _check(lib().mx_bf16_wgrad(_ptr(a), _ptr(b), M_total, N, K, _ptr(offs), E, pad_multiple, _ptr(c),
                                err.ptr() if err else None, _stream()))
+    return c
+
+
+# ---------------------------------------------------------------- FP8 per-tensor
+
+
+def fp8_amax(x, batch_axes=0):
+    """amax = max |x| per tensor (batch_axes=0: one value) or per leading
+    index (batch_axes=1: one per expert), as a device fp32 tensor."""
+    _need(x, torch.bfloat16, "x")
+    batch = x.shape[0] if batch_axes else 1
+    amax = torch.empty(batch, dtype=torch.float32, device=x.device)
+    _check(lib().mx_fp8_amax(_ptr(x), batch, x.numel() // batch, _ptr(amax), _stream()))
+    return amax
+
+
+def fp8_quantize(x, amax, axis=ROW):
+    """FP8 per-tensor codes of x [rows, cols] or [batch, rows, cols] with
+    amax [batch] (device fp32).  Returns {"q_row": [.., rows, cols],
+    "q_col": [.., cols, rows]} as requested by axis."""
+    _need(x, torch.bfloat16, "x")
+    lead = x.shape[:-2]
+    rows, cols = x.shape[-2], x.shape[-1]
+    batch = x.numel() // (rows * cols)
+    out = {}
+    if axis & ROW:
+        out["q_row"] = torch.empty(lead + (rows, cols), dtype=torch.uint8, device=x.device)
+    if axis & COL:
+        out["q_col"] = torch.empty(lead + (cols, rows), dtype=torch.uint8, device=x.device)
+    _check(lib().mx_fp8_quantize(_ptr(x), batch, rows, cols, _ptr(amax), axis, _ptr(out.get("q_row")),
+                                 _ptr(out.get("q_col")), _stream()))
+    return out
+
+
+def fp8_grouped_mm(mode, aq, amax_a, bq, amax_b, offs, pad_multiple=128, err: ErrorWord | None = None):
+    """Grouped GEMM on FP8 per-tensor operands.  GROUP_M: aq [M_total, K]
+    (amax_a [1]), bq [E, N, K] (amax_b [E]) -> [M_total, N].  GROUP_K: aq
+    [N, M_total], bq [K, M_total] (amax [1] each) -> [E, N, K]."""
+    _need(offs, torch.int32, "offs")
+    E = offs.numel()
+    if mode == GROUP_M:
+        M_total, K = aq.shape
+        N = bq.shape[1]
+        c = torch.empty((M_total, N), dtype=torch.bfloat16, device=aq.device)
+    else:
+        N, M_total = aq.shape
+        K = bq.shape[0]
+        c = torch.empty((E, N, K), dtype=torch.bfloat16, device=aq.device)
+    _check(lib().mx_fp8_grouped_mm(mode, _ptr(aq), _ptr(amax_a), _ptr(bq), _ptr(amax_b), M_total, N, K, _ptr(offs),
+                                   E, pad_multiple, _ptr(c), err.ptr() if err else None, _stream()))
     return c
 
 

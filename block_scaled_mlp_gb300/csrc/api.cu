@@ -7,6 +7,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -18,7 +19,12 @@ thread_local char g_msg[512] = "";
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_sms[64] = {0};
+std::atomic<long long> g_launches[MX_KERNEL_FAMILIES];
 }  // namespace
+
+void count_launch(int family) {
+  if (family >= 0 && family < MX_KERNEL_FAMILIES) g_launches[family].fetch_add(1, std::memory_order_relaxed);
+}
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -91,6 +97,7 @@ inline int64_t mma_scale_bytes(int64_t rows, int64_t cols) {
 int clear_padding(int layout, void* s, int64_t rows, int64_t cols, cudaStream_t st) {
   if (layout != MX_SCALE_MMA || !s) return MX_OK;
   if (rows % 128 == 0 && (cols / 32) % 4 == 0) return MX_OK;
+  count_launch(MX_KERNEL_MEMSET);
   return cuda_status(cudaMemsetAsync(s, 0, (size_t)mma_scale_bytes(rows, cols), st), "cudaMemsetAsync");
 }
 
@@ -259,6 +266,12 @@ const char* mx_status_string(int s) {
 
 const char* mx_last_error(void) { return g_msg; }
 
+int mx_launch_counts(int64_t* counts, int n) {
+  for (int i = 0; i < n && i < MX_KERNEL_FAMILIES; ++i)
+    counts[i] = counts ? (int64_t)g_launches[i].load(std::memory_order_relaxed) : 0;
+  return MX_KERNEL_FAMILIES;
+}
+
 int mx_quantize(const void* x, int64_t rows, int64_t cols, int axis, int layout, void* q_row, void* s_row,
                 void* q_col, void* s_col, void* stream) {
   return mx_quantize_mode(x, rows, cols, axis, layout, MX_SCALE_RCEIL, q_row, s_row, q_col, s_col, stream);
@@ -396,6 +409,60 @@ int mx_grouped_mm(int mode, const void* aq, const void* as, const void* bq, cons
     g.mode = GEMM_GROUP_M; g.M = M_total; g.N = N; g.K = K;
   } else {
     g.mode = GEMM_GROUP_K; g.M = N; g.N = K; g.K = M_total;
+  }
+  return launch_gemm(g, (cudaStream_t)stream);
+}
+
+// ---- FP8 per-tensor recipe ("[mxfp8 training] unified MXFP8TrainingConfig
+// and MXFP8TrainingTensor", FP8 GroupedMM)
+
+int mx_fp8_amax(const void* x, int64_t batch, int64_t n, float* amax, void* stream) {
+  if (!x || !amax) return fail(MX_ERR_INVALID_ARG, "null pointer argument");
+  if (batch <= 0 || n <= 0) return fail(MX_ERR_INVALID_ARG, "batch and n must be positive");
+  if (batch > 65535) return fail(MX_ERR_UNSUPPORTED, "at most 65535 items");
+  if (n % 8) return fail(MX_ERR_UNSUPPORTED, "n must be a multiple of 8 (got %lld)", (long long)n);
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(amax) & 3)) return fail(MX_ERR_ALIGNMENT, "x must be 16-byte aligned");
+  return launch_fp8_amax(x, batch, n, amax, (cudaStream_t)stream);
+}
+
+int mx_fp8_quantize(const void* x, int64_t batch, int64_t rows, int64_t cols, const float* amax, int axis,
+                    void* q_row, void* q_col, void* stream) {
+  if (!x || !amax) return fail(MX_ERR_INVALID_ARG, "x or amax is null");
+  if (batch <= 0 || rows <= 0 || cols <= 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
+  if (axis < MX_ROW || axis > MX_BOTH) return fail(MX_ERR_INVALID_ARG, "axis must be MX_ROW, MX_COL or MX_BOTH");
+  const bool row = axis & MX_ROW, col = axis & MX_COL;
+  if (cols % 32) return fail(MX_ERR_UNSUPPORTED, "cols must be a multiple of 32 (got %lld)", (long long)cols);
+  if (col && rows % 32) return fail(MX_ERR_UNSUPPORTED, "columnwise needs rows %% 32 == 0 (got %lld)", (long long)rows);
+  if ((row && !q_row) || (col && !q_col)) return fail(MX_ERR_INVALID_ARG, "output is null");
+  if (!aligned16(x) || (row && !aligned16(q_row)) || (col && !aligned16(q_col)))
+    return fail(MX_ERR_ALIGNMENT, "x and code buffers must be 16-byte aligned");
+  if (rows > INT32_MAX || cols > INT32_MAX || batch > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "dimension too large");
+  QuantLaunch q{};
+  q.x = x; q.rows = rows; q.cols = cols; q.batch = (int32_t)batch; q.layout = MX_SCALE_LINEAR;
+  q.q_row = row ? q_row : nullptr;
+  q.q_col = col ? q_col : nullptr; q.qc_ld = rows; q.qc_off = 0; q.qc_bs = rows * cols;
+  q.tw = 1; q.amax = amax;
+  return launch_quant(q, (cudaStream_t)stream);
+}
+
+int mx_fp8_grouped_mm(int mode, const void* aq, const float* amax_a, const void* bq, const float* amax_b,
+                      int64_t M_total, int64_t N, int64_t K, const int32_t* offs, int32_t E, int32_t pad_multiple,
+                      void* c, int32_t* err_word, void* stream) {
+  if (mode != MX_GROUP_M && mode != MX_GROUP_K) return fail(MX_ERR_INVALID_ARG, "mode must be MX_GROUP_M or MX_GROUP_K");
+  if (!aq || !amax_a || !bq || !amax_b || !c || !offs) return fail(MX_ERR_INVALID_ARG, "null pointer argument");
+  if (M_total <= 0 || N <= 0 || K <= 0) return fail(MX_ERR_INVALID_ARG, "sizes must be positive");
+  if (E < 1 || E > 1024) return fail(MX_ERR_INVALID_ARG, "E must be in [1, 1024] (got %d)", E);
+  if (pad_multiple != 128) return fail(MX_ERR_UNSUPPORTED, "pad_multiple must be 128 (got %d)", pad_multiple);
+  if (M_total % 128 || N % 128 || K % 128) return fail(MX_ERR_UNSUPPORTED, "M_total, N, K must be multiples of 128");
+  if (!aligned16(aq) || !aligned16(bq) || !aligned16(c)) return fail(MX_ERR_ALIGNMENT, "buffers must be 16-byte aligned");
+  if (M_total > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "dimension too large");
+  GemmLaunch g{};
+  g.mx = 1; g.tw = 1; g.a = aq; g.b = bq; g.offs = offs; g.E = E; g.c0 = c; g.err = err_word;
+  g.amax_a = amax_a; g.amax_b = amax_b;
+  if (mode == MX_GROUP_M) {
+    g.mode = GEMM_GROUP_M; g.M = M_total; g.N = N; g.K = K; g.amax_b_per_expert = 1;
+  } else {
+    g.mode = GEMM_GROUP_K; g.M = N; g.N = K; g.K = M_total; g.amax_b_per_expert = 0;
   }
   return launch_gemm(g, (cudaStream_t)stream);
 }
@@ -752,11 +819,64 @@ int mx_gather_rows(const void* x, int64_t rows_in, int64_t cols, const int32_t* 
 namespace {
 // The temporary buffer of mx_mlp_fwd_static_scratch.  In host code this name
 // is only a host-side handle, not a device address: the device address is
-// looked up per device with cudaGetSymbolAddress and cached below.
+// looked up with cudaGetSymbolAddress in the CUDA context that is current at
+// the call (the array has one instance per context) and cached under that
+// context's unique ID, so a reset device or a caller's own non-primary
+// context gets its own lookup instead of a stale address.
 static __device__ __align__(256) uint8_t g_static_scratch[MX_STATIC_SCRATCH_BYTES];
 
 std::mutex g_static_mu;
-void* g_static_ptr[64] = {nullptr};
+std::once_flag g_ctx_fn_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+struct StaticSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+constexpr int kStaticSlots = 16;
+StaticSlot g_static_slots[kStaticSlots] = {};
+int g_static_next = 0;
+
+// Unique ID of the current context; false if none is current or the driver
+// calls are unavailable (the address is then looked up on every call).
+bool current_ctx_id(unsigned long long* id) {
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext c = nullptr;
+  return g_ctx_current(&c) == CUDA_SUCCESS && c && g_ctx_id(c, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_static_scratch in the current context (the runtime
+// binds the device's primary context if none is current).
+int static_scratch_address(void** out) {
+  std::call_once(g_ctx_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  unsigned long long id = 0;
+  if (current_ctx_id(&id))
+    for (const StaticSlot& s : g_static_slots)
+      if (s.ptr && s.ctx_id == id) {
+        *out = s.ptr;
+        return MX_OK;
+      }
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(static scratch)");
+  if (current_ctx_id(&id)) {  // the context the lookup ran in
+    g_static_slots[g_static_next] = StaticSlot{id, ptr};
+    g_static_next = (g_static_next + 1) % kStaticSlots;
+  }
+  *out = ptr;
+  return MX_OK;
+}
 }  // namespace
 
 extern "C" int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const void* w3, const void* w2,
@@ -771,21 +891,8 @@ extern "C" int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const vo
                 "mx_mlp_fwd_static_scratch: this problem needs %zu scratch bytes, more than the static "
                 "array's %u; use mx_mlp_fwd with a caller buffer",
                 scratch_bytes, (unsigned)MX_STATIC_SCRATCH_BYTES);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(MX_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
-      void* ptr = nullptr;
-      e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-      if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(static scratch)");
-      g_static_ptr[dev] = ptr;
-    }
-    scratch = g_static_ptr[dev];
-  }
+  if ((rc = static_scratch_address(&scratch))) return rc;
   return mx_mlp_fwd(x, w1, w3, w2, M_total, d, h, offs, E, pad_multiple, recipe, ctx, scratch, out, err_word,
                     stream);
 }

@@ -283,6 +283,16 @@ MX_DEVINL void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       : "memory");
 }
 
+// D (TMEM, fp32) (+)= A(smem) . B(smem)^T with E4M3 operands and no block
+// scales (the FP8 per-tensor recipe applies its scales in the epilogue).
+MX_DEVINL void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Copy a 32-row x 16-byte block from shared memory to TMEM, replicated into
 // each of the four 32-lane quarters.
 MX_DEVINL void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -339,6 +349,14 @@ MX_DEVINL void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, 
       " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
       " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+MX_DEVINL void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

@@ -154,18 +154,25 @@ size_t token_group_pad_workspace(int64_t R, int32_t E) {
 int launch_token_group_pad(const int32_t* expert_of, int64_t R, int32_t E, int32_t pad, int64_t M_cap,
                            int32_t* offs, int32_t* row_dst, int32_t* row_src, void* workspace, int32_t* err,
                            cudaStream_t stream) {
+  count_launch(MX_KERNEL_MEMSET);
   cudaError_t e = cudaMemsetAsync(row_src, 0xFF, (size_t)M_cap * 4, stream);  // -1: pad and tail
   if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync");
-  if (R == 0) return cuda_status(cudaMemsetAsync(offs, 0, (size_t)E * 4, stream), "cudaMemsetAsync");
+  if (R == 0) {
+    count_launch(MX_KERNEL_MEMSET);
+    return cuda_status(cudaMemsetAsync(offs, 0, (size_t)E * 4, stream), "cudaMemsetAsync");
+  }
   int32_t* status = reinterpret_cast<int32_t*>(workspace);
   int32_t* counts = status + 4;
   const int64_t n_chunks = (R + TGP_CHUNK - 1) / TGP_CHUNK;
   const int grid = (int)std::min<int64_t>((n_chunks + TGP_WARPS - 1) / TGP_WARPS, (int64_t)num_sms() * 4);
   const size_t smem = (size_t)TGP_WARPS * E * 4;
+  count_launch(MX_KERNEL_DISPATCH);
   tgp_count_kernel<<<grid, TGP_WARPS * 32, smem, stream>>>(expert_of, R, E, counts, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e, "tgp_count_kernel launch");
+  count_launch(MX_KERNEL_DISPATCH);
   tgp_scan_kernel<<<1, 1024, 0, stream>>>(counts, n_chunks, E, pad, M_cap, offs, status, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e, "tgp_scan_kernel launch");
+  count_launch(MX_KERNEL_DISPATCH);
   tgp_place_kernel<<<grid, TGP_WARPS * 32, smem, stream>>>(expert_of, R, E, counts, status, row_dst, row_src);
   return cuda_status(cudaGetLastError(), "tgp_place_kernel launch");
 }
@@ -175,6 +182,7 @@ int launch_gather_rows(const void* x, int64_t rows_in, int64_t cols, const int32
   if (rows_out == 0) return MX_OK;
   const int64_t vpr = cols / 8;
   const int grid = (int)std::min<int64_t>((rows_out + 7) / 8, (int64_t)num_sms() * 16);
+  count_launch(MX_KERNEL_DISPATCH);
   gather_rows_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows_in, vpr, src, rows_out, div,
                                                 reinterpret_cast<uint4*>(y), err);
   return cuda_status(cudaGetLastError(), "gather_rows_kernel launch");

@@ -38,7 +38,10 @@ constexpr int MAX_GROUPS = 1024;
 // KA: 128-byte K atoms per stage (2 only for MXFP8 on one CTA: eight MMAs
 // per stage instead of four, because a stage's fixed latency is what limits
 // the four-MMA pipeline; two stages of 99 KB then fill shared memory).
-template <bool MX, int BN, int SUB = 1, int CL = 1, int KA = 1>
+// TW: E4M3 operands without block scales (FP8 per-tensor recipe): no scale
+// tiles, kind::f8f6f4 MMAs, and the TMEM the scales would take holds a
+// second accumulator, so a tile's epilogue overlaps the next tile's MMAs.
+template <bool MX, int BN, int SUB = 1, int CL = 1, int KA = 1, bool TW = false>
 struct Cfg {
   static_assert(SUB == 1 || (!MX && BN == 256), "two sub-tiles only for the bf16 kernel");
   static_assert(CL == 1 || SUB == 1, "CTA pairs only with single sub-tiles");
@@ -49,11 +52,13 @@ struct Cfg {
   static constexpr int ATOM_B = (BN / CL) * 128;
   static constexpr int A_BYTES = KA * ATOM_A;
   static constexpr int B_BYTES = KA * ATOM_B;               // this CTA's rows of the B tile
-  static constexpr int SFA_BYTES = MX ? KA * 512 : 0;      // one scale tile of A per atom
-  static constexpr int SFB_BYTES = MX ? KA * (BN / 128) * 512 : 0;  // all of the tile's B scales
+  static_assert(!TW || (MX && KA == 1 && SUB == 1), "FP8 per-tensor: E4M3 operands, one K atom");
+  static constexpr bool BS = MX && !TW;                     // block-scaled MXFP8
+  static constexpr int SFA_BYTES = BS ? KA * 512 : 0;      // one scale tile of A per atom
+  static constexpr int SFB_BYTES = BS ? KA * (BN / 128) * 512 : 0;  // all of the tile's B scales
   static constexpr int STAGES = KA == 2 ? 2 : CL == 2 ? 6 : SUB == 2 ? 3 : (BN == 256 ? 4 : 6);
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // bytes one CTA loads
-  static constexpr int NUM_ACC = (BN == 256 || SUB == 2) ? 1 : 2;
+  static constexpr int NUM_ACC = (TW || !(BN == 256 || SUB == 2)) ? 2 : 1;
   static constexpr int EPI_BYTES = EPI_WARPS * 32 * 64;    // one 32x32 bf16 buffer per warp
   static constexpr int TMEM_COLS = 512;
   static constexpr int SF_COL = NUM_ACC * BN;               // per-stage scale slots from here
@@ -61,9 +66,14 @@ struct Cfg {
   static constexpr int SF_SLOT = KA * SF_ATOM;               // TMEM columns of one stage's scales
   static constexpr size_t SMEM = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES +
                                  MAX_GROUPS * 4 * (CL == 1 ? 2 : 1) + 1024 /*align*/ + 256 /*barriers*/;
+  // instruction descriptors: block-scaled (E8M0 scales, fp32 D implied);
+  // kind::f8f6f4 with fp32 D (bits 4-5 = 1) and E4M3 A and B (type 0);
+  // kind::f16 with fp32 D and bf16 A and B (type 1)
   static constexpr uint32_t IDESC =
-      MX ? ((1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24))
-         : ((1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24));
+      BS ? ((1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24))
+         : TW ? ((1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((CL * BM) >> 4) << 24))
+              : ((1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                 ((uint32_t)((CL * BM) >> 4) << 24));
 };
 
 struct GemmParams {
@@ -90,6 +100,11 @@ struct GemmParams {
   ScaleDst ysc;               // [hy, M/32] columnwise scales
   int64_t hy;                 // h
   uint32_t rceil;             // 1: RCEIL scales, 0: FLOOR
+  // FP8 per-tensor recipe: amax of A (one) and of B (one, or one per expert
+  // when amax_b_per_expert); C = acc * (1/s_a) * (1/s_b), s = 448 / amax
+  const float* amax_a;
+  const float* amax_b;
+  int32_t amax_b_per_expert;
   int32_t starve;             // self-test only: the producer issues nothing, so waits expire
   int32_t* err;
 };
@@ -265,13 +280,19 @@ MX_DEVINL TileInfo tile_info(const GemmParams& p, const Groups& g, int64_t u, in
   return ti;
 }
 
-template <bool MX, int BN, int CL, int SUB, bool FUSE, int KA>
+// Dequantization factor of an FP8 per-tensor operand: 1 / s with
+// s = RN_f32(448 / max(amax, 2^-40)).
+MX_DEVINL float tw_inv_scale(float amax) {
+  return __frcp_rn(__fdiv_rn(448.0f, fmaxf(amax, 0x1p-40f)));
+}
+
+template <bool MX, int BN, int CL, int SUB, bool FUSE, int KA, bool TW>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 GemmParams p) {
-  using C = Cfg<MX, BN, SUB, CL, KA>;
+  using C = Cfg<MX, BN, SUB, CL, KA, TW>;
   static_assert(!FUSE || (MX && CL == 1 && SUB == 1 && BN == 256), "fused SwiGLU: MXFP8, one CTA, 128x256 tiles");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -363,8 +384,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (leader) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (MX) prefetch_tmap(&tmSFB);
-        if (MX && CL == 2) prefetch_tmap(&tmSFA);
+        if (C::BS) prefetch_tmap(&tmSFB);
+        if (C::BS && CL == 2) prefetch_tmap(&tmSFA);
       }
       int stage = 0; uint32_t phase = 0;
       const int64_t sfa_row_tiles = p.K / 128;  // scale tiles per 128-row block of A
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               tma_load_3d_pair(sB + stage * C::B_BYTES, &tmB, (int32_t)k, nrow, ti.e, bar);
             else
               tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, (int32_t)k, nrow, bar);
-            if (MX) {
+            if (C::BS) {
               tma_load_2d_pair(sSFA + stage * C::SFA_BYTES, &tmSFA, 0, (int32_t)(ti.m_blk * sfa_row_tiles + kt),
                                bar);
               if (p.mode == GEMM_GROUP_M)
@@ -399,7 +420,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           } else if (CL == 1 && leader) {
             const uint32_t bytes =
-                C::A_BYTES + C::B_BYTES + (MX ? (ti.store ? C::SFA_BYTES : 0) + C::SFB_BYTES : 0);
+                C::A_BYTES + C::B_BYTES + (C::BS ? (ti.store ? C::SFA_BYTES : 0) + C::SFB_BYTES : 0);
             mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
             for (int at = 0; at < KA; ++at) {
@@ -417,7 +438,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               else
                 tma_load_2d(dB, &tmB, ka, (int32_t)(ti.n_blk * BN), &full[stage]);
             }
-            if (MX) {
+            if (C::BS) {
               // the KA scale tiles of A are adjacent; B's come in one box of
               // [tile rows][KA atoms][512 B]
               if (ti.store)
@@ -475,7 +496,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int at = 0; at < KA; ++at) {
             const uint32_t sf_col = tmem + C::SF_COL + stage * C::SF_SLOT + at * C::SF_ATOM;
-            if (MX && leader) {
+            if (C::BS && leader) {
               const uint64_t sfa = sfa_desc0 + (uint64_t)((stage * C::SFA_BYTES + at * 512) >> 4);
               if (CL == 2) tmem_cp_32x128b_x4_pair(sf_col, sfa);
               else tmem_cp_32x128b_x4(sf_col, sfa);
@@ -496,7 +517,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t a = ad + (uint64_t)((sub * BM * 128) >> 4) + 2 * k;
                 const uint32_t sf_ids = ((uint32_t)k << 4) | ((uint32_t)k << 29);
                 if (!leader) continue;
-                if (MX && CL == 2)
+                if (TW && CL == 2)
+                  mma_f8_pair(d_tmem, a, bd + 2 * k, C::IDESC, accum);
+                else if (TW)
+                  mma_f8(d_tmem, a, bd + 2 * k, C::IDESC, accum);
+                else if (MX && CL == 2)
                   mma_mxf8_pair(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
                 else if (MX)
                   mma_mxf8(d_tmem, a, bd + 2 * k, C::IDESC | sf_ids, sf_col, sf_col + 4, accum);
@@ -577,11 +602,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           bulk_commit();
         }
       };
-      auto pack = [](const uint32_t (&r)[32], uint32_t (&w)[16]) {
+      // FP8 per-tensor: the fp32 accumulator times (1/s_a)(1/s_b), then RN bf16
+      float tfac = 1.0f;
+      if constexpr (TW)
+        tfac = __fmul_rn(tw_inv_scale(p.amax_a[0]), tw_inv_scale(p.amax_b[p.amax_b_per_expert ? ti.e : 0]));
+      auto pack = [tfac](const uint32_t (&r)[32], uint32_t (&w)[16]) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          if constexpr (TW) {
+            w[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                       f2_splat(tfac)));
+          } else {
+            const __nv_bfloat162 b2 =
+                __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
         }
       };
       if (ti.num_kb == 0) {
@@ -798,11 +833,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-template <bool MX, int BN, int CL, int SUB, bool FUSE = false, int KA = 1>
+template <bool MX, int BN, int CL, int SUB, bool FUSE = false, int KA = 1, bool TW = false>
 int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tC0,
                const CUtensorMap& tC1, const CUtensorMap& tSFA, const CUtensorMap& tSFB, GemmParams& p,
                cudaStream_t stream) {
-  using C = Cfg<MX, BN, SUB, CL, KA>;
+  using C = Cfg<MX, BN, SUB, CL, KA, TW>;
   p.m_tiles = (p.M + C::TM - 1) / C::TM;
   p.n_tiles = (p.N + BN - 1) / BN;
   {
@@ -826,11 +861,12 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   p.tiles = units;
   if (units == 0) return MX_OK;
   if (units > INT32_MAX) return fail(MX_ERR_UNSUPPORTED, "gemm: too many tiles");
-  auto k = gemm_kernel<MX, BN, CL, SUB, FUSE, KA>;
+  auto k = gemm_kernel<MX, BN, CL, SUB, FUSE, KA, TW>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
   if (CL == 1) {
     const int grid = (int)std::min<int64_t>(units, num_sms());
+    count_launch(FUSE ? MX_KERNEL_GEMM_SWIGLU : MX_KERNEL_GEMM);
     k<<<grid, GEMM_THREADS, C::SMEM, stream>>>(tA, tB, tC0, tC1, tSFA, tSFB, p);
     return cuda_status(cudaGetLastError(), "gemm_kernel launch");
   }
@@ -861,6 +897,7 @@ int launch_cfg(const GemmLaunch& g, const CUtensorMap& tA, const CUtensorMap& tB
   }
   const int clusters = (int)std::min<int64_t>(units, nres);
   cfg.gridDim = dim3(2 * clusters);
+  count_launch(FUSE ? MX_KERNEL_GEMM_SWIGLU : MX_KERNEL_GEMM);
   e = cudaLaunchKernelEx(&cfg, k, tA, tB, tC0, tC1, tSFA, tSFB, p);
   return cuda_status(e, "gemm_kernel cluster launch");
 }
@@ -968,6 +1005,9 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.ysc = ScaleDst{(uint8_t*)g.ys_col, (Sc + 3) / 4, Sc, 1};
   }
   p.rceil = g.floor_scale ? 0u : 1u;
+  p.amax_a = g.amax_a;
+  p.amax_b = g.amax_b;
+  p.amax_b_per_expert = g.amax_b_per_expert;
   p.starve = g.starve;
   p.err = g.err;
   // B scales viewed as 32-bit words: one 512-byte tile = 128 words; tile
@@ -984,7 +1024,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     rc = make_tmap(&tSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.mode == GEMM_GROUP_M ? 5 : 4, const_cast<void*>(g.sfb),
                    dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
-  } else if (mx) {
+  } else if (mx && !g.tw) {
     const uint64_t col_tiles = (uint64_t)(g.K / 128);
     const uint64_t tile_rows = (uint64_t)(g.N / 128);
     if (g.mode == GEMM_GROUP_M) {
@@ -1005,7 +1045,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // A scales viewed as 32-bit words, one 512-byte tile per row: tile
   // (row block rb, column cb) at row rb*(K/128) + cb.
   CUtensorMap tSFA = tB;
-  if (pair) {
+  if (pair && !g.tw) {
     uint64_t dims[2] = {128, (uint64_t)(g.M / 128) * (uint64_t)(g.K / 128)};
     uint64_t strides[1] = {512};
     uint32_t box[2] = {128, 1};
@@ -1020,6 +1060,12 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
       return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: columnwise y needs both buffers and M a multiple of 128");
     if (ka == 2) return launch_cfg<true, 256, 1, 1, true, 2>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
     return launch_cfg<true, 256, 1, 1, true, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+  }
+  if (g.tw) {
+    if (!mx || BN != 256 || !g.amax_a || !g.amax_b)
+      return fail(MX_ERR_INVALID_ARG, "FP8 per-tensor GEMM: E4M3 operands and both amax pointers");
+    if (pair) return launch_cfg<true, 256, 2, 1, false, 1, true>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
+    return launch_cfg<true, 256, 1, 1, false, 1, true>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);
   }
   if (mx) {
     if (pair) return launch_cfg<true, BN, 2, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);

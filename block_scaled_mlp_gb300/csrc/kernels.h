@@ -17,6 +17,8 @@ int num_sms();
 // Records a thread-local message; returns `code`.
 int fail(int code, const char* fmt, ...);
 int cuda_status(cudaError_t e, const char* what);
+// Adds one to the launch counter of a kernel family (mx_kernel_family).
+void count_launch(int family);
 int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const uint64_t* dims,
               const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
 
@@ -40,9 +42,16 @@ struct QuantLaunch {
   void* t_col;
   int64_t tc_ld, tc_off, tc_bs;
   int floor_scale;   // 1: FLOOR E8M0 scales; 0 (default): RCEIL
+  // FP8 per-tensor codes instead of MX blocks: item b scaled by
+  // 448 / amax[b] (device fp32); no scale bytes are written
+  int tw;
+  const float* amax;
   int32_t* err;
 };
 int launch_quant(const QuantLaunch& q, cudaStream_t stream);
+// amax[b] = max |x| over item b of x [batch, n] (bf16, n % 8 == 0, 16-byte
+// aligned); clears amax first.
+int launch_fp8_amax(const void* x, int64_t batch, int64_t n, float* amax, cudaStream_t stream);
 
 // ---------------------------------------------------------------- SwiGLU
 struct SwigluLaunch {
@@ -89,6 +98,12 @@ struct GemmLaunch {
   void* yq_col;      // optional columnwise y: codes [h, M] and MMA-layout scales [h, M/32]
   void* ys_col;
   int floor_scale;   // 1: FLOOR E8M0 scales for y
+  // FP8 per-tensor recipe (mx = 1, E4M3 codes without block scales): amax
+  // of A ([1]) and of B ([1], or [E] when amax_b_per_expert), device fp32
+  int tw;
+  const float* amax_a;
+  const float* amax_b;
+  int amax_b_per_expert;
   int starve;        // self-test of the bounded waits: the producer issues nothing
   int32_t* err;
 };

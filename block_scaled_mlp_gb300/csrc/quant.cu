@@ -41,6 +41,7 @@ struct QuantKParams {
   // columnwise bf16 transpose: dest [cols, *] bf16
   uint16_t* t_col; int64_t tc_ld; int64_t tc_off; int64_t tc_bs;
   uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
+  const float* amax;  // FP8 per-tensor mode: amax of each batch item
   int32_t tile_scales;  // MMA layout, tile-aligned: a tile's scales are one 512-byte tile per axis
   int32_t* err;
 };
@@ -54,9 +55,13 @@ struct QuantKParams {
 // the layout's padding), meet at a named barrier, and warp 0 writes each
 // tile with one 16-byte store per lane, instead of 1024 single-byte stores
 // scattered over the tile.
-template <bool ROW, int COLK>
+//
+// TW: FP8 per-tensor codes instead of MX blocks (no scale bytes written):
+// every element of batch item b is scaled by s = 448 / amax[b].
+template <bool ROW, int COLK, bool TW = false>
 __global__ void __launch_bounds__(QT_THREADS, 2)
     quant_kernel(const __grid_constant__ CUtensorMap tmx, QuantKParams p) {
+  static_assert(!TW || COLK != 2, "per-tensor FP8 writes codes only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sscale = smem + QT_STAGES * QT_TILE_BYTES;  // [2 tile parities][row 512 | col 512]
@@ -144,7 +149,9 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           pk[4 * k] = v.x; pk[4 * k + 1] = v.y; pk[4 * k + 2] = v.z; pk[4 * k + 3] = v.w;
         }
         uint32_t codes[8];
-        const uint32_t s = quant_row32(pk, codes, p.rceil);
+        uint32_t s = 0;
+        if constexpr (TW) tw_row32(pk, codes, splat_f32x2(tw_scale(p.amax[b])));
+        else s = quant_row32(pk, codes, p.rceil);
         const int64_t r = r0 + rr;
         const int64_t c = c0 + box * 64 + jj * 32;
         const bool in = r < p.rows && c < p.cols;
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           uint8_t* dst = qrow + r * p.qr_ld + c;
           store16(dst, codes[0], codes[1], codes[2], codes[3]);
           store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
-          if (!p.tile_scales) sd.put(r, c >> 5, s);
+          if (!TW && !p.tile_scales) sd.put(r, c >> 5, s);
         }
         if (p.tile_scales) srow_t[(rr & 31) * 16 + (rr >> 5) * 4 + box * 2 + jj] = in ? (uint8_t)s : 0;
       }
@@ -180,14 +187,16 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           uint8_t* qcol = p.q_col + b * p.qc_bs;
           ScaleDst sd = p.s_col;
           sd.base += b * p.sc_bs;
-          uint32_t ca[8], cb[8], sa, sb;
-          quant_col32x2(v, ca, cb, sa, sb, p.rceil);
+          uint32_t ca[8], cb[8], sa = 0, sb = 0;
+          if constexpr (TW) tw_col32x2(v, ca, cb, splat_f32x2(tw_scale(p.amax[b])));
+          else quant_col32x2(v, ca, cb, sa, sb, p.rceil);
           uint8_t* dst = qcol + cg * p.qc_ld + p.qc_off + rg;
           store16(dst, ca[0], ca[1], ca[2], ca[3]);
           store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
           store16(dst + p.qc_ld, cb[0], cb[1], cb[2], cb[3]);
           store16(dst + p.qc_ld + 16, cb[4], cb[5], cb[6], cb[7]);
-          if (p.tile_scales) {
+          if (TW) {
+          } else if (p.tile_scales) {
             scol_t[(cl & 31) * 16 + (cl >> 5) * 4 + rb] = (uint8_t)sa;
             scol_t[((cl + 1) & 31) * 16 + ((cl + 1) >> 5) * 4 + rb] = (uint8_t)sb;
           } else {
@@ -235,7 +244,59 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
   }
 }
 
+// amax of each batch item (FP8 per-tensor recipe): blockIdx.y is the item;
+// each thread keeps the packed bf16 maximum of |x| over 16-byte vectors
+// (four independent loads in flight), the block reduces it and one atomicMax
+// on the fp32 bit pattern merges the blocks of an item (non-negative floats
+// order like their bit patterns; a NaN, 0x7FC00000, beats every number).
+constexpr int AMAX_THREADS = 256;
+
+__global__ void __launch_bounds__(AMAX_THREADS)
+    fp8_amax_kernel(const uint4* __restrict__ x, int64_t vec_per_item, float* amax) {
+  const uint4* xb = x + (int64_t)blockIdx.y * vec_per_item;
+  const int64_t stride = (int64_t)gridDim.x * AMAX_THREADS;
+  uint32_t m[4] = {0, 0, 0, 0};
+  int64_t i = (int64_t)blockIdx.x * AMAX_THREADS + threadIdx.x;
+  for (; i + 3 * stride < vec_per_item; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldcs(xb + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = max2(m[k], max2(max2(abs2(v[k].x), abs2(v[k].y)), max2(abs2(v[k].z), abs2(v[k].w))));
+  }
+  for (; i < vec_per_item; i += stride) {
+    const uint4 v = __ldcs(xb + i);
+    m[0] = max2(m[0], max2(max2(abs2(v.x), abs2(v.y)), max2(abs2(v.z), abs2(v.w))));
+  }
+  uint32_t r = max2(max2(m[0], m[1]), max2(m[2], m[3]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) r = max2(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+  __shared__ uint32_t s_m[AMAX_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = r;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = s_m[0];
+    for (int w = 1; w < AMAX_THREADS / 32; ++w) t = max2(t, s_m[w]);
+    atomicMax(reinterpret_cast<unsigned int*>(amax) + blockIdx.y, max_halves(t) << 16);
+  }
+}
+
 }  // namespace
+
+int launch_fp8_amax(const void* x, int64_t batch, int64_t n, float* amax, cudaStream_t stream) {
+  if (batch <= 0 || n <= 0) return MX_OK;
+  count_launch(MX_KERNEL_MEMSET);
+  cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)batch * 4, stream);
+  if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync");
+  const int64_t vec = n / 8;
+  const int64_t want = ((int64_t)num_sms() * 8 + batch - 1) / batch;   // ~8 blocks per SM in all
+  const int64_t need = (vec + AMAX_THREADS * 4 - 1) / (AMAX_THREADS * 4);
+  const int gx = (int)std::max<int64_t>(1, std::min<int64_t>(want, need));
+  count_launch(MX_KERNEL_QUANT);
+  fp8_amax_kernel<<<dim3(gx, (unsigned)batch), AMAX_THREADS, 0, stream>>>(reinterpret_cast<const uint4*>(x), vec,
+                                                                          amax);
+  return cuda_status(cudaGetLastError(), "fp8_amax_kernel launch");
+}
 
 int launch_quant(const QuantLaunch& q, cudaStream_t stream) {
   const bool row = q.q_row != nullptr;
@@ -264,30 +325,39 @@ int launch_quant(const QuantLaunch& q, cudaStream_t stream) {
   p.sc_off = q.qc_off / 32; p.sc_bs = q.sc_bs;
   p.t_col = (uint16_t*)q.t_col; p.tc_ld = q.tc_ld; p.tc_off = q.tc_off; p.tc_bs = q.tc_bs;
   p.rceil = q.floor_scale ? 0u : 1u;
+  p.amax = q.amax;
   // whole scale tiles per 128x128 tile: MMA layout, columnwise MXFP8 output
   // (rowwise alone measured ~3% slower with the per-tile barrier than with
   // byte stores), the columnwise scale columns starting on a tile boundary
-  p.tile_scales = (q.layout == MX_SCALE_MMA && colk == 1 && (p.sc_off & 3) == 0) ? 1 : 0;
+  p.tile_scales = (!q.tw && q.layout == MX_SCALE_MMA && colk == 1 && (p.sc_off & 3) == 0) ? 1 : 0;
   p.err = q.err;
 
   const int64_t n_tiles = p.row_tiles * p.col_tiles * q.batch;
   if (n_tiles == 0) return MX_OK;
   int grid = (int)std::min<int64_t>(n_tiles, (int64_t)num_sms() * 2);
   cudaError_t e;
-#define MX_LAUNCH_Q(R, C)                                                                      \
+#define MX_LAUNCH_Q(R, C, TW)                                                                  \
   do {                                                                                         \
-    auto k = quant_kernel<R, C>;                                                               \
+    auto k = quant_kernel<R, C, TW>;                                                           \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QT_SMEM);    \
     if (e == cudaSuccess) {                                                                    \
+      count_launch(MX_KERNEL_QUANT);                                                           \
       k<<<grid, QT_THREADS, QT_SMEM, stream>>>(tm, p);                                         \
       e = cudaGetLastError();                                                                  \
     }                                                                                          \
   } while (0)
-  if (row && colk == 0) MX_LAUNCH_Q(true, 0);
-  else if (row && colk == 1) MX_LAUNCH_Q(true, 1);
-  else if (row && colk == 2) MX_LAUNCH_Q(true, 2);
-  else if (!row && colk == 1) MX_LAUNCH_Q(false, 1);
-  else if (!row && colk == 2) MX_LAUNCH_Q(false, 2);
+  if (q.tw) {
+    if (!q.amax || colk == 2) return fail(MX_ERR_INVALID_ARG, "per-tensor FP8 cast: amax required, codes only");
+    if (row && colk == 0) MX_LAUNCH_Q(true, 0, true);
+    else if (row && colk == 1) MX_LAUNCH_Q(true, 1, true);
+    else if (!row && colk == 1) MX_LAUNCH_Q(false, 1, true);
+    else return MX_ERR_INVALID_ARG;
+  }
+  else if (row && colk == 0) MX_LAUNCH_Q(true, 0, false);
+  else if (row && colk == 1) MX_LAUNCH_Q(true, 1, false);
+  else if (row && colk == 2) MX_LAUNCH_Q(true, 2, false);
+  else if (!row && colk == 1) MX_LAUNCH_Q(false, 1, false);
+  else if (!row && colk == 2) MX_LAUNCH_Q(false, 2, false);
   else return MX_ERR_INVALID_ARG;
 #undef MX_LAUNCH_Q
   return cuda_status(e, "quant_kernel launch");

@@ -577,11 +577,11 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   if (s.q_col) {
     auto k = swiglu_fwd_kernel<true>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SF_SMEM);
-    if (e == cudaSuccess) { k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
+    if (e == cudaSuccess) { count_launch(MX_KERNEL_SWIGLU_FWD); k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
   } else {
     auto k = swiglu_fwd_kernel<false>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SF_SMEM);
-    if (e == cudaSuccess) { k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
+    if (e == cudaSuccess) { count_launch(MX_KERNEL_SWIGLU_FWD); k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
   }
   return cuda_status(e, "swiglu_fwd_kernel launch");
 }
@@ -624,7 +624,7 @@ int launch_swiglu_bwd(const SwigluLaunch& s, cudaStream_t stream) {
   do {                                                                                          \
     auto k = swiglu_bwd_kernel<MODE>;                                                           \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SB_SMEM);     \
-    if (e == cudaSuccess) { k<<<grid, THREADS, SB_SMEM, stream>>>(tdy, th, p); e = cudaGetLastError(); } \
+    if (e == cudaSuccess) { count_launch(MX_KERNEL_SWIGLU_BWD); k<<<grid, THREADS, SB_SMEM, stream>>>(tdy, th, p); e = cudaGetLastError(); } \
   } while (0)
   if (mode == 0) MX_LAUNCH_B(0);
   else if (mode == 1) MX_LAUNCH_B(1);

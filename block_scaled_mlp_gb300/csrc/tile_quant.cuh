@@ -181,6 +181,39 @@ MX_DEVINL void quant_col16x2(const Ld& ld, uint32_t (&ca)[4], uint32_t (&cb)[4],
   }
 }
 
+// ---- FP8 per-tensor ("tensorwise") scaling: one fp32 scale s per tensor,
+// s = RN_f32(448 / max(amax, 2^-40)); code = E4M3 (RNE, saturating) of
+// RN_f32(x * s).  s is not a power of two, so the product rounds once in
+// fp32 before the E4M3 conversion rounds again.
+MX_DEVINL float tw_scale(float amax) { return __fdiv_rn(448.0f, fmaxf(amax, 0x1p-40f)); }
+
+// 32 row elements held as 16 packed bf16 pairs -> 8 words of codes.
+MX_DEVINL void tw_row32(const uint32_t (&p)[16], uint32_t (&codes)[8], uint64_t s2) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) codes[i] = e4m3x2_scaled(p[2 * i], s2) | (e4m3x2_scaled(p[2 * i + 1], s2) << 16);
+}
+
+// Two columns of 32 rows held as 32 packed words (column A in the low
+// halves) -> 8 words of codes per column.
+MX_DEVINL void tw_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_t (&cb)[8], uint64_t s2) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint64_t x, r;
+      const uint32_t w = v[4 * i + k];
+      asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(s2));
+      asm("mov.b64 {%0, %1}, %2;" : "=r"(lo[k]), "=r"(hi[k]) : "l"(r));
+    }
+    ca[i] = cvt_e4m3x2(__uint_as_float(lo[0]), __uint_as_float(lo[1])) |
+            (cvt_e4m3x2(__uint_as_float(lo[2]), __uint_as_float(lo[3])) << 16);
+    cb[i] = cvt_e4m3x2(__uint_as_float(hi[0]), __uint_as_float(hi[1])) |
+            (cvt_e4m3x2(__uint_as_float(hi[2]), __uint_as_float(hi[3])) << 16);
+  }
+}
+
 MX_DEVINL void store16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
 }

@@ -367,8 +367,11 @@ MX_API int mx_gather_rows(const void* x, int64_t rows_in, int64_t cols, const in
  * - Problems whose scratch_bytes (mx_mlp_workspace_size) exceed
  *   MX_STATIC_SCRATCH_BYTES are rejected with MX_ERR_UNSUPPORTED.
  * - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- * - The first call on a device looks up the array's device address (with
- *   that device current) and caches it; make that first call before any
+ * - The array has one instance per CUDA context.  The first call in a
+ *   context (the one current on the calling thread; the device's primary
+ *   context if none is) looks up the array's device address there and
+ *   caches it under the context's unique ID, so a device reset or a
+ *   different context is looked up afresh.  Make that first call before any
  *   CUDA stream capture.
  * - All calls share the one array and the kernels overwrite every byte they
  *   read back, so no clearing is needed between calls; calls that overlap
@@ -380,6 +383,87 @@ MX_API int mx_mlp_fwd_static_scratch(const void* x, const void* w1, const void* 
                                      int64_t M_total, int64_t d, int64_t h, const int32_t* offs,
                                      int32_t E, int32_t pad_multiple, int recipe, void* ctx,
                                      void* out, int32_t* err_word, void* stream);
+
+/*
+ * ---- FP8 per-tensor ("tensorwise") recipe: the non-MX FP8 grouped MM
+ * ("[mxfp8 training] unified MXFP8TrainingConfig and MXFP8TrainingTensor",
+ * "Temporarily removed FP8GroupedMM quantize_ workflow support": FP8
+ * GroupedMM is the other, non-MX recipe; its arithmetic is not given there.
+ * Reading used here: one fp32 scale per tensor, or per expert for a
+ * [E, N, K] weight, s = RN_f32(448 / max(amax, 2^-40)) with amax = max |x|;
+ * code = E4M3 (round to nearest even, saturating) of RN_f32(x * s); the
+ * dequantized value is code / s.)  A tensor's scale is carried as its amax
+ * (device fp32), from which every consumer derives s.
+ */
+
+/*
+ * mx_fp8_amax - amax[b] = max |x| over item b of x [batch, n] (bf16, device).
+ *   x: 16-byte aligned, n % 8 == 0; batch <= 65535.
+ *   amax: device fp32 [batch], overwritten (the call clears it first).  A
+ *   NaN in an item makes its amax NaN.  HBM-bound: reads x once.
+ * Errors: MX_ERR_INVALID_ARG (null, sizes), MX_ERR_UNSUPPORTED (n % 8),
+ * MX_ERR_ALIGNMENT.
+ */
+MX_API int mx_fp8_amax(const void* x, int64_t batch, int64_t n, float* amax, void* stream);
+
+/*
+ * mx_fp8_quantize - FP8 per-tensor codes of x [batch, rows, cols] (bf16),
+ * item b scaled by s = 448 / max(amax[b], 2^-40) (amax device fp32 [batch],
+ * e.g. from mx_fp8_amax; only the device reads it).
+ *   axis MX_ROW: q_row [batch, rows, cols] codes (contiguous along cols);
+ *   axis MX_COL: q_col [batch, cols, rows] codes (the transpose, contiguous
+ *   along rows: the K-major operand of a GEMM contracting over rows).
+ *   cols % 32 == 0; rows % 32 == 0 for MX_COL; x and code buffers 16-byte
+ *   aligned.  No scale bytes are written: the scale is the amax.
+ */
+MX_API int mx_fp8_quantize(const void* x, int64_t batch, int64_t rows, int64_t cols, const float* amax, int axis,
+                           void* q_row, void* q_col, void* stream);
+
+/*
+ * mx_fp8_grouped_mm - grouped GEMM on FP8 per-tensor operands (E4M3 codes,
+ * no block scales), fp32 accumulation on the tensor cores, then
+ * C = RN_bf16(acc * (1/s_a) * (1/s_b)).
+ *   MX_GROUP_M: A [M_total, K] codes with amax_a [1]; B [E, N, K] codes with
+ *     amax_b [E] (one per expert); C [M_total, N]: rows of group e use
+ *     expert e, rows past offs[E-1] are written as zeros.
+ *   MX_GROUP_K: A [N, M_total] and B [K, M_total] (token-contiguous copies,
+ *     e.g. mx_fp8_quantize with MX_COL), amax_a [1] and amax_b [1];
+ *     C [E, N, K], C[e] = A[:, group e] . B[:, group e]^T, empty experts zero.
+ *   offs, E, pad_multiple (= 128), err_word: as for mx_grouped_mm.
+ *   M_total, N, K multiples of 128; buffers 16-byte aligned.
+ */
+MX_API int mx_fp8_grouped_mm(int mode, const void* aq, const float* amax_a, const void* bq, const float* amax_b,
+                             int64_t M_total, int64_t N, int64_t K, const int32_t* offs, int32_t E,
+                             int32_t pad_multiple, void* c, int32_t* err_word, void* stream);
+
+/*
+ * Kernel launch counters (observability; no counterpart on the pages).
+ * The torchtitan page's GPU suite holds the fused MLP to an op-count
+ * contract ("Add MXFP8 fused-MLP overrides in torchtitan", Numerics and
+ * tests: one fused activation op per direction instead of the standalone
+ * casts).  Every device operation the library enqueues is counted on the
+ * host at launch, by family:
+ */
+enum mx_kernel_family {
+  MX_KERNEL_QUANT = 0,        /* quant_kernel: one MX cast (rows and/or columns) */
+  MX_KERNEL_SWIGLU_FWD = 1,   /* swiglu_fwd_kernel: SwiGLU + MX quantization of y */
+  MX_KERNEL_SWIGLU_BWD = 2,   /* swiglu_bwd_kernel: SwiGLU backward + MX quantization of dh13 */
+  MX_KERNEL_GEMM = 3,         /* gemm_kernel: MXFP8 or bf16 GEMM (dense, M- or K-grouped) */
+  MX_KERNEL_GEMM_SWIGLU = 4,  /* gemm_kernel with the fused SwiGLU epilogue (w13 GEMM + y quantization) */
+  MX_KERNEL_DISPATCH = 5,     /* token-group padding and row gathers */
+  MX_KERNEL_MEMSET = 6,       /* cudaMemsetAsync of scale padding or dispatch maps */
+  MX_KERNEL_FAMILIES = 7
+};
+
+/*
+ * mx_launch_counts - copies the launch counters (totals since the library
+ * was loaded, all devices and threads, counted when the launch is issued)
+ * into counts[0 .. min(n, MX_KERNEL_FAMILIES)); returns MX_KERNEL_FAMILIES.
+ * counts may be NULL with n = 0 to query the number of families.  Take the
+ * difference of two readings around the calls of interest (calls from other
+ * threads in between are counted too).
+ */
+MX_API int mx_launch_counts(int64_t* counts, int n);
 
 /*
  * mx_selftest_wait_timeout - test entry of the failure detection: launches a
