@@ -40,6 +40,15 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_launch_counters_readable_without_a_gpu(L):
+    import block_scaled_mlp_gb300 as mx
+    assert L.mx_launch_counts(None, 0) == len(mx.KERNEL_FAMILIES)
+    before = mx.launch_counts()
+    p = ctypes.c_void_p(0x10000)
+    assert L.mx_quantize(None, 64, 64, 3, 1, p, p, p, p, None) == 1   # rejected on the host: nothing launched
+    assert mx.launch_counts() == before
+
+
 def test_status_strings(L):
     assert L.mx_status_string(0) == b"MX_OK"
     assert L.mx_status_string(8) == b"MX_ERR_BAD_OFFSETS"
