@@ -8,23 +8,29 @@ backward GEMMs, fused SwiGLU backward and both weight gradients) through
 the C ABI, inputs resident in HBM.  Prints ONE JSON line (rank 0).
 
 Workloads (seeded synthetic data, shapes of the pages' MXFP8 fused-MLP
-workloads): llama3_8b_ffn (default: dense, M=8192, d=4096, h=14336,
-wgrad_with_hp recipe), moe_16e, moe_64e (grouped, default recipe).
+workloads): moe_64e (default: 64 fine-grained routed experts, d=7168,
+h=2048, 16384 tokens x top-8, the largest configuration on one GPU),
+moe_16e (grouped, default recipe) and llama3_8b_ffn (dense, M=8192,
+d=4096, h=14336, wgrad_with_hp recipe; also measured, device-timed, as an
+extra key of every default run).
 
 Reported beside the device-timed value:
   e2e           the same step through the public API with host buffers:
-                x and dout copied in from pinned memory, out and dx copied
-                back, every step.
+                x and dout copied in from pinned memory, and out, dx, dw1,
+                dw3 and dw2 copied back, every step (the weights stay
+                resident on the device: `resident_bytes`).
   roofline      the dominant kernel (the MXFP8 tcgen05 GEMM): algorithmic
                 FLOPs of its launches / their CUDA-event durations, measured
                 in a per-kernel pass of the same step (the same kernels
-                launched one by one with events between them).
+                launched one by one with events between them), against the
+                measured burst bf16 peak x 2 (each launch is timed alone).
   cpu_baseline  the CPU oracle on a bounded sample of the workload.
   --impl reference runs that oracle sample as the reference arm.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -43,13 +49,23 @@ import synth  # noqa: E402
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "source": "fallback"}
 MXFP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+MXFP8_NOMINAL_TFLOPS = 4500.0   # GB300 dense MXFP8, nominal
 L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of the MXFP8 GEMM launches of
-# one step (w13 with SwiGLU, w2, dy, dx), from one ncu capture of the current
-# kernels, next to the bytes those launches must move (operands read once,
-# outputs written once); workloads without a capture report null
-MXFP8_GEMM_TRAFFIC = {"llama3_8b_ffn": 2.9386e9}
-MXFP8_GEMM_ALGO_BYTES = {"llama3_8b_ffn": 1.745e9}
+# one step, from one ncu capture, next to the bytes those launches must move
+# (operands read once, outputs written once).  `src` is the digest of the
+# GEMM sources the capture ran (gemm_source_digest()); when the sources have
+# changed since, the figure no longer describes the kernel and is reported
+# as null.
+MXFP8_GEMM_TRAFFIC = {}
+
+
+def gemm_source_digest():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "block_scaled_mlp_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -247,18 +263,18 @@ def run_gpu(args, rank, world, dev):
     launches_per_step = 12 if (w["recipe"] == "wgrad_hp" or d >= 5120) else 13
 
     # ---- end to end through the public API with host buffers: every step
-    # copies its inputs (x, dout) in from pinned host memory and its results
-    # (out, dx) back.  Double-buffered like a training input pipeline: step
-    # i+1's inputs go up on one copy stream and step i-1's results come down
-    # on another while step i computes; the timed region spans the first
-    # upload to the last download.
+    # copies its inputs (x, dout) in from pinned host memory and all of its
+    # results (out, dx, dw1, dw3, dw2) back; the weights stay resident.
+    # Double-buffered like a training input pipeline: step i+1's inputs go
+    # up on one copy stream and step i-1's results come down on another
+    # while step i computes; the timed region spans the first upload to the
+    # last download.
     host_cpus = bind_to_gpu_cpus(dev)
     hx = t["x"].cpu().pin_memory()
     hd = t["dout"].cpu().pin_memory()
-    ho = [torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    hdx = [torch.empty((M, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    res_dev = [(out,) + grads, tuple(torch.empty_like(a) for a in (out,) + grads)]
+    res_host = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in res_dev[0]]
     xin = [(torch.empty_like(t["x"]), torch.empty_like(t["dout"])) for _ in range(2)]
-    yout = [(out, grads[0]), (torch.empty_like(out), torch.empty_like(grads[0]))]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
     in_ready, in_free = [ev(), ev()], [ev(), ev()]
@@ -269,6 +285,14 @@ def run_gpu(args, rank, world, dev):
             xin[k][0].copy_(hx, non_blocking=True)
             xin[k][1].copy_(hd, non_blocking=True)
             in_ready[k].record(up)
+
+    def step_into(x, dout, r):
+        rc = L.mx_mlp_fwd(P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1), 128, recipe,
+                          P(ctx), P(scratch), P(r[0]), err.ptr(), mx._stream())
+        mx._check(rc)
+        rc = L.mx_mlp_bwd(P(ctx), P(dout), P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1),
+                          128, recipe, P(scratch), P(r[1]), P(r[2]), P(r[3]), P(r[4]), err.ptr(), mx._stream())
+        mx._check(rc)
 
     barrier()
     torch.cuda.synchronize(dev)
@@ -286,35 +310,46 @@ def run_gpu(args, rank, world, dev):
         stream.wait_event(in_ready[k])
         if i >= 2:
             stream.wait_event(out_free[k])              # step i-2's results are down
-        step(xin[k][0], xin[k][1], yout[k][0], yout[k][1])
+        step_into(xin[k][0], xin[k][1], res_dev[k])
         in_free[k].record(stream)
         out_ready[k].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(out_ready[k])
-            ho[k].copy_(yout[k][0], non_blocking=True)
-            hdx[k].copy_(yout[k][1], non_blocking=True)
+            for hdst, dsrc in zip(res_host, res_dev[k]):
+                hdst.copy_(dsrc, non_blocking=True)
             out_free[k].record(down)
     stream.wait_stream(down)
     a1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
+    err.check()
     ms_e2e = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
     e2e_value = whole_job_tflops(w["flops"], world, ms_e2e)
     h2d = (hx.numel() + hd.numel()) * 2
-    d2h = (ho[0].numel() + hdx[0].numel()) * 2
+    d2h = sum(a.numel() * a.element_size() for a in res_host)
+    resident = sum(t[k].numel() * 2 for k in ("w1", "w3", "w2"))
 
     # ---- per-kernel pass: the same kernels launched one by one with events
     kern = kernel_breakdown(mx, w, t, offs, recipe, dev, max(1, min(args.steps, 10)))
     peaks = load_peaks()
-    mx_peak = peaks["bf16_tflops_sustained"] * MXFP8_OVER_BF16
+    mx_peak = peaks["bf16_tflops"] * MXFP8_OVER_BF16
     g = kern["mx_gemm"]
     achieved = g["flops"] / (g["ms"] * 1e-3) / 1e12
-    roofline = {"kernel": "gemm_kernel<MXFP8,BN=256> (tcgen05 block-scaled)", "bound": "tensor",
+    tr = MXFP8_GEMM_TRAFFIC.get(args.workload)
+    digest = gemm_source_digest()
+    fresh = tr is not None and tr["src"] == digest
+    roofline = {"kernel": "gemm_kernel<MXFP8> (tcgen05 block-scaled)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": round(mx_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / mx_peak, 4), "traffic": MXFP8_GEMM_TRAFFIC.get(args.workload),
+                "frac": round(achieved / mx_peak, 4),
+                "frac_of_nominal": round(achieved / MXFP8_NOMINAL_TFLOPS, 4),
+                "traffic": tr["bytes"] if fresh else None,
                 "traffic_unit": "DRAM bytes per step over the step's MXFP8 GEMM launches (ncu)",
-                "algorithmic_bytes": MXFP8_GEMM_ALGO_BYTES.get(args.workload),
-                "peak_source": f"{peaks['source']} bf16 sustained x {MXFP8_OVER_BF16} (nominal fp8/bf16 ratio)"}
+                "algorithmic_bytes": tr["algo"] if tr else None,
+                "traffic_note": (tr["note"] if fresh else
+                                 ("no capture of the current GEMM sources" if tr is None or not fresh else None)),
+                "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x {MXFP8_OVER_BF16} "
+                               f"(nominal fp8/bf16 ratio; each GEMM launch is timed alone); "
+                               f"frac_of_nominal against {MXFP8_NOMINAL_TFLOPS} TFLOP/s dense MXFP8"}
     mem = kern["mem"]
     mem_gbs = mem["bytes"] / (mem["ms"] * 1e-3) / 1e9
 
@@ -342,17 +377,50 @@ def run_gpu(args, rank, world, dev):
                          "peak_source": peaks["source"]},
         "kernels_ms_per_step": {k: round(v["ms"], 4) for k, v in kern.items() if isinstance(v, dict)},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "host_cpus": host_cpus},
+                "d2h_bytes_per_step": d2h, "resident_bytes": resident,
+                "resident": "w1, w3, w2 (bf16) stay on the device; x, dout up and out, dx, dw1, dw3, dw2 down "
+                            "every step", "host_cpus": host_cpus},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     if w["kind"] == "grouped":
         res["dispatch"] = dispatch_measure(mx, w, dev, peaks["hbm_gbs"])
+        res["fp8_tensorwise_grouped"] = fp8_grouped_measure(mx, t, offs, dev, peaks, mx_peak)
+    if not args.no_extra and rank == 0 and args.workload != "llama3_8b_ffn":
+        res["llama3_8b_ffn"] = extra_workload_measure(mx, "llama3_8b_ffn", dev)
     if w["kind"] == "dense" and not args.no_quant_sweep and rank == 0:
         res["linear_lm_head"] = linear_measure(mx, dev, mx_peak)
     if not args.no_quant_sweep and rank == 0:
         res["quant_sweep"] = quant_sweep_measure(mx, dev, peaks["hbm_gbs"])
     return res
+
+
+def extra_workload_measure(mx, name, dev, steps=10, warmup=3):
+    """Device-timed fwd+bwd of another workload (inputs resident, CUDA
+    events around `steps` steps after `warmup` untimed ones)."""
+    w, inp = make_workload(name)
+    recipe = mx.RECIPE_RCEIL_WGRAD_HP if w["recipe"] == "wgrad_hp" else mx.RECIPE_RCEIL
+    t = {k: to_dev(inp[k], dev) for k in ("x", "w1", "w3", "w2", "dout")}
+    offs = None if inp["offs"] is None else torch.from_numpy(inp["offs"]).to(dev)
+
+    def step():
+        o_, c_ = mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], offs=offs, recipe=recipe)
+        mx.mlp_bwd(c_, t["dout"])
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    del t
+    torch.cuda.empty_cache()
+    return {"value": round(w["flops"] / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "steps": steps, "warmup": warmup, "recipe": w["recipe"],
+            "timing": "device (CUDA events), inputs resident, outputs allocated per step by the binding"}
 
 
 def _event_ms(fn, iters):
@@ -366,6 +434,35 @@ def _event_ms(fn, iters):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / iters
+
+
+def fp8_grouped_measure(mx, t, offs, dev, peaks, fp8_peak, iters=5):
+    """The FP8 per-tensor recipe on the workload's forward w1 GEMM shape:
+    amax of x and of each expert's w1, the cast of both (rows), and the
+    M-grouped GEMM x . w1[e]^T (E4M3 operands, no block scales).  GEMM
+    TFLOP/s against the fp8 peak; amax + cast GB/s against HBM."""
+    x, w1 = t["x"], t["w1"]
+    M, d = x.shape
+    E, h = w1.shape[0], w1.shape[1]
+    ax, aw = mx.fp8_amax(x), mx.fp8_amax(w1, batch_axes=1)
+    xq = mx.fp8_quantize(x, ax, mx.ROW)["q_row"]
+    wq = mx.fp8_quantize(w1, aw, mx.ROW)["q_row"]
+
+    def cast():
+        mx.fp8_amax(x)
+        mx.fp8_amax(w1, batch_axes=1)
+        mx.fp8_quantize(x, ax, mx.ROW)
+        mx.fp8_quantize(w1, aw, mx.ROW)
+    cast_ms = _event_ms(cast, iters)
+    gemm_ms = _event_ms(lambda: mx.fp8_grouped_mm(mx.GROUP_M, xq, ax, wq, aw, offs), iters)
+    flops = 2.0 * M * h * d                       # padded rows included: the kernel computes them
+    cast_bytes = (x.numel() + w1.numel()) * (2 + 2 + 1)   # amax read, cast read, codes written
+    tf = flops / (gemm_ms * 1e-3) / 1e12
+    gbs = cast_bytes / (cast_ms * 1e-3) / 1e9
+    return {"shape": f"[{M}, {d}] x [{E}, {h}, {d}]^T M-grouped", "gemm_ms": round(gemm_ms, 4),
+            "gemm_tflops": round(tf, 1), "gemm_frac": round(tf / fp8_peak, 4),
+            "amax_cast_ms": round(cast_ms, 4), "amax_cast_gbs": round(gbs, 1),
+            "amax_cast_frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
 def dispatch_measure(mx, w, dev, hbm_gbs, iters=10):
@@ -674,6 +771,24 @@ def run_profile_case(args):
         bs = torch.full((mx.mma_scale_bytes(K, Mt),), 120, dtype=torch.uint8, device=dev)
         fn = lambda: mx.grouped_mm(mx.GROUP_K, aq, as_, bq, bs, offs)
         work, unit = 2.0 * Mt * N * K, "FLOP"
+    elif c in ("gemm_group_m_fp8", "gemm_group_m_mx"):
+        # MoE 64E forward w13 GEMM: [M_total = 139264 padded rows, d = 7168] x
+        # [64 experts, 2h = 4096, 7168], FP8 per-tensor or MXFP8 operands
+        w = synth.WORKLOADS["moe_64e"]
+        counts = synth.dirichlet_group_counts(w["E"], w["tokens"], w["alpha"], w["seed"], w["n_empty"])
+        offs = torch.as_tensor(synth.offsets_from_counts(synth.pad_counts(counts)), device=dev)
+        Mt, N, K, E = int(offs[-1]), 2 * w["h"], w["d"], w["E"]
+        codes = lambda *sh: torch.randint(0, 126, sh, generator=g, device=dev, dtype=torch.uint8)
+        aq, bq = codes(Mt, K), codes(E, N, K)
+        if c == "gemm_group_m_fp8":
+            aa = torch.full((1,), 448.0, device=dev)
+            ab = torch.full((E,), 448.0, device=dev)
+            fn = lambda: mx.fp8_grouped_mm(mx.GROUP_M, aq, aa, bq, ab, offs)
+        else:
+            as_ = torch.full((mx.mma_scale_bytes(Mt, K),), 127, dtype=torch.uint8, device=dev)
+            bs = torch.full((E * mx.mma_scale_bytes(N, K),), 120, dtype=torch.uint8, device=dev)
+            fn = lambda: mx.grouped_mm(mx.GROUP_M, aq, as_, bq, bs, offs)
+        work, unit = 2.0 * Mt * N * K, "FLOP"
     elif c == "mlp_fwd_dense":   # default-recipe forward, M=8192, d=4096, h=8192: the fused w13 GEMM
         d, h = 4096, 8192        # (h13 + rowwise and columnwise MXFP8 y) is its first gemm_kernel launch
         x, w1, w3, w2 = rnd(M, d), rnd(h, d, std=0.02), rnd(h, d, std=0.02), rnd(d, h, std=0.02)
@@ -718,14 +833,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="llama3_8b_ffn", choices=sorted(k for k in synth.WORKLOADS if k != "tiny_dense"))
+    ap.add_argument("--workload", default="moe_64e", choices=sorted(k for k in synth.WORKLOADS if k != "tiny_dense"))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quant-sweep", action="store_true", help="skip the quantize-sweep GB/s object")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra llama3_8b_ffn measurement")
     ap.add_argument("--profile-case", default=None,
                     choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
                              "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch",
-                             "mlp_fwd_dense", "gemm_mx_cublas"])
+                             "mlp_fwd_dense", "gemm_mx_cublas", "gemm_group_m_fp8", "gemm_group_m_mx"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
