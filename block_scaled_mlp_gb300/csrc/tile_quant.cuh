@@ -34,6 +34,14 @@ MX_DEVINL uint32_t max2(uint32_t a, uint32_t b) {
       __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
+// max(|a|, |b|) per half in one instruction (the sign of the result is the
+// xor of the signs: callers use the magnitude bits only); NaN propagates as
+// the canonical NaN
+MX_DEVINL uint32_t maxabs2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 // larger magnitude of the two halves, as a 16-bit pattern (NaN -> >= 0x7F80)
 MX_DEVINL uint32_t max_halves(uint32_t m2) {
   const uint32_t lo = m2 & 0xFFFFu, hi = m2 >> 16;
@@ -41,9 +49,29 @@ MX_DEVINL uint32_t max_halves(uint32_t m2) {
   return isnan ? 0x7FC0u : max(lo, hi);
 }
 
-// Both elements of a packed bf16 pair times the power-of-two inverse scale
-// (inv2 holds it in both 32-bit halves), one packed fp32 multiply (RN, no
-// flush), then RNE saturating E4M3: the pair's two codes in the low 16 bits.
+// Both elements of a packed bf16 pair times a power-of-two inverse scale
+// given as a bf16 (exact: a power of two in the normal range), each product
+// formed by the mixed-precision FMA straight from the bf16 halves (RN_f32 of
+// the product, -0 added so that zeros keep their sign), then RNE saturating
+// E4M3: the pair's two codes in the low 16 bits.
+MX_DEVINL void scale2_pow2(uint32_t p, uint16_t inv_lo, uint16_t inv_hi, float& lo, float& hi) {
+  asm("{\n .reg .b16 pl, ph;\n mov.b32 {pl, ph}, %2;\n"
+      " fma.rn.f32.bf16 %0, pl, %3, 0f80000000;\n fma.rn.f32.bf16 %1, ph, %4, 0f80000000;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(p), "h"(inv_lo), "h"(inv_hi));
+}
+MX_DEVINL uint32_t e4m3x2_pow2(uint32_t p, uint16_t inv_bf16) {
+  float lo, hi;
+  scale2_pow2(p, inv_bf16, inv_bf16, lo, hi);
+  return cvt_e4m3x2(lo, hi);
+}
+
+// 2^-(s-127) as a bf16 bit pattern (s <= 247 for finite blocks: normal)
+MX_DEVINL uint16_t inv_scale_bf16_from_e8m0(uint32_t s) { return (uint16_t)((254u - s) << 7); }
+
+// Both elements of a packed bf16 pair times an fp32 scale (inv2 holds it in
+// both 32-bit halves), one packed fp32 multiply (RN, no flush), then RNE
+// saturating E4M3: the pair's two codes in the low 16 bits.
 MX_DEVINL uint32_t e4m3x2_scaled(uint32_t p, uint64_t inv2) {
   uint64_t v, r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(p << 16), "r"(p & 0xFFFF0000u));
@@ -63,19 +91,19 @@ MX_DEVINL uint64_t splat_f32x2(float f) {
 // pairs (element 2i in the low half of p[i]).  Writes the 32 codes as 8
 // words (element 0 in the lowest byte) and returns the scale byte.
 MX_DEVINL uint32_t quant_row32(const uint32_t (&p)[16], uint32_t (&codes)[8], uint32_t rceil = 1u) {
-  uint32_t m2 = abs2(p[0]);
+  uint32_t m2 = maxabs2(p[0], p[1]);
 #pragma unroll
-  for (int i = 1; i < 16; ++i) m2 = max2(m2, abs2(p[i]));
-  const uint32_t s = e8m0_from_amax_bits(max_halves(m2), rceil);
+  for (int i = 2; i < 16; ++i) m2 = maxabs2(m2, p[i]);
+  const uint32_t s = e8m0_from_amax_bits(max_halves(m2 & 0x7FFF7FFFu), rceil);
   if (s == 0xFF) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
     return s;
   }
-  const uint64_t inv2 = splat_f32x2(inv_scale_from_e8m0(s));
+  const uint16_t inv = inv_scale_bf16_from_e8m0(s);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    codes[i] = e4m3x2_scaled(p[2 * i], inv2) | (e4m3x2_scaled(p[2 * i + 1], inv2) << 16);
+    codes[i] = e4m3x2_pow2(p[2 * i], inv) | (e4m3x2_pow2(p[2 * i + 1], inv) << 16);
   return s;
 }
 
@@ -108,30 +136,26 @@ MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out, uint32_t
 // half).  Writes 8 words of codes per column and returns both scales.
 MX_DEVINL void quant_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_t (&cb)[8], uint32_t& sa,
                              uint32_t& sb, uint32_t rceil = 1u) {
-  uint32_t m2 = abs2(v[0]);
+  uint32_t m2 = maxabs2(v[0], v[1]);
 #pragma unroll
-  for (int i = 1; i < 32; ++i) m2 = max2(m2, abs2(v[i]));
+  for (int i = 2; i < 32; ++i) m2 = maxabs2(m2, v[i]);
+  m2 &= 0x7FFF7FFFu;
   const uint32_t la = m2 & 0xFFFFu, lb = m2 >> 16;
   sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la, rceil);
   sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb, rceil);
-  // column A in the low lanes, column B in the high lanes: one packed
-  // multiply scales an element of each column
-  uint64_t iab;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(iab) : "f"(inv_scale_from_e8m0(sa)), "f"(inv_scale_from_e8m0(sb)));
-  uint32_t lo[32], hi[32];
+  // column A in the low halves, column B in the high halves: each half is
+  // scaled by its own column's power of two straight from the bf16 bits
+  const uint16_t ia = inv_scale_bf16_from_e8m0(sa == 0xFF ? 127u : sa);
+  const uint16_t ib = inv_scale_bf16_from_e8m0(sb == 0xFF ? 127u : sb);
+  float lo[32], hi[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    uint64_t x, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(v[i] << 16), "r"(v[i] & 0xFFFF0000u));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(iab));
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo[i]), "=r"(hi[i]) : "l"(r));
-  }
+  for (int i = 0; i < 32; ++i) scale2_pow2(v[i], ia, ib, lo[i], hi[i]);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t a01 = cvt_e4m3x2(__uint_as_float(lo[4 * i]), __uint_as_float(lo[4 * i + 1]));
-    const uint32_t a23 = cvt_e4m3x2(__uint_as_float(lo[4 * i + 2]), __uint_as_float(lo[4 * i + 3]));
-    const uint32_t b01 = cvt_e4m3x2(__uint_as_float(hi[4 * i]), __uint_as_float(hi[4 * i + 1]));
-    const uint32_t b23 = cvt_e4m3x2(__uint_as_float(hi[4 * i + 2]), __uint_as_float(hi[4 * i + 3]));
+    const uint32_t a01 = cvt_e4m3x2(lo[4 * i], lo[4 * i + 1]);
+    const uint32_t a23 = cvt_e4m3x2(lo[4 * i + 2], lo[4 * i + 3]);
+    const uint32_t b01 = cvt_e4m3x2(hi[4 * i], hi[4 * i + 1]);
+    const uint32_t b23 = cvt_e4m3x2(hi[4 * i + 2], hi[4 * i + 3]);
     ca[i] = a01 | (a23 << 16);
     cb[i] = b01 | (b23 << 16);
   }
@@ -152,30 +176,24 @@ MX_DEVINL void quant_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_
 template <class Ld>
 MX_DEVINL void quant_col16x2(const Ld& ld, uint32_t (&ca)[4], uint32_t (&cb)[4], uint32_t& sa, uint32_t& sb,
                              uint32_t rceil = 1u) {
-  uint32_t m2 = abs2(ld(0));
+  uint32_t m2 = maxabs2(ld(0), ld(1));
 #pragma unroll
-  for (int i = 1; i < 16; ++i) m2 = max2(m2, abs2(ld(i)));
-  m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 16));
+  for (int i = 2; i < 16; ++i) m2 = maxabs2(m2, ld(i));
+  m2 = maxabs2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 16)) & 0x7FFF7FFFu;
   const uint32_t la = m2 & 0xFFFFu, lb = m2 >> 16;
   sa = e8m0_from_amax_bits(la > 0x7F80u ? 0x7FC0u : la, rceil);
   sb = e8m0_from_amax_bits(lb > 0x7F80u ? 0x7FC0u : lb, rceil);
-  uint64_t iab;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(iab) : "f"(inv_scale_from_e8m0(sa)), "f"(inv_scale_from_e8m0(sb)));
+  const uint16_t ia = inv_scale_bf16_from_e8m0(sa == 0xFF ? 127u : sa);
+  const uint16_t ib = inv_scale_bf16_from_e8m0(sb == 0xFF ? 127u : sb);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t lo[4], hi[4];
+    float lo[4], hi[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t w = ld(4 * i + k);
-      uint64_t x, r;
-      asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w << 16), "r"(w & 0xFFFF0000u));
-      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(iab));
-      asm("mov.b64 {%0, %1}, %2;" : "=r"(lo[k]), "=r"(hi[k]) : "l"(r));
-    }
-    const uint32_t a01 = cvt_e4m3x2(__uint_as_float(lo[0]), __uint_as_float(lo[1]));
-    const uint32_t a23 = cvt_e4m3x2(__uint_as_float(lo[2]), __uint_as_float(lo[3]));
-    const uint32_t b01 = cvt_e4m3x2(__uint_as_float(hi[0]), __uint_as_float(hi[1]));
-    const uint32_t b23 = cvt_e4m3x2(__uint_as_float(hi[2]), __uint_as_float(hi[3]));
+    for (int k = 0; k < 4; ++k) scale2_pow2(ld(4 * i + k), ia, ib, lo[k], hi[k]);
+    const uint32_t a01 = cvt_e4m3x2(lo[0], lo[1]);
+    const uint32_t a23 = cvt_e4m3x2(lo[2], lo[3]);
+    const uint32_t b01 = cvt_e4m3x2(hi[0], hi[1]);
+    const uint32_t b23 = cvt_e4m3x2(hi[2], hi[3]);
     ca[i] = sa == 0xFF ? 0x7F7F7F7Fu : (a01 | (a23 << 16));
     cb[i] = sb == 0xFF ? 0x7F7F7F7Fu : (b01 | (b23 << 16));
   }
