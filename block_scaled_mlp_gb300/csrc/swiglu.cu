@@ -188,21 +188,28 @@ __global__ void __launch_bounds__(THREADS, 2)
           const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
           uint32_t yp[4];
-          uint32_t slow = 0;
+          bool all = true;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            // a = RN_bf16(g s) certified against the bf16 midpoints (16 ulps
-            // cover the fast chain's error); y = RN_bf16(a u), exact product
+            // a = RN_bf16(g s), certified by its interval; y = RN_bf16(a u)
+            // from the exact product of the bf16 halves
             const uint64_t G = f2_from_bf16x2(gp[i]);
-            const uint64_t P = f2_mul(G, sig_fast2(G).S);
-            float g0, g1, p0, p1;
+            bool c;
+            const uint32_t A = silu2_cert(G, sig_fast2(G).S, c);
+            float g0, g1;
             f2_unpack(G, g0, g1);
-            f2_unpack(P, p0, p1);
-            slow |= (fabsf(g0) <= 64.0f && clear_of_midpoint(p0, 16) ? 0u : 1u) << (2 * i);
-            slow |= (fabsf(g1) <= 64.0f && clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
-            yp[i] = f2_to_bf16x2(f2_mul(f2_from_bf16x2(f2_to_bf16x2(P)), f2_from_bf16x2(up[i])));
+            all = all && c && fabsf(g0) <= 64.0f && fabsf(g1) <= 64.0f;
+            yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
           }
           *reinterpret_cast<uint4*>(yt + tile_chunk(rr, seg)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
+          uint32_t slow = 0;
+          if (!all) {  // rare: which elements failed
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint64_t G = f2_from_bf16x2(gp[i]);
+              slow |= silu2_bad(G, sig_fast2(G).S) << (2 * i);
+            }
+          }
           while (slow) {
             const int j = __ffs(slow) - 1;
             slow &= slow - 1;
@@ -401,44 +408,39 @@ __global__ void __launch_bounds__(THREADS, 2)
           const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
           uint32_t dgp[4], dup[4], yp[4];
-          uint32_t slow = 0;
+          bool all = true;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint64_t G = f2_from_bf16x2(gp[i]);
-            const uint64_t DY = f2_from_bf16x2(dp[i]);
             const SigFast2 f = sig_fast2(G);
-            // a = RN_bf16(g s) (certified below); du = RN_bf16(dy a), y = RN_bf16(a u)
-            const uint64_t P = f2_mul(G, f.S);
-            const uint64_t A = f2_from_bf16x2(f2_to_bf16x2(P));
-            dup[i] = f2_to_bf16x2(f2_mul(DY, A));
-            const uint64_t U = f2_from_bf16x2(up[i]);
-            if (MODE == 2) yp[i] = f2_to_bf16x2(f2_mul(A, U));
-            // dg tier 1: (dy u) * (s * (1 + g (t s))), dy u exact
-            const uint64_t DYU = f2_mul(DY, U);
+            // a = RN_bf16(g s), certified; du = RN_bf16(dy a), y = RN_bf16(a u)
+            // from exact products of bf16 halves
+            bool ca, cg;
+            const uint32_t A = silu2_cert(G, f.S, ca);
+            dup[i] = f2_to_bf16x2(f2_mul_bf16x2(dp[i], A));
+            if (MODE == 2) yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
+            // dg tier 1: (dy u) * (s * (1 + g (t s))), dy u exact, certified by
+            // its interval
+            const uint64_t DYU = f2_mul_bf16x2(dp[i], up[i]);
             const uint64_t GO = f2_mul(G, f2_mul(f.T, f.S));
             const uint64_t IN = f2_add(GO, f2_splat(1.0f));
             const uint64_t PG = f2_mul(DYU, f2_mul(f.S, IN));
-            dgp[i] = f2_to_bf16x2(PG);
-            float gv2[2], pv[2], gov[2], inv[2], dyuv[2], pgv[2];
-            f2_unpack(G, gv2[0], gv2[1]);
-            f2_unpack(P, pv[0], pv[1]);
-            f2_unpack(GO, gov[0], gov[1]);
-            f2_unpack(IN, inv[0], inv[1]);
-            f2_unpack(DYU, dyuv[0], dyuv[1]);
-            f2_unpack(PG, pgv[0], pgv[1]);
+            dgp[i] = dg2_cert(DYU, PG, dg2_width(f.S, GO, IN), cg);
+            float g0, g1;
+            f2_unpack(G, g0, g1);
+            all = all && ca && cg && fabsf(g0) <= 64.0f && fabsf(g1) <= 64.0f;
+          }
+          uint32_t slow = 0;
+          if (!all) {  // rare: which elements failed
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              // margin in fp32 ulps of dg: 24 + 26 |go| / |1 + go| (the
-              // cancellation in 1 + go amplifies the error of go)
-              const float ratio = fabsf(gov[hh]) * rcp_approx(fabsf(inv[hh]));
-              const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
-              const float adyu = fabsf(dyuv[hh]), apg = fabsf(pgv[hh]);
-              // dy u == 0 (padding rows, exact zeros, underflow): dg is the
-              // signed zero dyu * si, whose sign is certain below this margin
-              const bool ok_e = fabsf(gv2[hh]) <= 64.0f && clear_of_midpoint(pv[hh], 16) && margin < 16384.0f &&
-                                (adyu == 0.0f || (adyu >= 0x1p-100f && adyu <= 0x1p100f && apg >= 0x1p-100f)) &&
-                                clear_of_midpoint(pgv[hh], (uint32_t)margin);
-              slow |= (ok_e ? 0u : 1u) << (2 * i + hh);
+            for (int i = 0; i < 4; ++i) {
+              const uint64_t G = f2_from_bf16x2(gp[i]);
+              const SigFast2 f = sig_fast2(G);
+              const uint64_t DYU = f2_mul_bf16x2(dp[i], up[i]);
+              const uint64_t GO = f2_mul(G, f2_mul(f.T, f.S));
+              const uint64_t IN = f2_add(GO, f2_splat(1.0f));
+              const uint64_t PG = f2_mul(DYU, f2_mul(f.S, IN));
+              slow |= (silu2_bad(G, f.S) | dg2_bad(DYU, PG, dg2_width(f.S, GO, IN))) << (2 * i);
             }
           }
           *reinterpret_cast<uint4*>(ot + tile_chunk(rr, seg)) = make_uint4(dgp[0], dgp[1], dgp[2], dgp[3]);

@@ -324,6 +324,89 @@ MX_DEVINL SigFast2 sig_fast2(uint64_t G) {
   return r;
 }
 
+// ---- packed certificates (both lanes of a pair at once)
+//
+// Each returns the candidate bf16 pair and sets ok only if that rounding is
+// certain: the exact value lies in an interval around the fp32 fast value
+// that covers the fast chain's error, and both ends of the interval round to
+// the same bf16 (rounding is monotone, so everything between them does too).
+
+// RN_f32 of the products of the bf16 halves of a and b (lane 0 from the low
+// halves): exact in fp32's range (8 x 8 significant bits), computed by the
+// mixed-precision FMA with -0 as the addend so that a zero product keeps its
+// sign.
+MX_DEVINL uint64_t f2_mul_bf16x2(uint32_t a, uint32_t b) {
+  uint64_t r;
+  asm("{\n .reg .b16 al, ah, bl, bh;\n .reg .f32 lo, hi;\n"
+      " mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.bf16 lo, al, bl, 0f80000000;\n fma.rn.f32.bf16 hi, ah, bh, 0f80000000;\n"
+      " mov.b64 %0, {lo, hi};\n}"
+      : "=l"(r)
+      : "r"(a), "r"(b));
+  return r;
+}
+
+MX_DEVINL uint64_t f2_abs(uint64_t v) { return v & 0x7FFFFFFF7FFFFFFFull; }
+MX_DEVINL uint64_t f2_neg(uint64_t v) { return v ^ 0x8000000080000000ull; }
+
+// a = RN_bf16(g s): p = g s is within 9 fp32 ulps of g * sigma_c (sigma_c the
+// correctly rounded sigma); the interval [p(1 - 2^-19), p(1 + 2^-19)] is at
+// least 15.5 ulps wide on each side.
+MX_DEVINL uint32_t silu2_cert(uint64_t G, uint64_t S, bool& ok) {
+  const uint64_t P = f2_mul(G, S);
+  const uint32_t lo = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F7FFFE0u))));  // 1 - 2^-19
+  const uint32_t hi = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F800010u))));  // 1 + 2^-19
+  ok = lo == hi;
+  return lo;
+}
+
+// Margin constants of dg, in units of 2^-24: the fast value PG = dyu (s (1 +
+// g t s)) is within |dyu| s (DG_C0 |1 + go| + DG_C1 |go|) 2^-24 of the exact
+// dyu F(g) (go = g t s; the cancellation in 1 + go amplifies go's error),
+// including the rounding of PG and of the interval ends.
+constexpr float DG_C0 = 24.0f * 0x1p-24f;
+constexpr float DG_C1 = 26.0f * 0x1p-24f;
+
+// the half-width factor W = s (C0 |in| + C1 |go|) of the dg interval
+MX_DEVINL uint64_t dg2_width(uint64_t S, uint64_t GO, uint64_t IN) {
+  return f2_mul(S, f2_fma(f2_abs(GO), f2_splat(DG_C1), f2_mul(f2_abs(IN), f2_splat(DG_C0))));
+}
+
+// dg = RN_bf16(dyu F): the interval PG -+ dyu W (signed dyu: the ends swap,
+// the interval is the same).  A |PG| below 2^-100 (but not zero) is not
+// certified: there the fp32 roundings are not relative.
+MX_DEVINL uint32_t dg2_cert(uint64_t DYU, uint64_t PG, uint64_t W, bool& ok) {
+  const uint32_t lo = f2_to_bf16x2(f2_fma(DYU, f2_neg(W), PG));
+  const uint32_t hi = f2_to_bf16x2(f2_fma(DYU, W, PG));
+  float p0, p1;
+  f2_unpack(PG, p0, p1);
+  ok = (lo == hi) && (fabsf(p0) >= 0x1p-100f || p0 == 0.0f) && (fabsf(p1) >= 0x1p-100f || p1 == 0.0f);
+  return lo;
+}
+
+// Lanes (bit 0: low, bit 1: high) whose a = RN_bf16(g s) is not certified
+// (the per-element view of silu2_cert, for the rare groups that fail).
+MX_DEVINL uint32_t silu2_bad(uint64_t G, uint64_t S) {
+  const uint64_t P = f2_mul(G, S);
+  const uint32_t lo = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F7FFFE0u))));
+  const uint32_t hi = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F800010u))));
+  float g0, g1;
+  f2_unpack(G, g0, g1);
+  const uint32_t d = lo ^ hi;
+  return ((d & 0xFFFFu) || !(fabsf(g0) <= 64.0f) ? 1u : 0u) | ((d >> 16) || !(fabsf(g1) <= 64.0f) ? 2u : 0u);
+}
+
+// The same for dg (dg2_cert's interval and magnitude test, per lane).
+MX_DEVINL uint32_t dg2_bad(uint64_t DYU, uint64_t PG, uint64_t W) {
+  const uint32_t lo = f2_to_bf16x2(f2_fma(DYU, f2_neg(W), PG));
+  const uint32_t hi = f2_to_bf16x2(f2_fma(DYU, W, PG));
+  float p0, p1;
+  f2_unpack(PG, p0, p1);
+  const uint32_t d = lo ^ hi;
+  const bool t0 = fabsf(p0) >= 0x1p-100f || p0 == 0.0f, t1 = fabsf(p1) >= 0x1p-100f || p1 == 0.0f;
+  return ((d & 0xFFFFu) || !t0 ? 1u : 0u) | ((d >> 16) || !t1 ? 2u : 0u);
+}
+
 }  // namespace
 }  // namespace swiglu_math
 }  // namespace mx

@@ -1,21 +1,24 @@
 // Exhaustive check, over every bf16 g with |g| <= 64, of the packed fast path
-// the fused SwiGLU kernels use (swiglu_math.cuh):
+// and the certificates the fused SwiGLU kernels use (swiglu_math.cuh):
 //   * t = e^-g (own exp on ex2.approx) against fp64, in ulps;
 //   * s = rcp.approx(1 + t) against fp64 sigma;
-//   * silu: every result certified at 16 ulps equals
+//   * silu: every a certified by silu2_cert equals
 //     RN_bf16(RN_f32(g * RN_f32(sigma)));
-//   * dg: the g-dependent factor s (1 + g t s) against
-//     F = sigma (1 + g (1 - sigma)); its error (plus the final rounding of
-//     dy u times it) must stay below the margin 24 + 26 |go| / |1 + go| the
-//     kernels certify with.  dy u is exact in fp32, so this covers every
-//     (dy, u) pair.
-// Exit status 2 if a certified result is wrong or a margin is too small.
+//   * dg: the fast factor si = s (1 + g t s) against F = sigma (1 + g (1 -
+//     sigma)).  The kernels accept PG = RN(dyu si) when both ends of
+//     PG -+ dyu W round to the same bf16, W = dg2_width(s, go, 1 + go); that
+//     is sound when |si - F| plus the roundings of PG and of the interval end
+//     (each at most 2^-24 |si| per unit of dyu) stays below W.  dyu is exact
+//     in fp32, so this covers every (dy, u) pair.  The sign of si must be the
+//     sign of F (it decides the sign of a zero dg).
+// Exit status 2 if a certified result is wrong, a margin is too small or a
+// sign is wrong.
 #include <cstdio>
 #include <cstring>
 #include "swiglu_math.cuh"
 using namespace mx;
 using namespace mx::swiglu_math;
-struct Out { unsigned t_err, s_err, a_bad, a_fast, dg_ratio, dg_bad, dg_fast; };
+struct Out { unsigned t_err, s_err, a_bad, a_fast, dg_ratio, dg_bad, dg_fast, sign_bad; };
 __device__ void amaxf(unsigned* p, float v) { atomicMax(p, __float_as_uint(fmaxf(v, 0.f))); }
 __global__ void k(Out* o) {
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -31,28 +34,27 @@ __global__ void k(Out* o) {
   const double sig = 1.0 / (1.0 + et), oms_e = et / (1.0 + et);
   amaxf(&o->s_err, (float)(fabs(s - sig) / sig * 0x1p23));
   // silu: certified results must equal RN_bf16(RN_f32(g * RN_f32(sigma)))
-  const float p = __fmul_rn(g, s);
-  if (clear_of_midpoint(p, 16)) {
+  bool ok;
+  const uint32_t A = silu2_cert(G, f.S, ok);
+  if (ok) {
     atomicAdd(&o->a_fast, 1u);
     const float q = __fmul_rn(g, __double2float_rn(sig));
-    if (f32_to_bf16_bits(p) != f32_to_bf16_bits(q)) atomicAdd(&o->a_bad, 1u);
+    if ((A & 0xFFFFu) != f32_to_bf16_bits(q)) atomicAdd(&o->a_bad, 1u);
   }
   // dg: si = s (1 + g (t s)) against F = sigma (1 + g (1 - sigma))
   const uint64_t GO = f2_mul(G, f2_mul(f.T, f.S));
   const uint64_t IN = f2_add(GO, f2_splat(1.0f));
   const uint64_t SI = f2_mul(f.S, IN);
-  float go, in, si, x0, x1, x2; f2_unpack(GO, go, x0); f2_unpack(IN, in, x1); f2_unpack(SI, si, x2);
-  const float ratio = fabsf(go) * rcp_approx(fabsf(in));
-  const float margin = __fmaf_rn(26.0f, ratio, 24.0f);
-  if (margin < 16384.0f) {
-    atomicAdd(&o->dg_fast, 1u);
-    const double F = sig * (1.0 + gd * oms_e);
-    // error of p = RN(dyu si) against dyu F in ulps of p, plus the rounding of p
-    const double need = fabs((double)si - F) / fabs((double)si) * 0x1p24 + 1.0;
-    const float m = floorf(margin);  // the kernel compares against the truncated margin
-    amaxf(&o->dg_ratio, (float)(need / m));
-    if (need >= m) atomicAdd(&o->dg_bad, 1u);
-  }
+  const uint64_t W2 = dg2_width(f.S, GO, IN);
+  float si, w, x0, x1;
+  f2_unpack(SI, si, x0);
+  f2_unpack(W2, w, x1);
+  atomicAdd(&o->dg_fast, 1u);
+  const double F = sig * (1.0 + gd * oms_e);
+  const double need = fabs((double)si - F) + 0x1p-23 * 1.01 * fabs((double)si);
+  amaxf(&o->dg_ratio, (float)(need / (double)w));
+  if (!(need < (double)w)) atomicAdd(&o->dg_bad, 1u);
+  if ((si < 0.0f) != (F < 0.0) || si == 0.0f) atomicAdd(&o->sign_bad, 1u);
 }
 int main() {
   Out* d; cudaMalloc(&d, sizeof(Out)); cudaMemset(d, 0, sizeof(Out));
@@ -62,6 +64,7 @@ int main() {
   float te, se, dr; memcpy(&te, &h.t_err, 4); memcpy(&se, &h.s_err, 4); memcpy(&dr, &h.dg_ratio, 4);
   printf("t max ulp %.3f; s max rel err %.3f x 2^-23\n", te, se);
   printf("silu: %u certified, %u wrong\n", h.a_fast, h.a_bad);
-  printf("dg: %u g on the fast path, max needed/margin %.3f, %u with needed >= margin\n", h.dg_fast, dr, h.dg_bad);
-  return (h.a_bad || h.dg_bad) ? 2 : 0;
+  printf("dg: %u g on the fast path, max needed/margin %.3f, %u with needed >= margin, %u sign errors\n",
+         h.dg_fast, dr, h.dg_bad, h.sign_bad);
+  return (h.a_bad || h.dg_bad || h.sign_bad) ? 2 : 0;
 }
