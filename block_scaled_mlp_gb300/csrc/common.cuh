@@ -192,6 +192,15 @@ MX_DEVINL void tma_load_4d_pair(void* dst, const CUtensorMap* m, int32_t x, int3
       : "memory");
 }
 
+MX_DEVINL void tma_load_5d_pair(void* dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z, int32_t w,
+                                int32_t v, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 MX_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
