@@ -392,7 +392,7 @@ def run_gpu(args, rank, world, dev):
         res["linear_lm_head"] = linear_measure(mx, dev, mx_peak)
     if not args.no_quant_sweep and rank == 0:
         res["quant_sweep"] = quant_sweep_measure(mx, dev, peaks["hbm_gbs"])
-    return res
+    return res, w, inp
 
 
 def extra_workload_measure(mx, name, dev, steps=10, warmup=3):
@@ -638,9 +638,11 @@ def kernel_breakdown(mx, w, t, offs, recipe, dev, steps):
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_sample(w, inp, tokens, hidden):
+def oracle_sample(w, inp, tokens, hidden, keep=False):
     """A bounded sample of the workload for the CPU oracle: the first
-    `tokens` routed rows and the first `hidden` hidden units (all of d)."""
+    `tokens` routed rows and the first `hidden` hidden units (all of d).
+    With keep=True also returns the sample's inputs and the oracle's
+    results."""
     from oracle import mx_oracle as o
     x = inp["x"][:tokens]
     dout = inp["dout"][:tokens]
@@ -659,9 +661,11 @@ def oracle_sample(w, inp, tokens, hidden):
     rec = "wgrad_hp" if w["recipe"] == "wgrad_hp" else "rceil"
     t0 = time.perf_counter()
     f = o.mlp_fwd(x, w1, w3, w2, offs=offs, recipe=rec)
-    o.mlp_bwd(x, w1, w3, w2, dout, offs=offs, recipe=rec, fwd=f)
+    b = o.mlp_bwd(x, w1, w3, w2, dout, offs=offs, recipe=rec, fwd=f)
     dt = time.perf_counter() - t0
     flops = 18.0 * tokens * w["d"] * hidden
+    if keep:
+        return flops, dt, dict(x=x, w1=w1, w3=w3, w2=w2, dout=dout, fwd=f, bwd=b)
     return flops, dt
 
 
@@ -705,13 +709,56 @@ def run_reference(args):
     }
 
 
-def cpu_baseline(args):
-    w, inp = make_workload(args.workload)
+def cpu_baseline(args, w, inp, dev=None):
+    """The CPU oracle on a bounded sample of the workload, timed; with a
+    device, also the numerics of the GPU path on the same sample (SQNR
+    against the oracle's per-GEMM MXFP8 chain and against the unquantized
+    fp64 MLP, as the fused-MLP page's test suite tracks them)."""
     tokens, hidden = (256, 1024) if w["kind"] == "dense" else (256, 512)
-    fl, dt = oracle_sample(w, inp, tokens, hidden)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-            "seconds": round(dt, 2),
-            "sample": f"{tokens} tokens x {hidden} hidden units (all d={w['d']}) of {args.workload}, fwd+bwd"}
+    fl, dt, smp = oracle_sample(w, inp, tokens, hidden, keep=True)
+    res = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+           "seconds": round(dt, 2),
+           "sample": f"{tokens} tokens x {hidden} hidden units (all d={w['d']}) of {args.workload}, fwd+bwd"}
+    if dev is not None:
+        res["numerics"] = sample_numerics(w, smp, dev)
+    return res
+
+
+def sample_numerics(w, smp, dev):
+    """SQNR (dB) of out, dx, dw1, dw3, dw2 from the GPU path on the oracle
+    sample, against the oracle's per-GEMM MXFP8 chain (fp64 before each
+    bf16 rounding) and against the textbook fp64 SwiGLU MLP (no
+    quantization), plus the normwise error against the chain."""
+    import block_scaled_mlp_gb300 as mx
+    from oracle import mx_oracle as o
+    recipe = mx.RECIPE_RCEIL_WGRAD_HP if w["recipe"] == "wgrad_hp" else mx.RECIPE_RCEIL
+    t = {k: to_dev(smp[k], dev) for k in ("x", "w1", "w3", "w2", "dout")}
+    out, ctx = mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], recipe=recipe)
+    dx, dw1, dw3, dw2 = mx.mlp_bwd(ctx, t["dout"])
+    torch.cuda.synchronize(dev)
+    f, b = smp["fwd"], smp["bwd"]
+    h = smp["w1"].shape[0]
+    X, W1, W3, W2, D = (o.bf16_to_f64(smp[k]) for k in ("x", "w1", "w3", "w2", "dout"))
+    g, u = X @ W1.T, X @ W3.T
+    sg = 1.0 / (1.0 + np.exp(-g))
+    y = g * sg * u
+    dy = D @ W2
+    dg, du = dy * u * sg * (1.0 + g * (1.0 - sg)), dy * g * sg
+    plain = {"out": y @ W2.T, "dx": dg @ W1 + du @ W3, "dw1": dg.T @ X, "dw3": du.T @ X, "dw2": D.T @ y}
+    chain = {"out": f["out_f"], "dx": b["dx_f"], "dw1": b["dw13_f"][:h], "dw3": b["dw13_f"][h:],
+             "dw2": b["dw2_f"]}
+    got = {"out": out, "dx": dx, "dw1": dw1, "dw3": dw3, "dw2": dw2}
+
+    def sqnr(a, ref):
+        den = float(np.sum((a - ref) ** 2))
+        return None if den == 0.0 else round(10.0 * np.log10(float(np.sum(ref ** 2)) / den), 2)
+    r = {"sqnr_vs_mxfp8_chain_db": {}, "sqnr_vs_unquantized_db": {}, "normwise_vs_chain": {}}
+    for k, v in got.items():
+        a = o.bf16_to_f64(v.cpu().view(torch.int16).numpy().view(np.uint16))
+        r["sqnr_vs_mxfp8_chain_db"][k] = sqnr(a, chain[k])
+        r["sqnr_vs_unquantized_db"][k] = sqnr(a, plain[k])
+        r["normwise_vs_chain"][k] = float(f"{o.normwise_rel_err(a, chain[k]):.3e}")
+    return r
 
 
 # ------------------------------------------------------------------ profiling cases
@@ -789,6 +836,33 @@ def run_profile_case(args):
             bs = torch.full((E * mx.mma_scale_bytes(N, K),), 120, dtype=torch.uint8, device=dev)
             fn = lambda: mx.grouped_mm(mx.GROUP_M, aq, as_, bq, bs, offs)
         work, unit = 2.0 * Mt * N * K, "FLOP"
+    elif c == "moe64_gemms":
+        # the six MXFP8 GEMMs of a MoE 64E step, one after another (random
+        # codes, uniform scales), each timed on its own: prints one line each
+        w = synth.WORKLOADS["moe_64e"]
+        counts = synth.dirichlet_group_counts(w["E"], w["tokens"], w["alpha"], w["seed"], w["n_empty"])
+        offs = torch.as_tensor(synth.offsets_from_counts(synth.pad_counts(counts)), device=dev)
+        Mt, d, h, E = int(offs[-1]), w["d"], w["h"], w["E"]
+        codes = lambda *sh: torch.randint(0, 126, sh, generator=g, device=dev, dtype=torch.uint8)
+        sc = lambda rows, cols, v: torch.full((mx.mma_scale_bytes(rows, cols),), v, dtype=torch.uint8, device=dev)
+        shapes = [("w13", "M", 2 * h, d), ("w2", "M", d, h), ("dy", "M", h, d), ("dx", "M", d, 2 * h),
+                  ("dw2", "K", d, h), ("dw13", "K", 2 * h, d)]
+        for name, mode, N, K in shapes:
+            if mode == "M":
+                aq, bq = codes(Mt, K), codes(E, N, K)
+                as_, bs = sc(Mt, K, 127), torch.cat([sc(N, K, 120)] * E)
+                fn = lambda: mx.grouped_mm(mx.GROUP_M, aq, as_, bq, bs, offs)
+            else:
+                aq, bq = codes(N, Mt), codes(K, Mt)
+                as_, bs = sc(N, Mt, 127), sc(K, Mt, 120)
+                fn = lambda: mx.grouped_mm(mx.GROUP_K, aq, as_, bq, bs, offs)
+            fn()
+            torch.cuda.synchronize()
+            ms = _event_ms(fn, args.iters)
+            print(json.dumps({"case": f"moe64_{name}", "ms": round(ms, 4),
+                              "rate": round(2.0 * Mt * N * K / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s"}))
+            del aq, bq, as_, bs
+        return
     elif c == "mlp_fwd_dense":   # default-recipe forward, M=8192, d=4096, h=8192: the fused w13 GEMM
         d, h = 4096, 8192        # (h13 + rowwise and columnwise MXFP8 y) is its first gemm_kernel launch
         x, w1, w3, w2 = rnd(M, d), rnd(h, d, std=0.02), rnd(h, d, std=0.02), rnd(d, h, std=0.02)
@@ -841,7 +915,7 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
                              "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch",
-                             "mlp_fwd_dense", "gemm_mx_cublas", "gemm_group_m_fp8", "gemm_group_m_mx"])
+                             "mlp_fwd_dense", "gemm_mx_cublas", "gemm_group_m_fp8", "gemm_group_m_mx", "moe64_gemms"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
@@ -862,9 +936,9 @@ def main():
     torch.cuda.set_device(dev)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
-    res = run_gpu(args, rank, world, dev)
+    res, w, inp = run_gpu(args, rank, world, dev)
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(args)
+        res["cpu_baseline"] = cpu_baseline(args, w, inp, dev)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
