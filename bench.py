@@ -867,6 +867,12 @@ def run_profile_case(args):
                               "rate": round(2.0 * Mt * N * K / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s"}))
             del aq, bq, as_, bs
         return
+    elif c == "moe64_fwd":   # MoE 64E forward through mx_mlp_fwd (default recipe)
+        w, inp = make_workload("moe_64e")
+        t = {k: to_dev(inp[k], dev) for k in ("x", "w1", "w3", "w2")}
+        offs = torch.from_numpy(inp["offs"]).to(dev)
+        fn = lambda: mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], offs=offs, recipe=mx.RECIPE_RCEIL)
+        work, unit = w["flops"] / 3.0, "FLOP"
     elif c == "mlp_fwd_dense":   # default-recipe forward, M=8192, d=4096, h=8192: the fused w13 GEMM
         d, h = 4096, 8192        # (h13 + rowwise and columnwise MXFP8 y) is its first gemm_kernel launch
         x, w1, w3, w2 = rnd(M, d), rnd(h, d, std=0.02), rnd(h, d, std=0.02), rnd(d, h, std=0.02)
@@ -919,7 +925,7 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["quant", "quant_row", "quant_col", "swiglu_fwd", "swiglu_fwd_row", "swiglu_bwd",
                              "swiglu_bwd_hp", "gemm_mx", "gemm_bf16", "gemm_group_k", "dispatch",
-                             "mlp_fwd_dense", "gemm_mx_cublas", "gemm_group_m_fp8", "gemm_group_m_mx", "moe64_gemms"])
+                             "mlp_fwd_dense", "gemm_mx_cublas", "gemm_group_m_fp8", "gemm_group_m_mx", "moe64_gemms", "moe64_fwd"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

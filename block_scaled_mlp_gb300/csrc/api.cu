@@ -568,7 +568,10 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
   // outlasts a main loop of d < kFuseDualMinK (measured at d = 4096: 511 us
   // fused against 325 + 126 us for the GEMM and the SwiGLU kernel), so
   // shorter contractions run the two kernels instead (bit-identical).
-  constexpr int64_t kFuseDualMinK = 5120;
+#ifndef MX_FUSE_DUAL_MIN_K
+#define MX_FUSE_DUAL_MIN_K 5120
+#endif
+  constexpr int64_t kFuseDualMinK = MX_FUSE_DUAL_MIN_K;
   const bool fuse = hp || d >= kFuseDualMinK;
   {
     GemmLaunch g{};
