@@ -443,43 +443,28 @@ MX_DEVINL uint32_t f32_to_bf16_bits(float f) {
 }
 
 // ---------------------------------------------------------------- packed fp32 pairs
-// Two fp32 lanes in one 64-bit register (lane 0 in the low word); the
-// f32x2 arithmetic rounds each lane to nearest even, without flushing.
+// Two fp32 lanes as a float2 (lane 0 = .x).  The packed builtins compile to
+// the paired fp32 instructions (each lane rounded to nearest even, no
+// flush), and the compiler pairs the registers itself.
 
-MX_DEVINL uint64_t f2_pack(float lo, float hi) {
-  uint64_t v;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
-  return v;
+using f2 = float2;
+MX_DEVINL f2 f2_pack(float lo, float hi) { return make_float2(lo, hi); }
+MX_DEVINL void f2_unpack(f2 v, float& lo, float& hi) {
+  lo = v.x;
+  hi = v.y;
 }
-MX_DEVINL void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-MX_DEVINL uint64_t f2_splat(float f) { return f2_pack(f, f); }
+MX_DEVINL f2 f2_splat(float f) { return make_float2(f, f); }
 // the two bf16 halves of p as fp32 (exact)
-MX_DEVINL uint64_t f2_from_bf16x2(uint32_t p) {
-  return f2_pack(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+MX_DEVINL f2 f2_from_bf16x2(uint32_t p) {
+  return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
 }
-MX_DEVINL uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-MX_DEVINL uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-MX_DEVINL uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
+MX_DEVINL f2 f2_mul(f2 a, f2 b) { return __fmul2_rn(a, b); }
+MX_DEVINL f2 f2_add(f2 a, f2 b) { return __fadd2_rn(a, b); }
+MX_DEVINL f2 f2_fma(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
 // RN to a packed bf16 pair (lane 0 in the low half)
-MX_DEVINL uint32_t f2_to_bf16x2(uint64_t v) {
-  float lo, hi;
-  f2_unpack(v, lo, hi);
+MX_DEVINL uint32_t f2_to_bf16x2(f2 v) {
   uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(v.y), "f"(v.x));
   return r;
 }
 

@@ -714,8 +714,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           uint32_t slow = 0;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const uint64_t G = f2_from_bf16x2(gw[b][i]);
-            const uint64_t P = f2_mul(G, swiglu_math::sig_fast2(G).S);
+            const f2 G = f2_from_bf16x2(gw[b][i]);
+            const f2 P = f2_mul(G, swiglu_math::sig_fast2(G).S);
             float g0, g1, p0, p1;
             f2_unpack(G, g0, g1);
             f2_unpack(P, p0, p1);

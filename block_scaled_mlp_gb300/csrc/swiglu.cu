@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           for (int i = 0; i < 4; ++i) {
             // a = RN_bf16(g s), certified by its interval; y = RN_bf16(a u)
             // from the exact product of the bf16 halves
-            const uint64_t G = f2_from_bf16x2(gp[i]);
+            const f2 G = f2_from_bf16x2(gp[i]);
             bool c;
             const uint32_t A = silu2_cert(G, sig_fast2(G).S, c);
             float g0, g1;
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           if (!all) {  // rare: which elements failed
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint64_t G = f2_from_bf16x2(gp[i]);
+              const f2 G = f2_from_bf16x2(gp[i]);
               slow |= silu2_bad(G, sig_fast2(G).S) << (2 * i);
             }
           }
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           bool all = true;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint64_t G = f2_from_bf16x2(gp[i]);
+            const f2 G = f2_from_bf16x2(gp[i]);
             const SigFast2 f = sig_fast2(G);
             // a = RN_bf16(g s), certified; du = RN_bf16(dy a), y = RN_bf16(a u)
             // from exact products of bf16 halves
@@ -421,10 +421,10 @@ __global__ void __launch_bounds__(THREADS, 2)
             if (MODE == 2) yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
             // dg tier 1: (dy u) * (s * (1 + g (t s))), dy u exact, certified by
             // its interval
-            const uint64_t DYU = f2_mul_bf16x2(dp[i], up[i]);
-            const uint64_t GO = f2_mul(G, f2_mul(f.T, f.S));
-            const uint64_t IN = f2_add(GO, f2_splat(1.0f));
-            const uint64_t PG = f2_mul(DYU, f2_mul(f.S, IN));
+            const f2 DYU = f2_mul_bf16x2(dp[i], up[i]);
+            const f2 GO = f2_mul(G, f2_mul(f.T, f.S));
+            const f2 IN = f2_add(GO, f2_splat(1.0f));
+            const f2 PG = f2_mul(DYU, f2_mul(f.S, IN));
             dgp[i] = dg2_cert(DYU, PG, dg2_width(f.S, GO, IN), cg);
             float g0, g1;
             f2_unpack(G, g0, g1);
@@ -434,12 +434,12 @@ __global__ void __launch_bounds__(THREADS, 2)
           if (!all) {  // rare: which elements failed
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint64_t G = f2_from_bf16x2(gp[i]);
+              const f2 G = f2_from_bf16x2(gp[i]);
               const SigFast2 f = sig_fast2(G);
-              const uint64_t DYU = f2_mul_bf16x2(dp[i], up[i]);
-              const uint64_t GO = f2_mul(G, f2_mul(f.T, f.S));
-              const uint64_t IN = f2_add(GO, f2_splat(1.0f));
-              const uint64_t PG = f2_mul(DYU, f2_mul(f.S, IN));
+              const f2 DYU = f2_mul_bf16x2(dp[i], up[i]);
+              const f2 GO = f2_mul(G, f2_mul(f.T, f.S));
+              const f2 IN = f2_add(GO, f2_splat(1.0f));
+              const f2 PG = f2_mul(DYU, f2_mul(f.S, IN));
               slow |= (silu2_bad(G, f.S) | dg2_bad(DYU, PG, dg2_width(f.S, GO, IN))) << (2 * i);
             }
           }

@@ -296,26 +296,26 @@ MX_DEVINL float ex2_approx(float y) {
 // first-order correction leaves a relative error below 2^-36, so the result
 // is within ex2's error plus one rounding (at most 2.6 ulp, checked on
 // every bf16 g).
-MX_DEVINL uint64_t f2_exp_neg(uint64_t G) {
-  const uint64_t L = f2_splat(__uint_as_float(0x3FB8AA3Bu));     // RN_f32(log2 e)
-  const uint64_t NL = f2_splat(__uint_as_float(0xBFB8AA3Bu));
-  const uint64_t LC = f2_splat(__uint_as_float(0x32A57060u));    // RN_f32(log2 e - L)
-  const uint64_t NLN2 = f2_splat(__uint_as_float(0xBF317218u));  // -RN_f32(ln 2)
-  const uint64_t Y = f2_mul(G, NL);
-  const uint64_t R = f2_fma(G, L, Y);
-  const uint64_t C = f2_fma(G, LC, R);
-  const uint64_t K = f2_mul(C, NLN2);
+MX_DEVINL f2 f2_exp_neg(f2 G) {
+  const f2 L = f2_splat(__uint_as_float(0x3FB8AA3Bu));     // RN_f32(log2 e)
+  const f2 NL = f2_splat(__uint_as_float(0xBFB8AA3Bu));
+  const f2 LC = f2_splat(__uint_as_float(0x32A57060u));    // RN_f32(log2 e - L)
+  const f2 NLN2 = f2_splat(__uint_as_float(0xBF317218u));  // -RN_f32(ln 2)
+  const f2 Y = f2_mul(G, NL);
+  const f2 R = f2_fma(G, L, Y);
+  const f2 C = f2_fma(G, LC, R);
+  const f2 K = f2_mul(C, NLN2);
   float y0, y1;
   f2_unpack(Y, y0, y1);
-  const uint64_t E = f2_pack(ex2_approx(y0), ex2_approx(y1));
+  const f2 E = f2_pack(ex2_approx(y0), ex2_approx(y1));
   return f2_fma(E, K, E);
 }
 
 // t = e^-g and s = rcp.approx(1 + t) (at most 0.98 ulp) on both lanes.
 struct SigFast2 {
-  uint64_t T, S;
+  f2 T, S;
 };
-MX_DEVINL SigFast2 sig_fast2(uint64_t G) {
+MX_DEVINL SigFast2 sig_fast2(f2 G) {
   SigFast2 r;
   r.T = f2_exp_neg(G);
   float d0, d1;
@@ -335,25 +335,24 @@ MX_DEVINL SigFast2 sig_fast2(uint64_t G) {
 // halves): exact in fp32's range (8 x 8 significant bits), computed by the
 // mixed-precision FMA with -0 as the addend so that a zero product keeps its
 // sign.
-MX_DEVINL uint64_t f2_mul_bf16x2(uint32_t a, uint32_t b) {
-  uint64_t r;
-  asm("{\n .reg .b16 al, ah, bl, bh;\n .reg .f32 lo, hi;\n"
-      " mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
-      " fma.rn.f32.bf16 lo, al, bl, 0f80000000;\n fma.rn.f32.bf16 hi, ah, bh, 0f80000000;\n"
-      " mov.b64 %0, {lo, hi};\n}"
-      : "=l"(r)
+MX_DEVINL f2 f2_mul_bf16x2(uint32_t a, uint32_t b) {
+  float lo, hi;
+  asm("{\n .reg .b16 al, ah, bl, bh;\n"
+      " mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+      " fma.rn.f32.bf16 %0, al, bl, 0f80000000;\n fma.rn.f32.bf16 %1, ah, bh, 0f80000000;\n}"
+      : "=f"(lo), "=f"(hi)
       : "r"(a), "r"(b));
-  return r;
+  return make_float2(lo, hi);
 }
 
-MX_DEVINL uint64_t f2_abs(uint64_t v) { return v & 0x7FFFFFFF7FFFFFFFull; }
-MX_DEVINL uint64_t f2_neg(uint64_t v) { return v ^ 0x8000000080000000ull; }
+MX_DEVINL f2 f2_abs(f2 v) { return make_float2(fabsf(v.x), fabsf(v.y)); }
+MX_DEVINL f2 f2_neg(f2 v) { return make_float2(-v.x, -v.y); }
 
 // a = RN_bf16(g s): p = g s is within 9 fp32 ulps of g * sigma_c (sigma_c the
 // correctly rounded sigma); the interval [p(1 - 2^-19), p(1 + 2^-19)] is at
 // least 15.5 ulps wide on each side.
-MX_DEVINL uint32_t silu2_cert(uint64_t G, uint64_t S, bool& ok) {
-  const uint64_t P = f2_mul(G, S);
+MX_DEVINL uint32_t silu2_cert(f2 G, f2 S, bool& ok) {
+  const f2 P = f2_mul(G, S);
   const uint32_t lo = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F7FFFE0u))));  // 1 - 2^-19
   const uint32_t hi = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F800010u))));  // 1 + 2^-19
   ok = lo == hi;
@@ -368,14 +367,14 @@ constexpr float DG_C0 = 24.0f * 0x1p-24f;
 constexpr float DG_C1 = 26.0f * 0x1p-24f;
 
 // the half-width factor W = s (C0 |in| + C1 |go|) of the dg interval
-MX_DEVINL uint64_t dg2_width(uint64_t S, uint64_t GO, uint64_t IN) {
+MX_DEVINL f2 dg2_width(f2 S, f2 GO, f2 IN) {
   return f2_mul(S, f2_fma(f2_abs(GO), f2_splat(DG_C1), f2_mul(f2_abs(IN), f2_splat(DG_C0))));
 }
 
 // dg = RN_bf16(dyu F): the interval PG -+ dyu W (signed dyu: the ends swap,
 // the interval is the same).  A |PG| below 2^-100 (but not zero) is not
 // certified: there the fp32 roundings are not relative.
-MX_DEVINL uint32_t dg2_cert(uint64_t DYU, uint64_t PG, uint64_t W, bool& ok) {
+MX_DEVINL uint32_t dg2_cert(f2 DYU, f2 PG, f2 W, bool& ok) {
   const uint32_t lo = f2_to_bf16x2(f2_fma(DYU, f2_neg(W), PG));
   const uint32_t hi = f2_to_bf16x2(f2_fma(DYU, W, PG));
   float p0, p1;
@@ -386,8 +385,8 @@ MX_DEVINL uint32_t dg2_cert(uint64_t DYU, uint64_t PG, uint64_t W, bool& ok) {
 
 // Lanes (bit 0: low, bit 1: high) whose a = RN_bf16(g s) is not certified
 // (the per-element view of silu2_cert, for the rare groups that fail).
-MX_DEVINL uint32_t silu2_bad(uint64_t G, uint64_t S) {
-  const uint64_t P = f2_mul(G, S);
+MX_DEVINL uint32_t silu2_bad(f2 G, f2 S) {
+  const f2 P = f2_mul(G, S);
   const uint32_t lo = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F7FFFE0u))));
   const uint32_t hi = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F800010u))));
   float g0, g1;
@@ -397,7 +396,7 @@ MX_DEVINL uint32_t silu2_bad(uint64_t G, uint64_t S) {
 }
 
 // The same for dg (dg2_cert's interval and magnitude test, per lane).
-MX_DEVINL uint32_t dg2_bad(uint64_t DYU, uint64_t PG, uint64_t W) {
+MX_DEVINL uint32_t dg2_bad(f2 DYU, f2 PG, f2 W) {
   const uint32_t lo = f2_to_bf16x2(f2_fma(DYU, f2_neg(W), PG));
   const uint32_t hi = f2_to_bf16x2(f2_fma(DYU, W, PG));
   float p0, p1;

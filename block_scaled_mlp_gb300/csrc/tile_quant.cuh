@@ -70,22 +70,14 @@ MX_DEVINL uint32_t e4m3x2_pow2(uint32_t p, uint16_t inv_bf16) {
 MX_DEVINL uint16_t inv_scale_bf16_from_e8m0(uint32_t s) { return (uint16_t)((254u - s) << 7); }
 
 // Both elements of a packed bf16 pair times an fp32 scale (inv2 holds it in
-// both 32-bit halves), one packed fp32 multiply (RN, no flush), then RNE
-// saturating E4M3: the pair's two codes in the low 16 bits.
-MX_DEVINL uint32_t e4m3x2_scaled(uint32_t p, uint64_t inv2) {
-  uint64_t v, r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(p << 16), "r"(p & 0xFFFF0000u));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(v), "l"(inv2));
-  uint32_t lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(r));
-  return cvt_e4m3x2(__uint_as_float(lo), __uint_as_float(hi));
+// both lanes), one packed fp32 multiply (RN, no flush), then RNE saturating
+// E4M3: the pair's two codes in the low 16 bits.
+MX_DEVINL uint32_t e4m3x2_scaled(uint32_t p, f2 inv2) {
+  const f2 r = f2_mul(f2_from_bf16x2(p), inv2);
+  return cvt_e4m3x2(r.x, r.y);
 }
 
-MX_DEVINL uint64_t splat_f32x2(float f) {
-  uint64_t v;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(v) : "r"(__float_as_uint(f)));
-  return v;
-}
+MX_DEVINL f2 splat_f32x2(float f) { return f2_splat(f); }
 
 // Quantize one whole 32-element block held by one thread as 16 packed bf16
 // pairs (element 2i in the low half of p[i]).  Writes the 32 codes as 8
@@ -206,29 +198,21 @@ MX_DEVINL void quant_col16x2(const Ld& ld, uint32_t (&ca)[4], uint32_t (&cb)[4],
 MX_DEVINL float tw_scale(float amax) { return __fdiv_rn(448.0f, fmaxf(amax, 0x1p-40f)); }
 
 // 32 row elements held as 16 packed bf16 pairs -> 8 words of codes.
-MX_DEVINL void tw_row32(const uint32_t (&p)[16], uint32_t (&codes)[8], uint64_t s2) {
+MX_DEVINL void tw_row32(const uint32_t (&p)[16], uint32_t (&codes)[8], f2 s2) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) codes[i] = e4m3x2_scaled(p[2 * i], s2) | (e4m3x2_scaled(p[2 * i + 1], s2) << 16);
 }
 
 // Two columns of 32 rows held as 32 packed words (column A in the low
 // halves) -> 8 words of codes per column.
-MX_DEVINL void tw_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_t (&cb)[8], uint64_t s2) {
+MX_DEVINL void tw_col32x2(const uint32_t (&v)[32], uint32_t (&ca)[8], uint32_t (&cb)[8], f2 s2) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t lo[4], hi[4];
+    f2 r[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint64_t x, r;
-      const uint32_t w = v[4 * i + k];
-      asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w << 16), "r"(w & 0xFFFF0000u));
-      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(s2));
-      asm("mov.b64 {%0, %1}, %2;" : "=r"(lo[k]), "=r"(hi[k]) : "l"(r));
-    }
-    ca[i] = cvt_e4m3x2(__uint_as_float(lo[0]), __uint_as_float(lo[1])) |
-            (cvt_e4m3x2(__uint_as_float(lo[2]), __uint_as_float(lo[3])) << 16);
-    cb[i] = cvt_e4m3x2(__uint_as_float(hi[0]), __uint_as_float(hi[1])) |
-            (cvt_e4m3x2(__uint_as_float(hi[2]), __uint_as_float(hi[3])) << 16);
+    for (int k = 0; k < 4; ++k) r[k] = f2_mul(f2_from_bf16x2(v[4 * i + k]), s2);
+    ca[i] = cvt_e4m3x2(r[0].x, r[1].x) | (cvt_e4m3x2(r[2].x, r[3].x) << 16);
+    cb[i] = cvt_e4m3x2(r[0].y, r[1].y) | (cvt_e4m3x2(r[2].y, r[3].y) << 16);
   }
 }
 

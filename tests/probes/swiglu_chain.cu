@@ -25,7 +25,7 @@ __global__ void k(Out* o) {
   if (b >= 65536) return;
   const float g = __uint_as_float(b << 16);
   if (!(fabsf(g) <= 64.0f)) return;
-  const uint64_t G = f2_pack(g, g);
+  const f2 G = f2_pack(g, g);
   const SigFast2 f = sig_fast2(G);
   float t, s, t1, s1; f2_unpack(f.T, t, t1); f2_unpack(f.S, s, s1);
   const double gd = g, et = exp(-gd);
@@ -42,10 +42,10 @@ __global__ void k(Out* o) {
     if ((A & 0xFFFFu) != f32_to_bf16_bits(q)) atomicAdd(&o->a_bad, 1u);
   }
   // dg: si = s (1 + g (t s)) against F = sigma (1 + g (1 - sigma))
-  const uint64_t GO = f2_mul(G, f2_mul(f.T, f.S));
-  const uint64_t IN = f2_add(GO, f2_splat(1.0f));
-  const uint64_t SI = f2_mul(f.S, IN);
-  const uint64_t W2 = dg2_width(f.S, GO, IN);
+  const f2 GO = f2_mul(G, f2_mul(f.T, f.S));
+  const f2 IN = f2_add(GO, f2_splat(1.0f));
+  const f2 SI = f2_mul(f.S, IN);
+  const f2 W2 = dg2_width(f.S, GO, IN);
   float si, w, x0, x1;
   f2_unpack(SI, si, x0);
   f2_unpack(W2, w, x1);
