@@ -187,28 +187,22 @@ __global__ void __launch_bounds__(THREADS, 2)
           const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
           const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-          uint32_t yp[4];
-          bool all = true;
+          uint32_t yp[4], miss[4], any = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             // a = RN_bf16(g s), certified by its interval; y = RN_bf16(a u)
             // from the exact product of the bf16 halves
             const f2 G = f2_from_bf16x2(gp[i]);
-            bool c;
-            const uint32_t A = silu2_cert(G, sig_fast2(G).S, c);
-            float g0, g1;
-            f2_unpack(G, g0, g1);
-            all = all && c && fabsf(g0) <= 64.0f && fabsf(g1) <= 64.0f;
+            const uint32_t A = silu2_cert(G, sig_fast2(G).S, miss[i]);
+            miss[i] |= g_out_of_range2(gp[i]);
+            any |= miss[i];
             yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
           }
           *reinterpret_cast<uint4*>(yt + tile_chunk(rr, seg)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
           uint32_t slow = 0;
-          if (!all) {  // rare: which elements failed
+          if (any) {  // rare: which elements failed
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const f2 G = f2_from_bf16x2(gp[i]);
-              slow |= silu2_bad(G, sig_fast2(G).S) << (2 * i);
-            }
+            for (int i = 0; i < 4; ++i) slow |= miss_lanes(miss[i]) << (2 * i);
           }
           while (slow) {
             const int j = __ffs(slow) - 1;
@@ -407,16 +401,15 @@ __global__ void __launch_bounds__(THREADS, 2)
           const uint32_t dp[4] = {dv.x, dv.y, dv.z, dv.w};
           const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-          uint32_t dgp[4], dup[4], yp[4];
-          bool all = true;
+          uint32_t dgp[4], dup[4], yp[4], miss[4], any = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const f2 G = f2_from_bf16x2(gp[i]);
             const SigFast2 f = sig_fast2(G);
             // a = RN_bf16(g s), certified; du = RN_bf16(dy a), y = RN_bf16(a u)
             // from exact products of bf16 halves
-            bool ca, cg;
-            const uint32_t A = silu2_cert(G, f.S, ca);
+            uint32_t ma, mg;
+            const uint32_t A = silu2_cert(G, f.S, ma);
             dup[i] = f2_to_bf16x2(f2_mul_bf16x2(dp[i], A));
             if (MODE == 2) yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
             // dg tier 1: (dy u) * (s * (1 + g (t s))), dy u exact, certified by
@@ -425,23 +418,14 @@ __global__ void __launch_bounds__(THREADS, 2)
             const f2 GO = f2_mul(G, f2_mul(f.T, f.S));
             const f2 IN = f2_add(GO, f2_splat(1.0f));
             const f2 PG = f2_mul(DYU, f2_mul(f.S, IN));
-            dgp[i] = dg2_cert(DYU, PG, dg2_width(f.S, GO, IN), cg);
-            float g0, g1;
-            f2_unpack(G, g0, g1);
-            all = all && ca && cg && fabsf(g0) <= 64.0f && fabsf(g1) <= 64.0f;
+            dgp[i] = dg2_cert(DYU, PG, dg2_width(f.S, GO, IN), mg);
+            miss[i] = ma | mg | g_out_of_range2(gp[i]);
+            any |= miss[i];
           }
           uint32_t slow = 0;
-          if (!all) {  // rare: which elements failed
+          if (any) {  // rare: which elements failed
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const f2 G = f2_from_bf16x2(gp[i]);
-              const SigFast2 f = sig_fast2(G);
-              const f2 DYU = f2_mul_bf16x2(dp[i], up[i]);
-              const f2 GO = f2_mul(G, f2_mul(f.T, f.S));
-              const f2 IN = f2_add(GO, f2_splat(1.0f));
-              const f2 PG = f2_mul(DYU, f2_mul(f.S, IN));
-              slow |= (silu2_bad(G, f.S) | dg2_bad(DYU, PG, dg2_width(f.S, GO, IN))) << (2 * i);
-            }
+            for (int i = 0; i < 4; ++i) slow |= miss_lanes(miss[i]) << (2 * i);
           }
           *reinterpret_cast<uint4*>(ot + tile_chunk(rr, seg)) = make_uint4(dgp[0], dgp[1], dgp[2], dgp[3]);
           *reinterpret_cast<uint4*>(ot + SB_BOX + tile_chunk(rr, seg)) = make_uint4(dup[0], dup[1], dup[2], dup[3]);

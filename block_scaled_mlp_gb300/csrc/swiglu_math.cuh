@@ -326,10 +326,12 @@ MX_DEVINL SigFast2 sig_fast2(f2 G) {
 
 // ---- packed certificates (both lanes of a pair at once)
 //
-// Each returns the candidate bf16 pair and sets ok only if that rounding is
-// certain: the exact value lies in an interval around the fp32 fast value
-// that covers the fast chain's error, and both ends of the interval round to
-// the same bf16 (rounding is monotone, so everything between them does too).
+// Each returns the candidate bf16 pair and a mismatch word that is zero in
+// the 16-bit half of every lane whose rounding is certain: the exact value
+// lies in an interval around the fp32 fast value that covers the fast
+// chain's error, and both ends of the interval round to the same bf16
+// (rounding is monotone, so everything between them does too).  A failing
+// lane leaves a nonzero half, so the per-lane verdicts need no recomputation.
 
 // RN_f32 of the products of the bf16 halves of a and b (lane 0 from the low
 // halves): exact in fp32's range (8 x 8 significant bits), computed by the
@@ -351,18 +353,19 @@ MX_DEVINL f2 f2_neg(f2 v) { return make_float2(-v.x, -v.y); }
 // a = RN_bf16(g s): p = g s is within 9 fp32 ulps of g * sigma_c (sigma_c the
 // correctly rounded sigma); the interval [p(1 - 2^-19), p(1 + 2^-19)] is at
 // least 15.5 ulps wide on each side.
-MX_DEVINL uint32_t silu2_cert(f2 G, f2 S, bool& ok) {
+MX_DEVINL uint32_t silu2_cert(f2 G, f2 S, uint32_t& miss) {
   const f2 P = f2_mul(G, S);
   const uint32_t lo = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F7FFFE0u))));  // 1 - 2^-19
   const uint32_t hi = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F800010u))));  // 1 + 2^-19
-  ok = lo == hi;
+  miss = lo ^ hi;
   return lo;
 }
 
 // Margin constants of dg, in units of 2^-24: the fast value PG = dyu (s (1 +
 // g t s)) is within |dyu| s (DG_C0 |1 + go| + DG_C1 |go|) 2^-24 of the exact
 // dyu F(g) (go = g t s; the cancellation in 1 + go amplifies go's error),
-// including the rounding of PG and of the interval ends.
+// including the rounding of PG and of the interval ends, while PG is a
+// normal fp32 value.
 constexpr float DG_C0 = 24.0f * 0x1p-24f;
 constexpr float DG_C1 = 26.0f * 0x1p-24f;
 
@@ -371,40 +374,26 @@ MX_DEVINL f2 dg2_width(f2 S, f2 GO, f2 IN) {
   return f2_mul(S, f2_fma(f2_abs(GO), f2_splat(DG_C1), f2_mul(f2_abs(IN), f2_splat(DG_C0))));
 }
 
-// dg = RN_bf16(dyu F): the interval PG -+ dyu W (signed dyu: the ends swap,
-// the interval is the same).  A |PG| below 2^-100 (but not zero) is not
-// certified: there the fp32 roundings are not relative.
-MX_DEVINL uint32_t dg2_cert(f2 DYU, f2 PG, f2 W, bool& ok) {
-  const uint32_t lo = f2_to_bf16x2(f2_fma(DYU, f2_neg(W), PG));
-  const uint32_t hi = f2_to_bf16x2(f2_fma(DYU, W, PG));
-  float p0, p1;
-  f2_unpack(PG, p0, p1);
-  ok = (lo == hi) && (fabsf(p0) >= 0x1p-100f || p0 == 0.0f) && (fabsf(p1) >= 0x1p-100f || p1 == 0.0f);
-  return lo;
+// dg = RN_bf16(dyu F), returned as RN_bf16(PG): the interval
+// PG -+ (|dyu| W + 2^-149) also covers the absolute rounding error (at most
+// 2^-150) of a PG or an interval end in fp32's subnormal range.  The ends
+// are compared without their signs: when both round to a zero, the exact
+// value rounds to the zero of its own sign, which is PG's (the sign of the
+// fast factor is exact, see the probe), so PG's own rounding is the result.
+MX_DEVINL uint32_t dg2_cert(f2 DYU, f2 PG, f2 W, uint32_t& miss) {
+  const f2 AD = f2_abs(DYU);
+  const uint32_t lo = f2_to_bf16x2(f2_fma(AD, f2_neg(W), f2_add(PG, f2_splat(-0x1p-149f))));
+  const uint32_t hi = f2_to_bf16x2(f2_fma(AD, W, f2_add(PG, f2_splat(0x1p-149f))));
+  miss = (lo ^ hi) & 0x7FFF7FFFu;
+  return f2_to_bf16x2(PG);
 }
 
-// Lanes (bit 0: low, bit 1: high) whose a = RN_bf16(g s) is not certified
-// (the per-element view of silu2_cert, for the rare groups that fail).
-MX_DEVINL uint32_t silu2_bad(f2 G, f2 S) {
-  const f2 P = f2_mul(G, S);
-  const uint32_t lo = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F7FFFE0u))));
-  const uint32_t hi = f2_to_bf16x2(f2_mul(P, f2_splat(__uint_as_float(0x3F800010u))));
-  float g0, g1;
-  f2_unpack(G, g0, g1);
-  const uint32_t d = lo ^ hi;
-  return ((d & 0xFFFFu) || !(fabsf(g0) <= 64.0f) ? 1u : 0u) | ((d >> 16) || !(fabsf(g1) <= 64.0f) ? 2u : 0u);
-}
+// bit 15 / bit 31 set for a lane whose bf16 g has |g| > 64 or is not finite
+// (magnitude bits above 0x4280 carry into the top bit of their half)
+MX_DEVINL uint32_t g_out_of_range2(uint32_t gp) { return ((gp & 0x7FFF7FFFu) + 0x3D7F3D7Fu) & 0x80008000u; }
 
-// The same for dg (dg2_cert's interval and magnitude test, per lane).
-MX_DEVINL uint32_t dg2_bad(f2 DYU, f2 PG, f2 W) {
-  const uint32_t lo = f2_to_bf16x2(f2_fma(DYU, f2_neg(W), PG));
-  const uint32_t hi = f2_to_bf16x2(f2_fma(DYU, W, PG));
-  float p0, p1;
-  f2_unpack(PG, p0, p1);
-  const uint32_t d = lo ^ hi;
-  const bool t0 = fabsf(p0) >= 0x1p-100f || p0 == 0.0f, t1 = fabsf(p1) >= 0x1p-100f || p1 == 0.0f;
-  return ((d & 0xFFFFu) || !t0 ? 1u : 0u) | ((d >> 16) || !t1 ? 2u : 0u);
-}
+// the lanes (bit 0: low, bit 1: high) a mismatch word marks
+MX_DEVINL uint32_t miss_lanes(uint32_t miss) { return ((miss & 0xFFFFu) ? 1u : 0u) | ((miss >> 16) ? 2u : 0u); }
 
 }  // namespace
 }  // namespace swiglu_math
