@@ -260,11 +260,10 @@ def run_gpu(args, rank, world, dev):
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
     value = whole_job_tflops(w["flops"], world, ms_max)
-    # own kernels per step: 13, or 12 when the w13 GEMM carries the SwiGLU
-    # (wgrad_with_hp recipes)
-    # the w13 GEMM carries SwiGLU and the quantization of y, except for the
-    # MXFP8-wgrad recipes at d < 5120 (a separate SwiGLU launch)
-    launches_per_step = 12 if (w["recipe"] == "wgrad_hp" or d >= 5120) else 13
+    # own kernels per step: 12 when the w13 GEMM carries SwiGLU and the
+    # quantization of y (wgrad_with_hp recipes, and the MXFP8-wgrad recipes
+    # at d >= 4096), else 13 (a separate SwiGLU launch)
+    launches_per_step = 12 if (w["recipe"] == "wgrad_hp" or d >= 4096) else 13
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs (x, dout) in from pinned host memory and all of its

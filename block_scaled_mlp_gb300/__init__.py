@@ -69,6 +69,7 @@ _SIGS = {
     "mx_token_group_pad": ([_V, _I64, _I32, _I32, _I64, _V, _V, _V, _V, _V, _V], _I),
     "mx_gather_rows": ([_V, _I64, _I64, _V, _I64, _I32, _V, _V, _V], _I),
     "mx_selftest_wait_timeout": ([_V, _V], _I),
+    "mx_selftest_silu_table": ([_V, _V], _I),
     "mx_launch_counts": ([ctypes.POINTER(ctypes.c_int64), _I], _I),
     "mx_fp8_amax": ([_V, _I64, _I64, _V, _V], _I),
     "mx_fp8_quantize": ([_V, _I64, _I64, _I64, _V, _I, _V, _V, _V], _I),
@@ -123,6 +124,15 @@ def _need(t, dtype, name):
 
 
 KERNEL_FAMILIES = ("quant", "swiglu_fwd", "swiglu_bwd", "gemm", "gemm_swiglu", "dispatch", "memset")
+
+
+def silu_table():
+    """The library's table of a(g) = RN_bf16(g sigma(g)) over every bf16 g
+    (entry b for the g with bits b), as a uint16 tensor on the current
+    device."""
+    t = torch.empty(65536, dtype=torch.uint16, device="cuda")
+    _check(lib().mx_selftest_silu_table(t.data_ptr(), _stream()))
+    return t
 
 
 def launch_counts() -> dict:

@@ -50,6 +50,87 @@ int num_sms() {
   return g_sms[dev];
 }
 
+namespace {
+std::once_flag g_ctx_fn_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+// Unique ID of the current context; false if none is current or the driver
+// calls are unavailable (a per-context value is then set up on every call).
+bool current_ctx_id(unsigned long long* id) {
+  std::call_once(g_ctx_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext c = nullptr;
+  return g_ctx_current(&c) == CUDA_SUCCESS && c && g_ctx_id(c, id) == CUDA_SUCCESS;
+}
+
+// A device address that is set up once per CUDA context (a __device__
+// array has one instance per context): cached under the context's unique
+// ID, so a reset device or a caller's own non-primary context gets its own
+// set-up instead of a stale address.
+struct CtxCache {
+  static constexpr int kSlots = 16;
+  struct Slot {
+    unsigned long long ctx_id;
+    void* ptr;
+  };
+  std::mutex mu;
+  Slot slots[kSlots] = {};
+  int next = 0;
+  template <class F>
+  int lookup(void** out, F&& setup) {
+    std::lock_guard<std::mutex> lock(mu);
+    unsigned long long id = 0;
+    if (current_ctx_id(&id))
+      for (const Slot& s : slots)
+        if (s.ptr && s.ctx_id == id) {
+          *out = s.ptr;
+          return MX_OK;
+        }
+    void* ptr = nullptr;
+    const int rc = setup(&ptr);
+    if (rc) return rc;
+    if (current_ctx_id(&id)) {  // the context the set-up ran in
+      slots[next] = Slot{id, ptr};
+      next = (next + 1) % kSlots;
+    }
+    *out = ptr;
+    return MX_OK;
+  }
+};
+
+// a(g) = RN_bf16(RN_f32(g sigma(g))) for every bf16 g, indexed by its bits;
+// filled by launch_silu_table_init the first time a context uses it.
+static __device__ __align__(256) uint16_t g_silu_table[65536];
+CtxCache g_silu_cache;
+}  // namespace
+
+// Device address of the a(g) table in the current context.  The first call
+// in a context fills it on `stream` and waits for that stream (so the call
+// must not be under stream capture); later calls only look it up.
+int silu_table_address(const uint16_t** out, cudaStream_t stream) {
+  void* p = nullptr;
+  const int rc = g_silu_cache.lookup(&p, [stream](void** ptr) {
+    cudaError_t e = cudaGetSymbolAddress(ptr, g_silu_table);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(silu table)");
+    const int r = launch_silu_table_init(static_cast<uint16_t*>(*ptr), stream);
+    if (r) return r;
+    return cuda_status(cudaStreamSynchronize(stream), "silu table fill (first use in this context)");
+  });
+  *out = static_cast<const uint16_t*>(p);
+  return rc;
+}
+
 int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const uint64_t* dims,
               const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
   std::call_once(g_encode_once, [] {
@@ -334,6 +415,7 @@ int mx_swiglu_quant_mode(const void* h13, int64_t M, int64_t h, int axis, int la
   s.q_row = yq_row; s.s_row = ys_row;
   s.q_col = col ? yq_col : nullptr; s.s_col = col ? ys_col : nullptr;
   s.floor_scale = scale_mode == MX_SCALE_FLOOR;
+  if ((rc = silu_table_address(&s.silu_a, st))) return rc;
   return launch_swiglu_fwd(s, st);
 }
 
@@ -564,12 +646,13 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
   // F3 + F4 in one kernel: the w13 GEMM stores h13 and, in its epilogue,
   // y = SwiGLU(h13) as rowwise MXFP8 (+ columnwise for the MXFP8-wgrad
   // recipes, whose weight gradient of w2 contracts y over tokens).  The
-  // epilogue overlaps the next tile's main loop; with both quantizations it
-  // outlasts a main loop of d < kFuseDualMinK (measured at d = 4096: 511 us
-  // fused against 325 + 126 us for the GEMM and the SwiGLU kernel), so
-  // shorter contractions run the two kernels instead (bit-identical).
+  // epilogue overlaps the next tile's main loop.  With a(g) from the table
+  // the fused forward wins from d = 4096 on (M = 8192, h = 8192: 0.630 ms
+  // against 0.714 ms for the GEMM and the SwiGLU kernel); shorter
+  // contractions, where the epilogue can outlast the main loop, run the two
+  // kernels instead (bit-identical).
 #ifndef MX_FUSE_DUAL_MIN_K
-#define MX_FUSE_DUAL_MIN_K 5120
+#define MX_FUSE_DUAL_MIN_K 4096
 #endif
   constexpr int64_t kFuseDualMinK = MX_FUSE_DUAL_MIN_K;
   const bool fuse = hp || d >= kFuseDualMinK;
@@ -579,6 +662,7 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
     g.a = b.xq_r; g.sfa = b.xs_r; g.b = b.w13q_r; g.sfb = b.w13s_r;
     g.M = M; g.N = 2 * h; g.K = d; g.offs = offs; g.E = (int32_t)Ew; g.c0 = b.h13; g.err = err_word;
     if (fuse) {
+      if ((rc = silu_table_address(&g.silu_a, st))) return rc;
       g.fuse_swiglu = 1; g.yq = b.yq_r; g.ys = b.ys_r; g.floor_scale = fl;
       if (!hp) { g.yq_col = b.yq_c; g.ys_col = b.ys_c; }
     }
@@ -590,6 +674,7 @@ int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, in
     s.h13 = b.h13; s.M = M; s.h = h; s.layout = MX_SCALE_MMA; s.err = err_word;
     s.q_row = b.yq_r; s.s_row = b.ys_r;
     s.q_col = b.yq_c; s.s_col = b.ys_c;
+    if ((rc = silu_table_address(&s.silu_a, st))) return rc;
     if ((rc = launch_swiglu_fwd(s, st))) return rc;
   }
   // F5: w2 -> rowwise [d, h] and columnwise [h, d], per expert
@@ -828,57 +913,15 @@ namespace {
 // context gets its own lookup instead of a stale address.
 static __device__ __align__(256) uint8_t g_static_scratch[MX_STATIC_SCRATCH_BYTES];
 
-std::mutex g_static_mu;
-std::once_flag g_ctx_fn_once;
-PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
-PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
-struct StaticSlot {
-  unsigned long long ctx_id;
-  void* ptr;
-};
-constexpr int kStaticSlots = 16;
-StaticSlot g_static_slots[kStaticSlots] = {};
-int g_static_next = 0;
-
-// Unique ID of the current context; false if none is current or the driver
-// calls are unavailable (the address is then looked up on every call).
-bool current_ctx_id(unsigned long long* id) {
-  if (!g_ctx_current || !g_ctx_id) return false;
-  CUcontext c = nullptr;
-  return g_ctx_current(&c) == CUDA_SUCCESS && c && g_ctx_id(c, id) == CUDA_SUCCESS;
-}
+CtxCache g_static_cache;
 
 // Device address of g_static_scratch in the current context (the runtime
 // binds the device's primary context if none is current).
 int static_scratch_address(void** out) {
-  std::call_once(g_ctx_fn_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
-    fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  return g_static_cache.lookup(out, [](void** p) {
+    const cudaError_t e = cudaGetSymbolAddress(p, g_static_scratch);
+    return cuda_status(e, "cudaGetSymbolAddress(static scratch)");
   });
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  unsigned long long id = 0;
-  if (current_ctx_id(&id))
-    for (const StaticSlot& s : g_static_slots)
-      if (s.ptr && s.ctx_id == id) {
-        *out = s.ptr;
-        return MX_OK;
-      }
-  void* ptr = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-  if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(static scratch)");
-  if (current_ctx_id(&id)) {  // the context the lookup ran in
-    g_static_slots[g_static_next] = StaticSlot{id, ptr};
-    g_static_next = (g_static_next + 1) % kStaticSlots;
-  }
-  *out = ptr;
-  return MX_OK;
 }
 }  // namespace
 
@@ -909,6 +952,16 @@ namespace {
 constexpr size_t kSelftestBytes = 256 * 256 * 2 + 2 * 2048 + 256 * 256 * 2;  // A, B codes; scales; C
 static __device__ __align__(256) uint8_t g_selftest[kSelftestBytes];
 }  // namespace
+
+extern "C" int mx_selftest_silu_table(uint16_t* dst, void* stream) {
+  if (!dst) return fail(MX_ERR_INVALID_ARG, "dst is required");
+  const uint16_t* tab = nullptr;
+  int rc = silu_table_address(&tab, (cudaStream_t)stream);
+  if (rc) return rc;
+  return cuda_status(cudaMemcpyAsync(dst, tab, 65536 * sizeof(uint16_t), cudaMemcpyDeviceToDevice,
+                                     (cudaStream_t)stream),
+                     "cudaMemcpyAsync(silu table)");
+}
 
 extern "C" int mx_selftest_wait_timeout(int32_t* err_word, void* stream) {
   if (!err_word) return fail(MX_ERR_INVALID_ARG, "err_word is required");

@@ -100,6 +100,7 @@ struct GemmParams {
   ScaleDst ysc;               // [hy, M/32] columnwise scales
   int64_t hy;                 // h
   uint32_t rceil;             // 1: RCEIL scales, 0: FLOOR
+  const uint16_t* silu_a;     // a(g) = RN_bf16(g sigma(g)) indexed by the bits of bf16 g
   // FP8 per-tensor recipe: amax of A (one) and of B (one, or one per expert
   // when amax_b_per_expert); C = acc * (1/s_a) * (1/s_b), s = 448 / amax
   const float* amax_a;
@@ -705,37 +706,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         store_chunk(gw[1], &tmC0, ycol + 32, mrow);
         store_chunk(uw[0], &tmC0, p.hy + ycol, mrow);
         store_chunk(uw[1], &tmC0, p.hy + ycol + 32, mrow);
-        // y = SwiGLU(g, u) of this thread's row, the same certified fast path
-        // and exact tiers as the standalone SwiGLU kernel, then rows quantized
+        // y = SwiGLU(g, u) of this thread's row: a(g) = RN_bf16(g sigma(g))
+        // from the table of exact values over every bf16 g, then y =
+        // RN_bf16(a u) (the product of two bf16 values is exact in fp32),
+        // and the rows quantized
         const int64_t row = mrow + lane;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           uint32_t yw[16];
-          uint32_t slow = 0;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const f2 G = f2_from_bf16x2(gw[b][i]);
-            const f2 P = f2_mul(G, swiglu_math::sig_fast2(G).S);
-            float g0, g1, p0, p1;
-            f2_unpack(G, g0, g1);
-            f2_unpack(P, p0, p1);
-            slow |= (fabsf(g0) <= 64.0f && swiglu_math::clear_of_midpoint(p0, 16) ? 0u : 1u) << (2 * i);
-            slow |= (fabsf(g1) <= 64.0f && swiglu_math::clear_of_midpoint(p1, 16) ? 0u : 1u) << (2 * i + 1);
-            yw[i] = f2_to_bf16x2(f2_mul(f2_from_bf16x2(f2_to_bf16x2(P)), f2_from_bf16x2(uw[b][i])));
-          }
-          if (slow) {  // exact tiers for the uncertain elements (static indices: registers stay registers)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                if ((slow >> (2 * i + hh)) & 1u) {
-                  const float g = hh ? bf16_hi(gw[b][i]) : bf16_lo(gw[b][i]);
-                  const float uu = hh ? bf16_hi(uw[b][i]) : bf16_lo(uw[b][i]);
-                  const uint32_t y = f32_to_bf16_bits(__fmul_rn(bf16_lo(swiglu_math::silu_bits_slow(g)), uu));
-                  yw[i] = hh ? ((yw[i] & 0xFFFFu) | (y << 16)) : ((yw[i] & 0xFFFF0000u) | y);
-                }
-              }
-            }
+            const uint32_t gp = gw[b][i];
+            const uint32_t a =
+                (uint32_t)__ldg(p.silu_a + (gp & 0xFFFFu)) | ((uint32_t)__ldg(p.silu_a + (gp >> 16)) << 16);
+            yw[i] = f2_to_bf16x2(swiglu_math::f2_mul_bf16x2(a, uw[b][i]));
           }
           uint32_t codes[8];
           const uint32_t sc = quant_row32(yw, codes, p.rceil);
@@ -1052,6 +1036,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.ysc = ScaleDst{(uint8_t*)g.ys_col, (Sc + 3) / 4, Sc, 1};
   }
   p.rceil = g.floor_scale ? 0u : 1u;
+  p.silu_a = g.silu_a;
   p.amax_a = g.amax_a;
   p.amax_b = g.amax_b;
   p.amax_b_per_expert = g.amax_b_per_expert;
@@ -1103,6 +1088,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (fuse) {
     if (!mx || BN != 256 || g.mode == GEMM_GROUP_K || g.N % 256 || !g.yq || !g.ys)
       return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: MXFP8 forward form, 2h a multiple of 256");
+    if (!g.silu_a) return fail(MX_ERR_INVALID_ARG, "fused SwiGLU GEMM: the a(g) table is required");
     if (!g.yq_col != !g.ys_col || (g.yq_col && g.M % 128))
       return fail(MX_ERR_UNSUPPORTED, "fused SwiGLU GEMM: columnwise y needs both buffers and M a multiple of 128");
     if (pair) return launch_cfg<true, 256, 2, 1, true, 1>(g, tA, tB, tC0, tC1, tSFA, tSFB, p, stream);

@@ -64,6 +64,7 @@ struct SwigluLaunch {
   void* dh13_t;               // bwd, optional: [2h, M] bf16
   void* y_t;                  // bwd, optional: [h, M] bf16
   int floor_scale;            // 1: FLOOR E8M0 scales; 0 (default): RCEIL
+  const uint16_t* silu_a;     // fwd: a(g) for every bf16 g (see launch_silu_table_init)
   int32_t* err;
 };
 int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream);
@@ -98,6 +99,7 @@ struct GemmLaunch {
   void* yq_col;      // optional columnwise y: codes [h, M] and MMA-layout scales [h, M/32]
   void* ys_col;
   int floor_scale;   // 1: FLOOR E8M0 scales for y
+  const uint16_t* silu_a;  // a(g) = RN_bf16(g sigma(g)) for every bf16 g (65536 entries, device)
   // FP8 per-tensor recipe (mx = 1, E4M3 codes without block scales): amax
   // of A ([1]) and of B ([1], or [E] when amax_b_per_expert), device fp32
   int tw;
@@ -108,6 +110,10 @@ struct GemmLaunch {
   int32_t* err;
 };
 int launch_gemm(const GemmLaunch& g, cudaStream_t stream);
+
+// Fills table[b] = a(g) = RN_bf16(RN_f32(g sigma(g))) for every bf16 bit
+// pattern b = bits(g), by the exact tiers of swiglu_math.cuh (swiglu.cu).
+int launch_silu_table_init(uint16_t* table, cudaStream_t stream);
 
 // token-group padding (dispatch.cu)
 size_t token_group_pad_workspace(int64_t R, int32_t E);

@@ -28,14 +28,16 @@ using namespace swiglu_math;
 //
 // Both kernels stream tiles through a 2-stage TMA ring and run three roles:
 //   producer warp  TMA loads of the input tiles
-//   8 consumer     phase A: every element through the fp32 fast path into a
-//   warps          shared-memory result tile; elements whose rounding the
-//                  fast path cannot certify are queued.  Phase C: MX
+//   8 consumer     phase A: every element into a shared-memory result tile
+//   warps          (forward: a(g) from the table of exact values over every
+//                  bf16 g; backward: the fp32 fast path, elements whose
+//                  rounding it cannot certify are queued).  Phase C: MX
 //                  quantization of the previous (complete) tile, rows on
 //                  warps 4-7 and columns on warps 0-3
 //   fixer warp     phase B: recomputes the queued elements of a tile with
 //                  the exact tiers (32 at a time) and patches the result
-//                  tile, then releases the input stage
+//                  tile, then releases the input stage (forward: releases
+//                  it only)
 // Per tile, one barrier of consumers + fixer (A done) and one of consumers
 // only (C done).  The long dependency chains of the exact tiers run on the
 // fixer while the consumers quantize the previous tile and start the next,
@@ -84,7 +86,7 @@ constexpr int SF_R = 128, SF_C = 64;
 constexpr int SF_STAGES = 2;
 constexpr int SF_BOX = SF_R * SF_C * 2;       // 16 KB
 constexpr int SF_STAGE_BYTES = 2 * SF_BOX;    // g, u
-constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + 2 * QCAP * 2 + 1024 + 128;
+constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + 1024 + 128;
 
 struct SwiFwdParams {
   int64_t M, h;
@@ -92,6 +94,7 @@ struct SwiFwdParams {
   uint8_t* q_row; ScaleDst s_row;
   uint8_t* q_col; ScaleDst s_col;
   uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
+  const uint16_t* silu_a;  // a(g) = RN_bf16(g sigma(g)) indexed by the bits of bf16 g
   int32_t* err;
 };
 
@@ -101,10 +104,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ytile = smem + SF_STAGES * SF_STAGE_BYTES;            // 2 x 16 KB
-  uint16_t* queue = reinterpret_cast<uint16_t*>(ytile + 2 * SF_BOX);   // 2 x QCAP
-  uint64_t* full = reinterpret_cast<uint64_t*>(queue + 2 * QCAP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ytile + 2 * SF_BOX);
   uint64_t* empty = full + SF_STAGES;
-  __shared__ int s_qn[2];
   __shared__ long long s_abort;  // first tile index whose wait timed out
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
@@ -112,7 +113,6 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (tid == 0) {
     for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     fence_mbar_init();
-    s_qn[0] = s_qn[1] = 0;
     s_abort = 0x7FFFFFFFFFFFFFFFll;
   }
   __syncthreads();
@@ -135,31 +135,15 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
 
   if (warp == FIXER) {
-    // ---- phase B for tile t, between its A barrier and the next one
-    int stage = 0, buf = 0;
-    for (int64_t t = blockIdx.x;; t += gridDim.x, buf ^= 1) {
+    // the forward has nothing to fix (a(g) comes from the table of exact
+    // values): this warp only releases tile t's input stage once every
+    // consumer is past its phase A
+    int stage = 0;
+    for (int64_t t = blockIdx.x;; t += gridDim.x) {
       const bool have = t < n_tiles;
       bar_ab();
       if (!have || s_abort <= t) break;
-      const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
-      const uint8_t* ut = gt + SF_BOX;
-      uint8_t* yt = ytile + buf * SF_BOX;
-      const uint16_t* q = queue + buf * QCAP;
-      const int n = min(s_qn[buf], QCAP);
-      for (int i = lane; i < n; i += 32) {
-        const int idx = q[i];
-        const int row = idx / SF_C, col = idx % SF_C;
-        const int off = row * 128 + col * 2;
-        const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off));
-        const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off));
-        const float a = bf16_lo(silu_bits_slow(g));
-        *reinterpret_cast<uint16_t*>(yt + tile_off(row, col)) = (uint16_t)f32_to_bf16_bits(__fmul_rn(a, u));
-      }
-      __syncwarp();
-      if (lane == 0) {
-        s_qn[buf] = 0;
-        mbar_arrive(&empty[stage]);   // inputs of tile t no longer needed
-      }
+      if (lane == 0) mbar_arrive(&empty[stage]);   // inputs of tile t no longer needed
       if (++stage == SF_STAGES) stage = 0;
     }
     return;
@@ -177,7 +161,6 @@ __global__ void __launch_bounds__(THREADS, 2)
       const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
       const uint8_t* ut = gt + SF_BOX;
       uint8_t* yt = ytile + buf * SF_BOX;
-      uint16_t* q = queue + buf * QCAP;
       // ---- phase A
       if (ok) {
 #pragma unroll 1
@@ -187,37 +170,17 @@ __global__ void __launch_bounds__(THREADS, 2)
           const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
           const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-          uint32_t yp[4], miss[4], any = 0;
+          uint32_t yp[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            // a = RN_bf16(g s), certified by its interval; y = RN_bf16(a u)
-            // from the exact product of the bf16 halves
-            const f2 G = f2_from_bf16x2(gp[i]);
-            const uint32_t A = silu2_cert(G, sig_fast2(G).S, miss[i]);
-            miss[i] |= g_out_of_range2(gp[i]);
-            any |= miss[i];
+            // a = RN_bf16(g sigma(g)) from the table of exact values over
+            // every bf16 g; y = RN_bf16(a u) from the exact product of the
+            // bf16 halves
+            const uint32_t A = (uint32_t)__ldg(p.silu_a + (gp[i] & 0xFFFFu)) |
+                               ((uint32_t)__ldg(p.silu_a + (gp[i] >> 16)) << 16);
             yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
           }
           *reinterpret_cast<uint4*>(yt + tile_chunk(rr, seg)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
-          uint32_t slow = 0;
-          if (any) {  // rare: which elements failed
-#pragma unroll
-            for (int i = 0; i < 4; ++i) slow |= miss_lanes(miss[i]) << (2 * i);
-          }
-          while (slow) {
-            const int j = __ffs(slow) - 1;
-            slow &= slow - 1;
-            const int slot = atomicAdd(&s_qn[buf], 1);
-            if (slot < QCAP) {
-              q[slot] = (uint16_t)(rr * SF_C + seg * 8 + j);
-            } else {  // queue full: resolve here, over this thread's own store above
-              const int off = rr * 128 + (seg * 8 + j) * 2;
-              const float g = bf16_lo(*reinterpret_cast<const uint16_t*>(gt + off));
-              const float u = bf16_lo(*reinterpret_cast<const uint16_t*>(ut + off));
-              *reinterpret_cast<uint16_t*>(yt + tile_off(rr, seg * 8 + j)) =
-                  (uint16_t)f32_to_bf16_bits(__fmul_rn(bf16_lo(silu_bits_slow(g)), u));
-            }
-          }
         }
       }
       if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
@@ -536,7 +499,20 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
 }
 
+// a(g) for every bf16 bit pattern, by the exact tiers (the same function
+// the kernels fall back to for the elements their certificates leave open).
+__global__ void silu_table_kernel(uint16_t* table) {
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < 65536u) table[b] = (uint16_t)swiglu_math::silu_bits_slow(__uint_as_float(b << 16));
+}
+
 }  // namespace
+
+int launch_silu_table_init(uint16_t* table, cudaStream_t stream) {
+  if (!table) return fail(MX_ERR_INVALID_ARG, "silu table: null destination");
+  silu_table_kernel<<<256, 256, 0, stream>>>(table);
+  return cuda_status(cudaGetLastError(), "silu_table_kernel launch");
+}
 
 int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   CUtensorMap tm;
@@ -555,7 +531,9 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   p.q_row = (uint8_t*)s.q_row; p.s_row = ScaleDst{(uint8_t*)s.s_row, (Sr + 3) / 4, Sr, mma};
   p.q_col = (uint8_t*)s.q_col; p.s_col = ScaleDst{(uint8_t*)s.s_col, (Sc + 3) / 4, Sc, mma};
   p.rceil = s.floor_scale ? 0u : 1u;
+  p.silu_a = s.silu_a;
   p.err = s.err;
+  if (!p.silu_a) return fail(MX_ERR_INVALID_ARG, "swiglu forward: the a(g) table is required");
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
   if (n_tiles == 0) return MX_OK;
   const int grid = (int)std::min<int64_t>(n_tiles, (int64_t)num_sms() * 2);

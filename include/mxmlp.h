@@ -263,6 +263,10 @@ MX_API int mx_mlp_ctx_layout(int64_t M_total, int64_t d, int64_t h, int32_t E, i
  *   ctx, scratch: buffers of the sizes mx_mlp_workspace_size returns (16-byte
  *   aligned).  out [M_total, d] bf16.
  * Requirements: M_total % 128 == 0, d % 128 == 0, h % 128 == 0.
+ * The first call in a CUDA context that takes the fused w13 GEMM + SwiGLU
+ * path (d >= 5120, or the wgrad_with_hp recipe) fills the library's table of
+ * a(g) = RN_bf16(g sigma(g)) over every bf16 g (128 KB of static device
+ * memory) on `stream` and waits for `stream`; later calls do not wait.
  */
 MX_API int mx_mlp_fwd(const void* x, const void* w1, const void* w3, const void* w2, int64_t M_total,
                int64_t d, int64_t h, const int32_t* offs, int32_t E, int32_t pad_multiple,
@@ -475,6 +479,17 @@ MX_API int mx_launch_counts(int64_t* counts, int n);
  * counterpart on the pages); the call takes about 2 s of GPU time.
  */
 MX_API int mx_selftest_wait_timeout(int32_t* err_word, void* stream);
+
+/*
+ * mx_selftest_silu_table - test entry of the a(g) table the fused w13 GEMM
+ * epilogue reads: copies its 65536 entries (entry b = the bits of
+ * RN_bf16(RN_f32(g sigma(g))) for the bf16 g with bits b; the silu rounding
+ * of the page "Add MXFP8 fused-MLP overrides in torchtitan", Numerics) into
+ * dst (device memory, 131072 bytes, caller-owned) on `stream`, filling the
+ * table first if this context has not used it yet (which waits for
+ * `stream`).  MX_ERR_INVALID_ARG if dst is NULL.
+ */
+MX_API int mx_selftest_silu_table(uint16_t* dst, void* stream);
 
 #ifdef __cplusplus
 }

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
                  "mx_token_group_pad_workspace", "mx_token_group_pad", "mx_gather_rows",
                  "mx_linear_workspace_size", "mx_linear_fwd", "mx_linear_bwd", "mx_quantize_mode",
                  "mx_swiglu_quant_mode", "mx_swiglu_quant_bwd_mode", "mx_mlp_fwd_static_scratch",
-                 "mx_selftest_wait_timeout", "mx_mlp_ctx_layout"]:
+                 "mx_selftest_wait_timeout", "mx_selftest_silu_table", "mx_mlp_ctx_layout"]:
         assert want in names
 
 
@@ -169,6 +169,10 @@ def test_mlp_context_layout(L):
                 assert sizes["yq_col"] == h * M and sizes["ys_col"] == mx.mma_scale_bytes(h, M)
     off, n = ctypes.c_size_t(), ctypes.c_size_t()
     assert L.mx_mlp_ctx_layout(M, d, h, 0, 0, 10, ctypes.byref(off), ctypes.byref(n)) == 1
+
+
+def test_silu_table_needs_a_destination(L):
+    assert L.mx_selftest_silu_table(None, None) == 1  # MX_ERR_INVALID_ARG, before any device call
 
 
 def test_selftest_needs_an_error_word(L):

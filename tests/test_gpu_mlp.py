@@ -133,7 +133,7 @@ def _setup(kind):
         return _inputs_dense(256, 256, 512, seed=0)           # the tiny dense config
     if kind == "grouped_tail":
         return _inputs_grouped_tail([100, 0, 300, 28], 256, 384, seed=4, tail=128)
-    # d = 5120: long enough a contraction that the w13 GEMM also carries the
+    # d = 5120 (>= 4096): long enough a contraction that the w13 GEMM also carries the
     # columnwise quantization of y under the MXFP8-wgrad recipes
     if kind == "dense_wide":
         return _inputs_dense(256, 5120, 256, seed=6)
@@ -264,7 +264,7 @@ def test_end_to_end_vs_oracle(kind, recipe):
                                          ("grouped_tail_wide", mx.RECIPE_FLOOR)])
 def test_saved_columnwise_operands_vs_oracle(kind, recipe):
     """Under the MXFP8 weight-gradient recipes the forward saves y and x
-    quantized by columns; at d >= 5120 the w13 GEMM's epilogue writes the
+    quantized by columns; at d >= 4096 the w13 GEMM's epilogue writes the
     columnwise y (each 32-row block of its tile), below it the SwiGLU kernel
     does.  Both equal the oracle bit for bit, including the rows past the
     last group (zero codes, scale 0x00)."""
@@ -292,7 +292,7 @@ def test_saved_columnwise_operands_vs_oracle(kind, recipe):
 @pytest.mark.parametrize("kind,recipe", [("dense_wide", mx.RECIPE_RCEIL), ("grouped_tail_wide", mx.RECIPE_FLOOR),
                                          ("dense_wide", mx.RECIPE_RCEIL_WGRAD_HP)])
 def test_fused_forward_equals_op_chain(kind, recipe):
-    """At d >= 5120 the composite's w13 GEMM carries SwiGLU and both
+    """At d >= 4096 the composite's w13 GEMM carries SwiGLU and both
     quantizations of y; its outputs equal the per-op chain bit for bit."""
     inp, t, offs = _setup(kind)
     err = mx.ErrorWord()

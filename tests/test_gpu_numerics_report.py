@@ -131,9 +131,9 @@ def _profiled_kernels(fn):
 
 
 @pytest.mark.parametrize("kind,recipe,fused", [
-    ("dense", mx.RECIPE_RCEIL, False),            # d < 5120: separate SwiGLU kernel
+    ("dense", mx.RECIPE_RCEIL, False),            # d < 4096: separate SwiGLU kernel
     ("dense", mx.RECIPE_RCEIL_WGRAD_HP, True),    # wgrad_with_hp: SwiGLU in the w13 GEMM epilogue
-    ("grouped_wide", mx.RECIPE_RCEIL, True),      # d >= 5120: fused, rows and columns of y
+    ("grouped_wide", mx.RECIPE_RCEIL, True),      # d >= 4096: fused, rows and columns of y
 ])
 def test_op_count_contract(kind, recipe, fused):
     if kind == "grouped_wide":

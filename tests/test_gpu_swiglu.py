@@ -34,6 +34,21 @@ def test_silu_every_bf16_input_exact():
     assert not mism.any(), f"{mism.sum()} mismatches, e.g. g bits {g[mism][:8]}"
 
 
+def test_silu_table_every_bf16_input_exact():
+    """The table of a(g) the fused w13 GEMM epilogue reads: entry b equals
+    the oracle's RN_bf16(RN_f32(g sigma(g))) for the g with bits b, for all
+    65536 patterns (NaN inputs give NaN)."""
+    tab = mx.silu_table()
+    torch.cuda.synchronize()
+    a_gpu = tab.cpu().view(torch.int16).numpy().view(np.uint16)
+    g = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    a_ref = o.swiglu_fwd(g, np.full(65536, 0x3F80, dtype=np.uint16))   # u = 1
+    nan = np.isnan(o.bf16_to_f64(a_ref))
+    assert np.array_equal(np.isnan(o.bf16_to_f64(a_gpu)), nan)
+    mism = (a_gpu != a_ref) & ~nan
+    assert not mism.any(), f"{mism.sum()} mismatches, e.g. g bits {g[mism][:8]}"
+
+
 @pytest.mark.parametrize("M,h", [(256, 512), (384, 192), (128, 64)])
 def test_swiglu_fwd_dual_matches_oracle(M, h):
     h13 = _h13(M, h, seed=M + h)
