@@ -2,7 +2,7 @@
 // both from one read), plus a bf16 transposed copy used by the bf16
 // weight-gradient recipe.
 //
-// Design: a persistent kernel streams 128x128 bf16 tiles through a 3-stage
+// Design: a persistent kernel streams 128x128 bf16 tiles through a 2-stage
 // TMA ring in shared memory (one producer warp, eight consumer warps), each
 // tile as two 64-column boxes stored with the 128-byte swizzle (16-byte
 // chunk c of row r at chunk position c ^ (r & 7)).  The rowwise path gives
@@ -20,7 +20,12 @@ namespace {
 
 constexpr int QT_R = 128;          // tile rows
 constexpr int QT_C = 128;          // tile cols (two 64-column TMA boxes)
-constexpr int QT_STAGES = 3;
+// Two stages, two CTAs per SM: the quantize sweep (N x N, row / col /
+// both, fraction of measured HBM bandwidth) at 8192: 0.77 / 0.67 / 0.72 and
+// at 16384: 0.91 / 0.81 / 0.84, against 0.71-0.72 / 0.62-0.64 / 0.70 and
+// 0.84 / 0.78 / 0.82 with three stages; three CTAs of two stages, or one
+// CTA of four, measured lower still.
+constexpr int QT_STAGES = 2;
 constexpr int QT_BOX_BYTES = QT_R * 64 * 2;        // 16 KB
 constexpr int QT_TILE_BYTES = 2 * QT_BOX_BYTES;    // 32 KB
 constexpr int QT_CONSUMER_WARPS = 8;
