@@ -1,19 +1,20 @@
 // swiglu.cu - fused SwiGLU forward / backward with dual MXFP8 quantization.
 //
 // Forward: h13 = [g | u] tiles stream through a TMA ring; each consumer
-// thread computes y = RN_bf16(a * u) for 8 consecutive elements, quantizes
-// them rowwise straight from registers and parks the bf16 y tile in shared
-// memory, where the columnwise quantization reads it.  y never reaches
-// global memory.
+// thread computes y = RN_bf16(a(g) u) for the 32-element row block or the
+// 32-row column blocks it quantizes, straight from the g and u tiles into
+// registers (a(g) from a table of exact values over every bf16 g).  y never
+// reaches global memory.
 //
 // Backward: dy and h13 tiles in, dh13 = [dg | du] out, quantized rowwise and
-// columnwise the same way (or, for the bf16 weight-gradient recipe, written
-// transposed in bf16 together with the recomputed y).
+// columnwise (or, for the bf16 weight-gradient recipe, written transposed in
+// bf16 together with the recomputed y), through a shared-memory result tile.
 //
-// Numerics: swiglu_math.cuh (exactly rounded a, y, du, dg).  The fast path
-// runs on packed fp32 pairs (own exp from ex2.approx, rcp.approx); a result
-// is accepted only if it lies farther from a bf16 rounding midpoint than the
-// error bound of its chain, otherwise the exact tiers decide.
+// Numerics: swiglu_math.cuh (exactly rounded a, y, du, dg).  The backward's
+// fast path runs on packed fp32 pairs (own exp from ex2.approx, rcp.approx);
+// a result is accepted only if its rounding interval (the value plus or
+// minus the error bound of its chain) rounds to one bf16 value, otherwise the
+// exact tiers decide.
 #include "tile_quant.cuh"
 #include "swiglu_math.cuh"
 #include "kernels.h"
@@ -26,18 +27,18 @@ using namespace swiglu_math;
 
 // ------------------------------------------------------------------ kernels
 //
-// Both kernels stream tiles through a 2-stage TMA ring and run three roles:
+// The backward kernel streams tiles through a 2-stage TMA ring and runs
+// three roles (the forward, which needs no exact tiers, is simpler and is
+// described at its own section below):
 //   producer warp  TMA loads of the input tiles
-//   8 consumer     phase A: every element into a shared-memory result tile
-//   warps          (forward: a(g) from the table of exact values over every
-//                  bf16 g; backward: the fp32 fast path, elements whose
-//                  rounding it cannot certify are queued).  Phase C: MX
-//                  quantization of the previous (complete) tile, rows on
-//                  warps 4-7 and columns on warps 0-3
+//   8 consumer     phase A: every element through the fp32 fast path into a
+//   warps          shared-memory result tile; elements whose rounding it
+//                  cannot certify are queued.  Phase C: MX quantization of
+//                  the previous (complete) tile, rows on warps 4-7 and
+//                  columns on warps 0-3
 //   fixer warp     phase B: recomputes the queued elements of a tile with
 //                  the exact tiers (32 at a time) and patches the result
-//                  tile, then releases the input stage (forward: releases
-//                  it only)
+//                  tile, then releases the input stage
 // Per tile, one barrier of consumers + fixer (A done) and one of consumers
 // only (C done).  The long dependency chains of the exact tiers run on the
 // fixer while the consumers quantize the previous tile and start the next,
@@ -82,11 +83,29 @@ MX_DEVINL void store32(uint8_t* dst, const uint32_t (&c)[8]) {
 }
 
 // ---- forward: tile = 128 rows x 64 y-columns
+//
+// The forward needs no exact tiers (a(g) comes from the table of exact values
+// over every bf16 g), so it streams like the quantize kernel: one producer
+// warp keeps a 2-stage ring of g and u tiles (two 16 KB boxes with the
+// 128-byte swizzle: 16-byte chunk c of row r at chunk position c ^ (r & 7)),
+// and each consumer thread computes the y values it quantizes straight from
+// those tiles into registers, with no result tile and no block barrier.
+// Every thread quantizes one 32-element row block; with columns, warps 2k
+// and 2k+1 then stage their y rows in a small shared buffer, meet at a pair
+// barrier, and each thread quantizes 16 rows of one column pair from it
+// (lanes l and l ^ 16 share the pair's 32-row block).
 constexpr int SF_R = 128, SF_C = 64;
 constexpr int SF_STAGES = 2;
 constexpr int SF_BOX = SF_R * SF_C * 2;       // 16 KB
 constexpr int SF_STAGE_BYTES = 2 * SF_BOX;    // g, u
-constexpr size_t SF_SMEM = SF_STAGES * SF_STAGE_BYTES + 2 * SF_BOX + 1024 + 128;
+constexpr int SF_WARPS = 8;                   // consumer warps
+constexpr int SF_THREADS = (SF_WARPS + 1) * 32;
+// Shared memory per mode: the stages, plus 16 KB of y staging in dual mode.
+// The rest of the SM's 256 KB stays L1, where the a(g) table lookups hit:
+// at 8192 x 8192 the rowwise kernel ran 0.067 ms with this size against
+// 0.076 ms with 32 KB more, and the dual one 0.104 ms with one staging
+// buffer (and a second pair barrier per tile) against 0.111 ms with two.
+constexpr size_t sf_smem(bool col) { return SF_STAGES * SF_STAGE_BYTES + (col ? 4 * 32 * 128 : 0) + 1024 + 64; }
 
 struct SwiFwdParams {
   int64_t M, h;
@@ -98,26 +117,55 @@ struct SwiFwdParams {
   int32_t* err;
 };
 
+// y = RN_bf16(a(g) u) for a packed pair: a(g) from the table, the product of
+// two bf16 values exact in fp32
+MX_DEVINL uint32_t swiglu2(uint32_t gp, uint32_t up, const uint16_t* tab) {
+  const uint32_t a = (uint32_t)__ldg(tab + (gp & 0xFFFFu)) | ((uint32_t)__ldg(tab + (gp >> 16)) << 16);
+  return f2_to_bf16x2(f2_mul_bf16x2(a, up));
+}
+
+// Result staging for the columns (dual mode): warps 2k and 2k+1 cover rows
+// 32k..32k+31 of the tile; their y values go to the pair's 4 KB buffer, row
+// q at q * 128, its 16-byte chunk c at c ^ (q & 7) ^ ((q >> 4) << 2): the
+// row writes (a quarter-warp: four rows, eight chunks) and the column reads
+// (rows q and q + 16 in the two half-warps) both stay free of bank
+// conflicts.  The pair meets twice per tile: buffer written, buffer read.
+constexpr int SF_PAIR_BYTES = 32 * 128;
+MX_DEVINL int sf_pair_chunk(int q, int c) { return q * 128 + ((c ^ (q & 7) ^ ((q >> 4) << 2)) << 4); }
+// barrier 1 + pr of the two warps of pair pr (literal barrier ids, so that
+// the kernel reserves five barriers, not all sixteen)
+template <int ID>
+MX_DEVINL void pair_bar_id() { asm volatile("bar.sync %0, 64;" ::"n"(ID) : "memory"); }
+MX_DEVINL void pair_bar(int pr) {
+  switch (pr) {
+    case 0: pair_bar_id<1>(); break;
+    case 1: pair_bar_id<2>(); break;
+    case 2: pair_bar_id<3>(); break;
+    default: pair_bar_id<4>(); break;
+  }
+}
+
 template <bool COL>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(SF_THREADS, 2)
     swiglu_fwd_kernel(const __grid_constant__ CUtensorMap tmh, SwiFwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ytile = smem + SF_STAGES * SF_STAGE_BYTES;            // 2 x 16 KB
-  uint64_t* full = reinterpret_cast<uint64_t*>(ytile + 2 * SF_BOX);
+  uint8_t* ybuf = smem + SF_STAGES * SF_STAGE_BYTES;   // dual: [4 warp pairs][4 KB]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ybuf + (COL ? 4 * SF_PAIR_BYTES : 0));
   uint64_t* empty = full + SF_STAGES;
-  __shared__ long long s_abort;  // first tile index whose wait timed out
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  __shared__ int s_dead;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
 
-  if (tid == 0) {
-    for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SF_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], SF_WARPS); }
     fence_mbar_init();
-    s_abort = 0x7FFFFFFFFFFFFFFFll;
+    s_dead = 0;
   }
   __syncthreads();
 
-  if (warp == PRODUCER) {
+  if (warp == SF_WARPS) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmh);
       int stage = 0; uint32_t phase = 0;
@@ -134,107 +182,93 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
 
-  if (warp == FIXER) {
-    // the forward has nothing to fix (a(g) comes from the table of exact
-    // values): this warp only releases tile t's input stage once every
-    // consumer is past its phase A
-    int stage = 0;
-    for (int64_t t = blockIdx.x;; t += gridDim.x) {
-      const bool have = t < n_tiles;
-      bar_ab();
-      if (!have || s_abort <= t) break;
-      if (lane == 0) mbar_arrive(&empty[stage]);   // inputs of tile t no longer needed
-      if (++stage == SF_STAGES) stage = 0;
+  // -------------------------------------------------------------- consumers
+  // A wait that runs out marks the CTA dead.  Rowwise only, the consumers
+  // then stop; in dual mode every consumer warp still runs every tile and
+  // meets its pair barrier (so that no partner waits for it), skipping the
+  // waits and the work.
+  const uint16_t* tab = p.silu_a;
+  const int pr = warp >> 1;   // warp pair
+  int stage = 0; uint32_t phase = 0;
+  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
+    const int64_t r0 = rt * SF_R, c0 = ct * SF_C;
+    bool live = *reinterpret_cast<volatile int*>(&s_dead) == 0;
+    live = __all_sync(0xFFFFFFFFu, live);
+    if (live && !warp_wait(&full[stage], phase, p.err)) {
+      if (lane == 0) atomicExch(&s_dead, 1);
+      live = false;
     }
-    return;
-  }
+    if (!COL && !live) break;
+    uint8_t* yb = ybuf + pr * SF_PAIR_BYTES;
 
-  // ---- consumers
-  int stage = 0; uint32_t phase = 0; int buf = 0;
-  const int seg = lane & 7;
-  int64_t t_prev = -1;
-  for (int64_t t = blockIdx.x;; t += gridDim.x, buf ^= 1) {
-    const bool have = t < n_tiles;
-    if (have) {
-      const bool ok = mbar_wait(&full[stage], phase, p.err);
-      if (!ok) atomicMin(&s_abort, (long long)t);
+    if (live) {
       const uint8_t* gt = smem + stage * SF_STAGE_BYTES;
       const uint8_t* ut = gt + SF_BOX;
-      uint8_t* yt = ytile + buf * SF_BOX;
-      // ---- phase A
-      if (ok) {
-#pragma unroll 1
-        for (int it = 0; it < SF_R / (4 * CW); ++it) {
-          const int rr = it * (4 * CW) + warp * 4 + (lane >> 3);
-          const uint4 gv = *reinterpret_cast<const uint4*>(gt + rr * 128 + seg * 16);
-          const uint4 uv = *reinterpret_cast<const uint4*>(ut + rr * 128 + seg * 16);
-          const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
-          const uint32_t up[4] = {uv.x, uv.y, uv.z, uv.w};
-          uint32_t yp[4];
+      // rows: a quarter-warp covers rows 4q..4q+3 of the warp's 16-row band,
+      // two blocks per row, so its eight 16-byte reads land on eight
+      // distinct swizzled chunk positions
+      const int e = lane & 7, jj = e & 1;
+      const int rr = warp * 16 + (lane >> 3) * 4 + (e >> 1);
+      uint32_t y[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // a = RN_bf16(g sigma(g)) from the table of exact values over
-            // every bf16 g; y = RN_bf16(a u) from the exact product of the
-            // bf16 halves
-            const uint32_t A = (uint32_t)__ldg(p.silu_a + (gp[i] & 0xFFFFu)) |
-                               ((uint32_t)__ldg(p.silu_a + (gp[i] >> 16)) << 16);
-            yp[i] = f2_to_bf16x2(f2_mul_bf16x2(A, up[i]));
-          }
-          *reinterpret_cast<uint4*>(yt + tile_chunk(rr, seg)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int off = rr * 128 + (((jj * 4 + k) ^ (rr & 7)) << 4);
+        const uint4 g4 = *reinterpret_cast<const uint4*>(gt + off);
+        const uint4 u4 = *reinterpret_cast<const uint4*>(ut + off);
+        y[4 * k] = swiglu2(g4.x, u4.x, tab);
+        y[4 * k + 1] = swiglu2(g4.y, u4.y, tab);
+        y[4 * k + 2] = swiglu2(g4.z, u4.z, tab);
+        y[4 * k + 3] = swiglu2(g4.w, u4.w, tab);
       }
-      if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
-    }
-    bar_ab();
-    if (s_abort <= (have ? t : t_prev)) break;
-    // ---- phase C of the previous tile (complete: the fixer patched it
-    // before this barrier)
-    if (t_prev >= 0) {
-      const int pb = buf ^ 1;
-      const uint8_t* yt = ytile + pb * SF_BOX;
-      const int64_t rt = t_prev / p.col_tiles, ct = t_prev - rt * p.col_tiles;
-      const int64_t r0 = rt * SF_R, c0 = ct * SF_C;
-      if (warp >= 4 || !COL) {
-        // one thread per 32-element block; a warp covers 16 rows x 2 blocks
-        // (quarter-warp: rows 4g..4g+3, both halves)
-        const int w = COL ? warp - 4 : warp;
-        const int nw = COL ? 4 : CW;
-        const int jj = lane & 1;
-        for (int base = w * 16; base < SF_R; base += nw * 16) {
-          const int rr = base + (lane >> 3) * 4 + ((lane & 7) >> 1);
-          uint32_t codes[8];
-          const uint32_t sc = quant_tile_block(yt, rr, jj, codes, p.rceil);
-          const int64_t r = r0 + rr;
-          const int64_t c = c0 + jj * 32;
-          if (r < p.M) {
-            store32(p.q_row + r * p.h + c, codes);
-            p.s_row.put(r, c >> 5, sc);
-          }
-        }
-      } else {
-        const int item = warp * 32 + lane;
-        const int pc = item & 31, rb = item >> 5;
-        uint32_t v[32];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);   // this warp is done with the stage
+      if (COL) {
+        const int q = rr & 31;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = *reinterpret_cast<const uint32_t*>(yt + tile_word(rb * 32 + i, pc));
-        uint32_t ca[8], cb[8], sa, sb;
-        quant_col32x2(v, ca, cb, sa, sb, p.rceil);
-        const int64_t rg = r0 + rb * 32;
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(yb + sf_pair_chunk(q, jj * 4 + k)) =
+              make_uint4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+      }
+      uint32_t codes[8];
+      const uint32_t sc = quant_row32(y, codes, p.rceil);
+      const int64_t r = r0 + rr;
+      if (r < p.M) {
+        const int64_t c = c0 + jj * 32;
+        uint8_t* dst = p.q_row + r * p.h + c;
+        store16(dst, codes[0], codes[1], codes[2], codes[3]);
+        store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
+        p.s_row.put(r, c >> 5, sc);
+      }
+    }
+    if (++stage == SF_STAGES) { stage = 0; phase ^= 1; }
+    if (COL) {
+      pair_bar(pr);   // both warps' y rows are in the pair buffer
+      if (live) {
+        // columns: warp 2k + j takes column pairs 16j..16j+15 of the pair's
+        // 32-row block; lanes l and l ^ 16 share a pair, 16 rows each
+        const int rh = lane >> 4;
+        const int pc = (warp & 1) * 16 + (lane & 15);
+        uint32_t ca[4], cb[4], sa, sb;
+        quant_col16x2(
+            [&](int i) {
+              return *reinterpret_cast<const uint32_t*>(yb + sf_pair_chunk(rh * 16 + i, pc >> 2) + ((pc & 3) << 2));
+            },
+            ca, cb, sa, sb, p.rceil);
+        const int64_t rg = r0 + pr * 32;
         if (rg < p.M) {
-          const int64_t col = c0 + 2 * pc;
-          uint8_t* dst = p.q_col + col * p.M + rg;
+          const int64_t cg = c0 + 2 * pc;
+          uint8_t* dst = p.q_col + cg * p.M + rg + 16 * rh;
           store16(dst, ca[0], ca[1], ca[2], ca[3]);
-          store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
           store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
-          store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
-          p.s_col.put(col, rg >> 5, sa);
-          p.s_col.put(col + 1, rg >> 5, sb);
+          if (rh == 0) {
+            p.s_col.put(cg, rg >> 5, sa);
+            p.s_col.put(cg + 1, rg >> 5, sb);
+          }
         }
       }
+      pair_bar(pr);   // both warps have read the buffer
     }
-    if (!have) break;
-    bar_c();   // the previous tile's buffers are free for the next phase A
-    t_prev = t;
   }
 }
 
@@ -520,7 +554,7 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   uint64_t strides[1] = {(uint64_t)(2 * s.h * 2)};
   uint32_t box[2] = {SF_C, SF_R};
   int rc = make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(s.h13), dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
+                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   SwiFwdParams p{};
   p.M = s.M; p.h = s.h;
@@ -540,12 +574,20 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   cudaError_t e;
   if (s.q_col) {
     auto k = swiglu_fwd_kernel<true>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SF_SMEM);
-    if (e == cudaSuccess) { count_launch(MX_KERNEL_SWIGLU_FWD); k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sf_smem(true));
+    if (e == cudaSuccess) {
+      count_launch(MX_KERNEL_SWIGLU_FWD);
+      k<<<grid, SF_THREADS, sf_smem(true), stream>>>(tm, p);
+      e = cudaGetLastError();
+    }
   } else {
     auto k = swiglu_fwd_kernel<false>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SF_SMEM);
-    if (e == cudaSuccess) { count_launch(MX_KERNEL_SWIGLU_FWD); k<<<grid, THREADS, SF_SMEM, stream>>>(tm, p); e = cudaGetLastError(); }
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sf_smem(false));
+    if (e == cudaSuccess) {
+      count_launch(MX_KERNEL_SWIGLU_FWD);
+      k<<<grid, SF_THREADS, sf_smem(false), stream>>>(tm, p);
+      e = cudaGetLastError();
+    }
   }
   return cuda_status(e, "swiglu_fwd_kernel launch");
 }
