@@ -48,6 +48,7 @@ struct QuantKParams {
   uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
   const float* amax;  // FP8 per-tensor mode: amax of each batch item
   int32_t tile_scales;  // MMA layout, tile-aligned: a tile's scales are one 512-byte tile per axis
+  int32_t v8_row, v8_col;  // code destinations 32-byte aligned: one 256-bit store per 32 codes
   int32_t* err;
 };
 
@@ -162,8 +163,7 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
         const bool in = r < p.rows && c < p.cols;
         if (in) {
           uint8_t* dst = qrow + r * p.qr_ld + c;
-          store16(dst, codes[0], codes[1], codes[2], codes[3]);
-          store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
+          store32_codes(dst, codes, p.v8_row);
           if (!TW && !p.tile_scales) sd.put(r, c >> 5, s);
         }
         if (p.tile_scales) srow_t[(rr & 31) * 16 + (rr >> 5) * 4 + box * 2 + jj] = in ? (uint8_t)s : 0;
@@ -196,10 +196,8 @@ __global__ void __launch_bounds__(QT_THREADS, 2)
           if constexpr (TW) tw_col32x2(v, ca, cb, splat_f32x2(tw_scale(p.amax[b])));
           else quant_col32x2(v, ca, cb, sa, sb, p.rceil);
           uint8_t* dst = qcol + cg * p.qc_ld + p.qc_off + rg;
-          store16(dst, ca[0], ca[1], ca[2], ca[3]);
-          store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
-          store16(dst + p.qc_ld, cb[0], cb[1], cb[2], cb[3]);
-          store16(dst + p.qc_ld + 16, cb[4], cb[5], cb[6], cb[7]);
+          store32_codes(dst, ca, p.v8_col);
+          store32_codes(dst + p.qc_ld, cb, p.v8_col);
           if (TW) {
           } else if (p.tile_scales) {
             scol_t[(cl & 31) * 16 + (cl >> 5) * 4 + rb] = (uint8_t)sa;
@@ -336,6 +334,14 @@ int launch_quant(const QuantLaunch& q, cudaStream_t stream) {
   // byte stores), the columnwise scale columns starting on a tile boundary
   p.tile_scales = (!q.tw && q.layout == MX_SCALE_MMA && colk == 1 && (p.sc_off & 3) == 0) ? 1 : 0;
   p.err = q.err;
+#ifndef MX_QT_V8
+#define MX_QT_V8 1
+#endif
+  auto a32 = [](const void* ptr, int64_t a, int64_t b, int64_t c) {
+    return ((reinterpret_cast<uintptr_t>(ptr) | (uintptr_t)a | (uintptr_t)b | (uintptr_t)c) & 31) == 0;
+  };
+  p.v8_row = MX_QT_V8 && q.q_row && a32(q.q_row, p.qr_ld, p.qr_bs, 0);
+  p.v8_col = MX_QT_V8 && q.q_col && a32(q.q_col, p.qc_ld, p.qc_off, p.qc_bs);
 
   const int64_t n_tiles = p.row_tiles * p.col_tiles * q.batch;
   if (n_tiles == 0) return MX_OK;

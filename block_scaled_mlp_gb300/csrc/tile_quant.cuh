@@ -220,4 +220,17 @@ MX_DEVINL void store16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d
   *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
 }
 
+// 32 bytes to global memory: one 256-bit store when v8 (dst 32-byte aligned),
+// else two 16-byte stores (dst 16-byte aligned)
+MX_DEVINL void store32_codes(uint8_t* dst, const uint32_t (&c)[8], bool v8) {
+  if (v8) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(c[0]), "r"(c[1]),
+                 "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]), "r"(c[7])
+                 : "memory");
+  } else {
+    store16(dst, c[0], c[1], c[2], c[3]);
+    store16(dst + 16, c[4], c[5], c[6], c[7]);
+  }
+}
+
 }  // namespace mx
