@@ -100,6 +100,7 @@ struct GemmParams {
   ScaleDst ysc;               // [hy, M/32] columnwise scales
   int64_t hy;                 // h
   uint32_t rceil;             // 1: RCEIL scales, 0: FLOOR
+  int32_t v8_y;               // yq rows 32-byte aligned: one 256-bit store per 32 codes
   const uint16_t* silu_a;     // a(g) = RN_bf16(g sigma(g)) indexed by the bits of bf16 g
   // FP8 per-tensor recipe: amax of A (one) and of B (one, or one per expert
   // when amax_b_per_expert); C = acc * (1/s_a) * (1/s_b), s = 448 / amax
@@ -723,7 +724,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           uint32_t codes[8];
           const uint32_t sc = quant_row32(yw, codes, p.rceil);
-          store32g(p.yq + row * p.hy + ycol + 32 * b, codes);
+          store32_codes(p.yq + row * p.hy + ycol + 32 * b, codes, p.v8_y);
           p.ys.put(row, (ycol >> 5) + b, sc);
           if (p.yqc) {
             // columns: the warp's 32 rows are one 32-row block of each of
@@ -1036,6 +1037,7 @@ int launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.ysc = ScaleDst{(uint8_t*)g.ys_col, (Sc + 3) / 4, Sc, 1};
   }
   p.rceil = g.floor_scale ? 0u : 1u;
+  p.v8_y = ((reinterpret_cast<uintptr_t>(g.yq) | (uintptr_t)(g.N / 2)) & 31) == 0;
   p.silu_a = g.silu_a;
   p.amax_a = g.amax_a;
   p.amax_b = g.amax_b;

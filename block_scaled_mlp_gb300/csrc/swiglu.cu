@@ -77,10 +77,6 @@ MX_DEVINL uint32_t quant_tile_block(const uint8_t* tile, int rr, int jj, uint32_
   return quant_row32(pk, codes, rceil);
 }
 
-MX_DEVINL void store32(uint8_t* dst, const uint32_t (&c)[8]) {
-  store16(dst, c[0], c[1], c[2], c[3]);
-  store16(dst + 16, c[4], c[5], c[6], c[7]);
-}
 
 // ---- forward: tile = 128 rows x 64 y-columns
 //
@@ -114,6 +110,7 @@ struct SwiFwdParams {
   uint8_t* q_col; ScaleDst s_col;
   uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
   const uint16_t* silu_a;  // a(g) = RN_bf16(g sigma(g)) indexed by the bits of bf16 g
+  int32_t v8_row;          // row codes 32-byte aligned: one 256-bit store per block
   int32_t* err;
 };
 
@@ -236,8 +233,7 @@ __global__ void __launch_bounds__(SF_THREADS, 2)
       if (r < p.M) {
         const int64_t c = c0 + jj * 32;
         uint8_t* dst = p.q_row + r * p.h + c;
-        store16(dst, codes[0], codes[1], codes[2], codes[3]);
-        store16(dst + 16, codes[4], codes[5], codes[6], codes[7]);
+        store32_codes(dst, codes, p.v8_row);
         p.s_row.put(r, c >> 5, sc);
       }
     }
@@ -287,6 +283,7 @@ struct SwiBwdParams {
   uint16_t* dh13_t;                 // [2h, M]
   uint16_t* y_t;                    // [h, M]
   uint32_t rceil;                   // 1: RCEIL scales, 0: FLOOR
+  int32_t v8_row, v8_col, v8_t;     // destinations 32-byte aligned: 256-bit stores
   int32_t* err;
 };
 
@@ -468,7 +465,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           const int64_t r = r0 + rr;
           const int64_t c = (which ? p.h : 0) + c0 + jj * 32;
           if (r < p.M) {
-            store32(p.q_row + r * 2 * p.h + c, codes);
+            store32_codes(p.q_row + r * 2 * p.h + c, codes, p.v8_row);
             p.s_row.put(r, c >> 5, sc);
           }
         }
@@ -487,10 +484,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (rg < p.M) {
           const int64_t orow = (which ? p.h : 0) + c0 + 2 * pc;
           uint8_t* dst = p.q_col + orow * p.M + rg;
-          store16(dst, ca[0], ca[1], ca[2], ca[3]);
-          store16(dst + 16, ca[4], ca[5], ca[6], ca[7]);
-          store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
-          store16(dst + p.M + 16, cb[4], cb[5], cb[6], cb[7]);
+          store32_codes(dst, ca, p.v8_col);
+          store32_codes(dst + p.M, cb, p.v8_col);
           p.s_col.put(orow, rg >> 5, sa);
           p.s_col.put(orow + 1, rg >> 5, sb);
         }
@@ -518,9 +513,13 @@ __global__ void __launch_bounds__(THREADS, 2)
               uint16_t* da = base + orow * p.M + rg;
               uint16_t* db = da + p.M;
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                store16(da + q4 * 8, wa[4 * q4], wa[4 * q4 + 1], wa[4 * q4 + 2], wa[4 * q4 + 3]);
-                store16(db + q4 * 8, wb[4 * q4], wb[4 * q4 + 1], wb[4 * q4 + 2], wb[4 * q4 + 3]);
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t ua[8] = {wa[8 * h2], wa[8 * h2 + 1], wa[8 * h2 + 2], wa[8 * h2 + 3],
+                                        wa[8 * h2 + 4], wa[8 * h2 + 5], wa[8 * h2 + 6], wa[8 * h2 + 7]};
+                const uint32_t ub[8] = {wb[8 * h2], wb[8 * h2 + 1], wb[8 * h2 + 2], wb[8 * h2 + 3],
+                                        wb[8 * h2 + 4], wb[8 * h2 + 5], wb[8 * h2 + 6], wb[8 * h2 + 7]};
+                store32_codes(reinterpret_cast<uint8_t*>(da + h2 * 16), ua, p.v8_t);
+                store32_codes(reinterpret_cast<uint8_t*>(db + h2 * 16), ub, p.v8_t);
               }
             }
           }
@@ -538,6 +537,11 @@ __global__ void __launch_bounds__(THREADS, 2)
 __global__ void silu_table_kernel(uint16_t* table) {
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < 65536u) table[b] = (uint16_t)swiglu_math::silu_bits_slow(__uint_as_float(b << 16));
+}
+
+// a device pointer and a row stride (bytes) that keep every 32-byte block 32-byte aligned
+bool aligned32(const void* ptr, int64_t stride) {
+  return ((reinterpret_cast<uintptr_t>(ptr) | (uintptr_t)stride) & 31) == 0;
 }
 
 }  // namespace
@@ -568,6 +572,7 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   p.silu_a = s.silu_a;
   p.err = s.err;
   if (!p.silu_a) return fail(MX_ERR_INVALID_ARG, "swiglu forward: the a(g) table is required");
+  p.v8_row = aligned32(s.q_row, s.h);
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
   if (n_tiles == 0) return MX_OK;
   const int grid = (int)std::min<int64_t>(n_tiles, (int64_t)num_sms() * 2);
@@ -621,6 +626,9 @@ int launch_swiglu_bwd(const SwigluLaunch& s, cudaStream_t stream) {
   p.dh13_t = (uint16_t*)s.dh13_t; p.y_t = (uint16_t*)s.y_t;
   p.rceil = s.floor_scale ? 0u : 1u;
   p.err = s.err;
+  p.v8_row = aligned32(s.q_row, 2 * s.h);
+  p.v8_col = s.q_col && aligned32(s.q_col, s.M);
+  p.v8_t = (!s.dh13_t || aligned32(s.dh13_t, 2 * s.M)) && (!s.y_t || aligned32(s.y_t, 2 * s.M));
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
   if (n_tiles == 0) return MX_OK;
   const int grid = (int)std::min<int64_t>(n_tiles, (int64_t)num_sms() * 2);
