@@ -110,7 +110,7 @@ struct SwiFwdParams {
   uint8_t* q_col; ScaleDst s_col;
   uint32_t rceil;  // 1: RCEIL scales, 0: FLOOR
   const uint16_t* silu_a;  // a(g) = RN_bf16(g sigma(g)) indexed by the bits of bf16 g
-  int32_t v8_row;          // row codes 32-byte aligned: one 256-bit store per block
+  int32_t v8_row, v8_col;  // codes 32-byte aligned: one 256-bit store per 32 codes
   int32_t* err;
 };
 
@@ -252,11 +252,11 @@ __global__ void __launch_bounds__(SF_THREADS, 2)
             },
             ca, cb, sa, sb, p.rceil);
         const int64_t rg = r0 + pr * 32;
+        uint32_t col[8];
+        col16x2_gather(ca, cb, rh, col);   // lane rh: column 2 pc + rh, all 32 rows
         if (rg < p.M) {
           const int64_t cg = c0 + 2 * pc;
-          uint8_t* dst = p.q_col + cg * p.M + rg + 16 * rh;
-          store16(dst, ca[0], ca[1], ca[2], ca[3]);
-          store16(dst + p.M, cb[0], cb[1], cb[2], cb[3]);
+          store32_codes(p.q_col + (cg + rh) * p.M + rg, col, p.v8_col);
           if (rh == 0) {
             p.s_col.put(cg, rg >> 5, sa);
             p.s_col.put(cg + 1, rg >> 5, sb);
@@ -573,6 +573,7 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   p.err = s.err;
   if (!p.silu_a) return fail(MX_ERR_INVALID_ARG, "swiglu forward: the a(g) table is required");
   p.v8_row = aligned32(s.q_row, s.h);
+  p.v8_col = s.q_col && aligned32(s.q_col, s.M);
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
   if (n_tiles == 0) return MX_OK;
   const int grid = (int)std::min<int64_t>(n_tiles, (int64_t)num_sms() * 2);

@@ -99,6 +99,19 @@ MX_DEVINL uint32_t quant_row32(const uint32_t (&p)[16], uint32_t (&codes)[8], ui
   return s;
 }
 
+// After quant_col16x2, lanes l (rh = 0: rows 0-15) and l ^ 16 (rh = 1:
+// rows 16-31) swap halves: lane rh = 0 ends with column A's 32 codes and
+// lane rh = 1 with column B's (rows in order), ready for one 32-byte store
+// each.  All 32 lanes take part.
+MX_DEVINL void col16x2_gather(const uint32_t (&ca)[4], const uint32_t (&cb)[4], int rh, uint32_t (&out)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t r = __shfl_xor_sync(0xFFFFFFFFu, rh ? ca[i] : cb[i], 16);
+    out[i] = rh ? r : ca[i];
+    out[4 + i] = rh ? cb[i] : r;
+  }
+}
+
 // Quantize 8 elements (4 packed bf16 pairs, element 2i in the low half) of a
 // row block spread over 4 consecutive lanes.  Returns the 8 codes as two
 // 32-bit words (element 0 in the lowest byte) and the block scale byte.
