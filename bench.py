@@ -128,12 +128,15 @@ def bind_to_gpu_cpus(dev):
         p = torch.cuda.get_device_properties(dev)
         bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
         cpus = _cpulist(open(f"/sys/bus/pci/devices/{bus}/local_cpulist").read())
-        if cpus and len(cpus) < len(os.sched_getaffinity(0)):
+        if not cpus:
+            return None
+        if len(cpus) < len(os.sched_getaffinity(0)):
             os.sched_setaffinity(0, cpus)
-            return f"{min(cpus)}-{max(cpus)}" if max(cpus) - min(cpus) + 1 == len(cpus) else sorted(cpus)
+        # reported also when the process already runs on exactly these CPUs
+        # (a box with one NUMA node: nothing to bind)
+        return f"{min(cpus)}-{max(cpus)}" if max(cpus) - min(cpus) + 1 == len(cpus) else sorted(cpus)
     except Exception:
         return None
-    return None
 
 
 def max_over_ranks(ms: float, world: int, dev) -> float:
