@@ -3,11 +3,14 @@ configuration bench.py times): the Llama-3-8B FFN (dense, wgrad_with_hp)
 and the two routed-expert MoE layers (grouped, default recipe).
 
 The oracle cannot redo these steps whole on the host, so it recomputes
-sampled outputs one by one from the same inputs: sampled entries of h13,
-out and dx, and sampled weight-gradient entries, each to the normwise 2e-3
-bar against fp64 accumulation; the quantized activations it needs along the
-way are recomputed from the GPU's own h13 (stage-wise, as in the small
-tests).  Padding rows must be exact zeros."""
+sampled outputs one by one from the same inputs: per sampled group (the
+smallest, the median and the largest non-empty expert; the whole matrix
+for the dense layer) 32 rows x 128 columns of h13, out and dx, and 32 x 64
+entries of each weight gradient over the group's tokens, each to the
+normwise 2e-3 bar against fp64 accumulation; the quantized activations it
+needs along the way are recomputed from the GPU's own h13 (stage-wise, as
+in the small tests).  Padding rows must be exact zeros, and so must an
+empty expert's weight gradients."""
 import numpy as np
 import pytest
 import torch
@@ -53,35 +56,42 @@ def test_full_size_sampled(name):
     torch.cuda.synchronize()
     err.check()
     h13_gpu = ctx.h13()
-    x, dout = inp["x"], inp["dout"]
-    M, d = x.shape
-    h = inp["w1"].shape[-2]
-    rng = np.random.default_rng(7)
-
-    # the group (expert) whose rows and weight gradients are sampled: the
-    # non-empty group of median size (keeps the host-side work bounded)
     if grouped:
         bounds = o.group_bounds(inp["offs"])
-        live = [(b - a, i) for i, (a, b) in enumerate(bounds) if b > a]
-        live.sort()
-        e = live[len(live) // 2][1]
-        s0, s1 = bounds[e]
-        W1, W3, W2 = inp["w1"][e], inp["w3"][e], inp["w2"][e]
         real = inp["real_rows"]
         assert not bits(out)[~real].any() and not bits(dx)[~real].any(), "padding rows must be zero"
         assert not bits(out)[int(inp["offs"][-1]):].any()
         for ee, (a, b) in enumerate(bounds):
             if a == b:
                 assert not bits(dw1[ee]).any() and not bits(dw2[ee]).any(), "empty expert"
+        # the groups (experts) whose rows and weight gradients are sampled:
+        # the smallest, the median and the largest non-empty group
+        live = sorted((b - a, i) for i, (a, b) in enumerate(bounds) if b > a)
+        groups = sorted({live[0][1], live[len(live) // 2][1], live[-1][1]})
     else:
-        e, s0, s1 = 0, 0, M
+        groups = [0]
+    for e in groups:
+        _check_group(e, inp, grouped, hp, h13_gpu, out, dx, dw1, dw3, dw2, np.random.default_rng(7 + e))
+
+
+def _check_group(e, inp, grouped, hp, h13_gpu, out, dx, dw1, dw3, dw2, rng):
+    """Sampled entries of h13, out, dx (rows of group e) and of expert e's
+    weight gradients against the oracle, each to the normwise bar."""
+    x, dout = inp["x"], inp["dout"]
+    M, d = x.shape
+    h = inp["w1"].shape[-2]
+    if grouped:
+        s0, s1 = o.group_bounds(inp["offs"])[e]
+        W1, W3, W2 = inp["w1"][e], inp["w3"][e], inp["w2"][e]
+    else:
+        s0, s1 = 0, M
         W1, W3, W2 = inp["w1"], inp["w3"], inp["w2"]
     real_rows = np.arange(s0, s1)
     if grouped:
         real_rows = real_rows[inp["real_rows"][s0:s1]]
-    R = np.sort(rng.choice(real_rows, 8, replace=False))
-    J = np.sort(rng.choice(2 * h, 64, replace=False))
-    Jd = np.sort(rng.choice(d, 64, replace=False))
+    R = np.sort(rng.choice(real_rows, min(32, len(real_rows)), replace=False))
+    J = np.sort(rng.choice(2 * h, 128, replace=False))
+    Jd = np.sort(rng.choice(d, 128, replace=False))
     W13 = np.concatenate([W1, W3], axis=0)
 
     # F3: h13[R, J]
@@ -89,7 +99,7 @@ def test_full_size_sampled(name):
     wq, ws = _row_q(W13[J])
     ref = o.mx_mm(xq, xs, wq, ws)
     h13_s = bits(h13_gpu[torch.as_tensor(R, device="cuda")][:, torch.as_tensor(J, device="cuda")])
-    assert o.normwise_rel_err(o.bf16_to_f64(h13_s), ref) <= TOL
+    assert o.normwise_rel_err(o.bf16_to_f64(h13_s), ref) <= TOL, ("h13", e)
 
     # F4 + F6: out[R, Jd] from the GPU's h13 rows
     h13_R = bits(h13_gpu[torch.as_tensor(R, device="cuda")])
@@ -98,7 +108,7 @@ def test_full_size_sampled(name):
     w2q, w2s = _row_q(W2[Jd])
     ref = o.mx_mm(yq, ys, w2q, w2s)
     out_s = bits(out)[R][:, Jd]
-    assert o.normwise_rel_err(o.bf16_to_f64(out_s), ref) <= TOL
+    assert o.normwise_rel_err(o.bf16_to_f64(out_s), ref) <= TOL, ("out", e)
 
     # B2 + B4 + B5: dx[R, Jd]
     dq, ds = _row_q(dout[R])
@@ -109,15 +119,15 @@ def test_full_size_sampled(name):
     w13qc, w13sc = _row_q(W13.T[Jd])                 # rows Jd of the columnwise w13
     ref = o.mx_mm(dhq, dhs, w13qc, w13sc)
     dx_s = bits(dx)[R][:, Jd]
-    assert o.normwise_rel_err(o.bf16_to_f64(dx_s), ref) <= TOL
+    assert o.normwise_rel_err(o.bf16_to_f64(dx_s), ref) <= TOL, ("dx", e)
 
     # B3 / B6: sampled weight-gradient entries over the group's tokens
-    # (a few hundred entries each, so that the normwise bar is not dominated
-    # by the bf16 rounding of a handful of values)
-    I2 = np.sort(rng.choice(d, 16, replace=False))   # rows of dw2
-    J2 = np.sort(rng.choice(h, 32, replace=False))   # cols of dw2
-    I1 = np.sort(rng.choice(h, 16, replace=False))   # rows of dw1 / dw3
-    J1 = np.sort(rng.choice(d, 32, replace=False))
+    # (a thousand or more entries each, so that the normwise bar is not
+    # dominated by the bf16 rounding of a handful of values)
+    I2 = np.sort(rng.choice(d, 32, replace=False))   # rows of dw2
+    J2 = np.sort(rng.choice(h, 64, replace=False))   # cols of dw2
+    I1 = np.sort(rng.choice(h, 32, replace=False))   # rows of dw1 / dw3
+    J1 = np.sort(rng.choice(d, 64, replace=False))
     tok = slice(s0, s1)
     h13_cols = bits(h13_gpu[s0:s1])                   # [T, 2h] of the group
     g_all, u_all = o.split_h13(h13_cols)
@@ -130,7 +140,7 @@ def test_full_size_sampled(name):
         bq, bs = o.quantize_cols(y_cols)
         ref2 = o.mx_mm(aq, as_, bq, bs)
     dw2_s = bits(dw2[e] if grouped else dw2)[I2][:, J2]
-    assert o.normwise_rel_err(o.bf16_to_f64(dw2_s), ref2) <= TOL
+    assert o.normwise_rel_err(o.bf16_to_f64(dw2_s), ref2) <= TOL, ("dw2", e)
 
     # dh13 columns I1 (dg) and h + I1 (du) for all tokens of the group
     dqg, dsg = _row_q(dout_g)
@@ -146,4 +156,4 @@ def test_full_size_sampled(name):
             bq, bs = o.quantize_cols(x_g[:, J1])
             ref1 = o.mx_mm(aq, as_, bq, bs)
         got = bits(dw[e] if grouped else dw)[I1][:, J1]
-        assert o.normwise_rel_err(o.bf16_to_f64(got), ref1) <= TOL, name_w
+        assert o.normwise_rel_err(o.bf16_to_f64(got), ref1) <= TOL, (name_w, e)
