@@ -208,7 +208,6 @@ MX_DEVINL uint32_t silu_bits_from(float g, const SigFast& f) {
   return silu_bits_slow(g);
 }
 
-MX_DEVINL uint32_t silu_bits(float g) { return silu_bits_from(g, sig_fast(g)); }
 
 // dg by fp64 with exact-tie handling (see the comment inside).
 __device__ __noinline__ uint32_t dg_bits_fp64(float dyf, float g, float u) {

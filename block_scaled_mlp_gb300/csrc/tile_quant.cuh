@@ -1,10 +1,10 @@
 // tile_quant.cuh - MXFP8 block quantization of bf16 values held in registers,
 // used by the standalone cast kernel and by the fused SwiGLU kernels.
 //
-// Row blocks: one thread holds a whole 32-element block (quant_row32), or
-// four consecutive lanes each hold 8 of its elements (quant_row8).  Column
-// blocks: one thread holds the 32 elements of two adjacent columns as packed
-// pairs.  Scaling by the power-of-two inverse scale is exact; the E4M3
+// Row blocks: one thread holds a whole 32-element block (quant_row32).
+// Column blocks: one thread holds the 32 elements of two adjacent columns as
+// packed pairs (quant_col32x2), or lanes l and l ^ 16 hold 16 rows each
+// (quant_col16x2).  Scaling by the power-of-two inverse scale is exact; the E4M3
 // conversion rounds to nearest even and saturates.
 #pragma once
 
@@ -110,30 +110,6 @@ MX_DEVINL void col16x2_gather(const uint32_t (&ca)[4], const uint32_t (&cb)[4], 
     out[i] = rh ? r : ca[i];
     out[4 + i] = rh ? cb[i] : r;
   }
-}
-
-// Quantize 8 elements (4 packed bf16 pairs, element 2i in the low half) of a
-// row block spread over 4 consecutive lanes.  Returns the 8 codes as two
-// 32-bit words (element 0 in the lowest byte) and the block scale byte.
-MX_DEVINL uint2 quant_row8(const uint32_t (&p)[4], uint32_t& scale_out, uint32_t rceil = 1u) {
-  uint32_t m2 = max2(max2(abs2(p[0]), abs2(p[1])), max2(abs2(p[2]), abs2(p[3])));
-  m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
-  m2 = max2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 2));
-  const uint32_t s = e8m0_from_amax_bits(max_halves(m2), rceil);
-  scale_out = s;
-  uint2 out;
-  if (s == 0xFF) {
-    out.x = out.y = 0x7F7F7F7Fu;
-    return out;
-  }
-  const float inv = inv_scale_from_e8m0(s);
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    c[i] = cvt_e4m3x2(bf16_lo(p[i]) * inv, bf16_hi(p[i]) * inv);
-  out.x = c[0] | (c[1] << 16);
-  out.y = c[2] | (c[3] << 16);
-  return out;
 }
 
 // Quantize two 32-element column blocks held by one thread as 32 packed
