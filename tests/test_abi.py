@@ -89,6 +89,7 @@ def test_mlp_workspace_and_validation(L):
     assert L.mx_mlp_workspace_size(256, 256, 512, 0, 1, ctypes.byref(c2), ctypes.byref(s2)) == 0
     p = _fake()
     assert L.mx_mlp_fwd(p, p, p, p, 200, 256, 512, None, 0, 128, 0, p, p, p, None, None) == 4
+    assert L.mx_mlp_fwd(p, p, p, p, 0, 256, 512, None, 0, 128, 0, p, p, p, None, None) == 1   # no rows
     assert L.mx_mlp_fwd(p, p, p, p, 256, 256, 512, p, 4, 128, 9, p, p, p, None, None) == 1
     assert L.mx_mlp_bwd(p, None, p, p, p, p, 256, 256, 512, None, 0, 128, 0, p, p, p, p, p, None, None) == 1
 

@@ -305,3 +305,41 @@ def test_fused_forward_equals_op_chain(kind, recipe):
     for name, a, b in [("out", out, ch["out"]), ("dx", dx, ch["dx"]), ("dw1", dw1, ch["dw1"]),
                        ("dw3", dw3, ch["dw3"]), ("dw2", dw2, ch["dw2"])]:
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("recipe", [mx.RECIPE_RCEIL, mx.RECIPE_RCEIL_WGRAD_HP])
+def test_all_experts_empty(recipe):
+    """Every group empty (offs all zero), 128 tail rows holding non-zero x:
+    the output, the input gradient and every expert's weight gradients are
+    exact zeros."""
+    inp, t, offs = _inputs_grouped_tail([0, 0, 0, 0], 256, 256, seed=21, tail=128)
+    inp["dout"][:] = synth.normal_bf16(inp["dout"].shape, 1.0, 22)
+    t["dout"] = to_dev(inp["dout"])
+    err = mx.ErrorWord()
+    out, ctx = mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], offs=offs, recipe=recipe, err=err)
+    dx, dw1, dw3, dw2 = mx.mlp_bwd(ctx, t["dout"], err=err)
+    torch.cuda.synchronize()
+    err.check()
+    for name, a in (("out", out), ("dx", dx), ("dw1", dw1), ("dw3", dw3), ("dw2", dw2)):
+        assert not bits(a).any(), name
+
+
+@pytest.mark.parametrize("recipe", [mx.RECIPE_RCEIL, mx.RECIPE_RCEIL_WGRAD_HP])
+def test_single_expert_equals_dense(recipe):
+    """One expert holding every row (E = 1, no padding) is the dense layer:
+    the grouped forms give the dense forms' outputs and gradients bit for
+    bit (the same products summed in the same order)."""
+    M, d, h = 256, 256, 384
+    inp, t, _ = _inputs_dense(M, d, h, seed=23)
+    offs = to_dev(np.array([M], dtype=np.int32), torch.int32)
+    err = mx.ErrorWord()
+    out_d, ctx_d = mx.mlp_fwd(t["x"], t["w1"], t["w3"], t["w2"], recipe=recipe, err=err)
+    grads_d = mx.mlp_bwd(ctx_d, t["dout"], err=err)
+    w1g, w3g, w2g = (t[k].unsqueeze(0).contiguous() for k in ("w1", "w3", "w2"))
+    out_g, ctx_g = mx.mlp_fwd(t["x"], w1g, w3g, w2g, offs=offs, recipe=recipe, err=err)
+    grads_g = mx.mlp_bwd(ctx_g, t["dout"], err=err)
+    torch.cuda.synchronize()
+    err.check()
+    assert np.array_equal(bits(out_g), bits(out_d))
+    for name, a, b in zip(("dx", "dw1", "dw3", "dw2"), grads_g, grads_d):
+        assert np.array_equal(bits(a).reshape(bits(b).shape), bits(b)), name
