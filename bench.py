@@ -300,31 +300,39 @@ def run_gpu(args, rank, world, dev):
                           128, recipe, P(scratch), P(r[1]), P(r[2]), P(r[3]), P(r[4]), err.ptr(), mx._stream())
         mx._check(rc)
 
+    def pipelined(n):
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        upload(0)
+        for i in range(n):
+            k = i % 2
+            if i + 1 < n:
+                if i >= 1:
+                    up.wait_event(in_free[(i + 1) % 2])    # step i-1 no longer reads that buffer
+                upload((i + 1) % 2)
+            stream.wait_event(in_ready[k])
+            if i >= 2:
+                stream.wait_event(out_free[k])              # step i-2's results are down
+            step_into(xin[k][0], xin[k][1], res_dev[k])
+            in_free[k].record(stream)
+            out_ready[k].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(out_ready[k])
+                for hdst, dsrc in zip(res_host, res_dev[k]):
+                    hdst.copy_(dsrc, non_blocking=True)
+                out_free[k].record(down)
+        stream.wait_stream(down)
+
+    # untimed passes of the same pipeline first, so that the timed region
+    # does not hold the first copies through freshly allocated pinned buffers
+    pipelined(max(2, min(args.warmup, 3)))
+    torch.cuda.synchronize(dev)
+    err.check()
     barrier()
     torch.cuda.synchronize(dev)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    up.wait_stream(stream)
-    down.wait_stream(stream)
-    upload(0)
-    for i in range(args.steps):
-        k = i % 2
-        if i + 1 < args.steps:
-            if i >= 1:
-                up.wait_event(in_free[(i + 1) % 2])    # step i-1 no longer reads that buffer
-            upload((i + 1) % 2)
-        stream.wait_event(in_ready[k])
-        if i >= 2:
-            stream.wait_event(out_free[k])              # step i-2's results are down
-        step_into(xin[k][0], xin[k][1], res_dev[k])
-        in_free[k].record(stream)
-        out_ready[k].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(out_ready[k])
-            for hdst, dsrc in zip(res_host, res_dev[k]):
-                hdst.copy_(dsrc, non_blocking=True)
-            out_free[k].record(down)
-    stream.wait_stream(down)
+    pipelined(args.steps)
     a1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
