@@ -272,7 +272,7 @@ def run_gpu(args, rank, world, dev):
     # copies its inputs (x, dout) in from pinned host memory and all of its
     # results (out, dx, dw1, dw3, dw2) back; the weights stay resident.
     # Double-buffered like a training input pipeline: step i+1's inputs go
-    # up on one copy stream and step i-1's results come down on another
+    # up on one copy stream and earlier steps' results come down on another
     # while step i computes; the timed region spans the first upload to the
     # last download.
     host_cpus = bind_to_gpu_cpus(dev)
@@ -283,19 +283,25 @@ def run_gpu(args, rank, world, dev):
     xin = [(torch.empty_like(t["x"]), torch.empty_like(t["dout"])) for _ in range(2)]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
-    in_ready, in_free = [ev(), ev()], [ev(), ev()]
-    out_ready, out_free = [ev(), ev()], [ev(), ev()]
+    x_ready, dout_ready, in_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    fwd_done, out_ready, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
     def upload(k):
         with torch.cuda.stream(up):
             xin[k][0].copy_(hx, non_blocking=True)
+            x_ready[k].record(up)
             xin[k][1].copy_(hd, non_blocking=True)
-            in_ready[k].record(up)
+            dout_ready[k].record(up)
 
-    def step_into(x, dout, r):
+    def step_into(k, r):
+        # the forward needs x only; dout may still be on its way up
+        x, dout = xin[k]
+        stream.wait_event(x_ready[k])
         rc = L.mx_mlp_fwd(P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1), 128, recipe,
                           P(ctx), P(scratch), P(r[0]), err.ptr(), mx._stream())
         mx._check(rc)
+        fwd_done[k].record(stream)
+        stream.wait_event(dout_ready[k])
         rc = L.mx_mlp_bwd(P(ctx), P(dout), P(x), P(t["w1"]), P(t["w3"]), P(t["w2"]), M, d, h, P(offs), max(E, 1),
                           128, recipe, P(scratch), P(r[1]), P(r[2]), P(r[3]), P(r[4]), err.ptr(), mx._stream())
         mx._check(rc)
@@ -310,15 +316,18 @@ def run_gpu(args, rank, world, dev):
                 if i >= 1:
                     up.wait_event(in_free[(i + 1) % 2])    # step i-1 no longer reads that buffer
                 upload((i + 1) % 2)
-            stream.wait_event(in_ready[k])
             if i >= 2:
                 stream.wait_event(out_free[k])              # step i-2's results are down
-            step_into(xin[k][0], xin[k][1], res_dev[k])
+            step_into(k, res_dev[k])
             in_free[k].record(stream)
             out_ready[k].record(stream)
             with torch.cuda.stream(down):
+                # out leaves as soon as the forward has written it, the
+                # gradients once the backward is done
+                down.wait_event(fwd_done[k])
+                res_host[0].copy_(res_dev[k][0], non_blocking=True)
                 down.wait_event(out_ready[k])
-                for hdst, dsrc in zip(res_host, res_dev[k]):
+                for hdst, dsrc in zip(res_host[1:], res_dev[k][1:]):
                     hdst.copy_(dsrc, non_blocking=True)
                 out_free[k].record(down)
         stream.wait_stream(down)
