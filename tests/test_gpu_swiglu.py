@@ -146,3 +146,42 @@ def test_swiglu_bwd_extreme_inputs():
     vnan = np.isnan(o.bf16_to_f64(dh13))
     assert np.array_equal(np.isnan(o.bf16_to_f64(got)), vnan)
     assert np.array_equal(got[~vnan], dh13[~vnan])
+
+
+@pytest.mark.parametrize("form", ["rows", "rows+cols", "hp"])
+def test_swiglu_bwd_every_element_open(form):
+    """Every g outside the fast path's range (|g| > 64) in the first row
+    tiles, so every element of those tiles goes to the exact tiers: 4096
+    open elements per 64x64 tile against a queue of 1024, the rest resolved
+    in place by the consumers that found them.  The last row tile mixes
+    open and certified elements.  All three output forms against the
+    oracle, bit for bit."""
+    M, h = 192, 128
+    rng = np.random.default_rng(41)
+    g = rng.choice([-1.0, 1.0], (M, h)) * rng.uniform(64.5, 3000.0, (M, h))
+    g[-64:, ::2] = rng.standard_normal((64, h // 2))
+    g[0, :2] = [-100.0, 88.75]
+    u = rng.standard_normal((M, h)) * 2.0
+    dy = rng.standard_normal((M, h))
+    h13 = np.concatenate([o.round_to_bf16_bits(g), o.round_to_bf16_bits(u)], axis=1)
+    dyb = o.round_to_bf16_bits(dy)
+    axis = mx.BOTH if form == "rows+cols" else mx.ROW
+    res = mx.swiglu_quant_bwd(to_dev(dyb), to_dev(h13), axis, mx.SCALE_MMA, bf16_transposed=form == "hp")
+    torch.cuda.synchronize()
+    dh13, y = _bwd_ref(dyb, h13)
+    q, s = o.quantize_rows(dh13)
+    assert np.array_equal(u8(res["q_row"]), q)
+    assert np.array_equal(u8(res["s_row"]), o.scales_to_mma(s))
+    if form == "rows+cols":
+        qc, sc = o.quantize_cols(dh13)
+        assert np.array_equal(u8(res["q_col"]), qc)
+        assert np.array_equal(u8(res["s_col"]), o.scales_to_mma(sc))
+    if form == "hp":
+        got = bits(res["dh13_t"]).T
+        vnan = np.isnan(o.bf16_to_f64(dh13))
+        assert np.array_equal(np.isnan(o.bf16_to_f64(got)), vnan)
+        assert np.array_equal(got[~vnan], dh13[~vnan])
+        gy = bits(res["y_t"]).T
+        ynan = np.isnan(o.bf16_to_f64(y))
+        assert np.array_equal(np.isnan(o.bf16_to_f64(gy)), ynan)
+        assert np.array_equal(gy[~ynan], y[~ynan])
