@@ -85,7 +85,7 @@ MX_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   }
 }
 
-// The same wait by every lane of a warp, with one verdict for all of them
+// The same wait by every lane of a warp, with one outcome for all of them
 // (a lane that saw the bound expire makes the whole warp give up).
 MX_DEVINL bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   const bool ok = mbar_wait(bar, parity, err);

@@ -330,7 +330,7 @@ MX_DEVINL SigFast2 sig_fast2(f2 G) {
 // lies in an interval around the fp32 fast value that covers the fast
 // chain's error, and both ends of the interval round to the same bf16
 // (rounding is monotone, so everything between them does too).  A failing
-// lane leaves a nonzero half, so the per-lane verdicts need no recomputation.
+// lane leaves a nonzero half, so the per-lane decisions need no recomputation.
 
 // RN_f32 of the products of the bf16 halves of a and b (lane 0 from the low
 // halves): exact in fp32's range (8 x 8 significant bits), computed by the
