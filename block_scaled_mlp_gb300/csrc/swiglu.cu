@@ -96,12 +96,24 @@ constexpr int SF_BOX = SF_R * SF_C * 2;       // 16 KB
 constexpr int SF_STAGE_BYTES = 2 * SF_BOX;    // g, u
 constexpr int SF_WARPS = 8;                   // consumer warps
 constexpr int SF_THREADS = (SF_WARPS + 1) * 32;
-// Shared memory per mode: the stages, plus 16 KB of y staging in dual mode.
-// The rest of the SM's 256 KB stays L1, where the a(g) table lookups hit:
-// at 8192 x 8192 the rowwise kernel ran 0.067 ms with this size against
-// 0.076 ms with 32 KB more, and the dual one 0.104 ms with one staging
-// buffer (and a second pair barrier per tile) against 0.111 ms with two.
-constexpr size_t sf_smem(bool col) { return SF_STAGES * SF_STAGE_BYTES + (col ? 4 * 32 * 128 : 0) + 1024 + 64; }
+// Shared memory per mode: the stages, plus 16 KB of y staging in dual mode,
+// plus 64 bytes of barriers and flags; no static shared memory and no
+// alignment slack (the dynamic region is declared 1024-aligned, which the
+// kernel checks).  The rest of the SM's 256 KB stays L1, where the a(g)
+// table lookups hit: two CTAs need 130.1 KB (rows) and 162.1 KB (dual)
+// with the 1 KB each reserves, inside the 132 KB and 164 KB shared-memory
+// configurations.  At 8192 x 8192 the rowwise kernel ran 0.067 ms with 1
+// KB of slack and 1 KB of static flags per CTA against 0.076 ms with 32 KB
+// more, and the dual one 0.104 ms with one staging buffer (and a second
+// pair barrier per tile) against 0.111 ms with two.
+constexpr size_t sf_smem(bool col) { return SF_STAGES * SF_STAGE_BYTES + (col ? 4 * 32 * 128 : 0) + 64; }
+// Preferred shared-memory carveout (percent of the SM's maximum), which
+// picks the shared-memory configuration and so the L1 left for the table.
+// Swept at 8192 x 8192: rows 58.0-58.6 us at 50-70% (60.2 at the driver's
+// default and at 72-85%, 66.9 at 100%, 70.9 below 50% where one CTA per SM
+// fits); dual 84.5-84.7 us at 58-70% (87 at 72-85%, 102 below 58%).  The
+// middle of each range:
+constexpr int sf_carveout(bool col) { return col ? 64 : 55; }
 
 struct SwiFwdParams {
   int64_t M, h;
@@ -146,11 +158,18 @@ template <bool COL>
 __global__ void __launch_bounds__(SF_THREADS, 2)
     swiglu_fwd_kernel(const __grid_constant__ CUtensorMap tmh, SwiFwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // the 128-byte-swizzled TMA boxes need a 1024-byte aligned base; the
+  // launch sizes no slack for rounding up, so a misaligned base is reported
+  // and the CTA does nothing
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_error(p.err, MX_ERR_ALIGNMENT);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* ybuf = smem + SF_STAGES * SF_STAGE_BYTES;   // dual: [4 warp pairs][4 KB]
   uint64_t* full = reinterpret_cast<uint64_t*>(ybuf + (COL ? 4 * SF_PAIR_BYTES : 0));
   uint64_t* empty = full + SF_STAGES;
-  __shared__ int s_dead;
+  int& s_dead = *reinterpret_cast<int*>(empty + SF_STAGES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n_tiles = p.row_tiles * p.col_tiles;
 
@@ -581,6 +600,7 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   if (s.q_col) {
     auto k = swiglu_fwd_kernel<true>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sf_smem(true));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, sf_carveout(true));
     if (e == cudaSuccess) {
       count_launch(MX_KERNEL_SWIGLU_FWD);
       k<<<grid, SF_THREADS, sf_smem(true), stream>>>(tm, p);
@@ -589,6 +609,7 @@ int launch_swiglu_fwd(const SwigluLaunch& s, cudaStream_t stream) {
   } else {
     auto k = swiglu_fwd_kernel<false>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sf_smem(false));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, sf_carveout(false));
     if (e == cudaSuccess) {
       count_launch(MX_KERNEL_SWIGLU_FWD);
       k<<<grid, SF_THREADS, sf_smem(false), stream>>>(tm, p);
