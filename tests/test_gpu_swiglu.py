@@ -49,6 +49,28 @@ def test_silu_table_every_bf16_input_exact():
     assert not mism.any(), f"{mism.sum()} mismatches, e.g. g bits {g[mism][:8]}"
 
 
+@pytest.mark.parametrize("axis", ["rows", "both"])
+def test_swiglu_fwd_every_bf16_g(axis):
+    """The forward kernel on all 65536 bf16 patterns of g (u = 1, so y =
+    a(g)): the part of the table the kernel keeps in shared memory, the
+    global lookups outside it and the patterns at its edges all give the
+    oracle's codes and scales, rows and columns."""
+    M, h = 512, 128
+    g = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(M, h)
+    h13 = np.concatenate([g, np.full((M, h), 0x3F80, dtype=np.uint16)], axis=1)
+    ax = mx.BOTH if axis == "both" else mx.ROW
+    res = mx.swiglu_quant(to_dev(h13), ax, mx.SCALE_MMA)
+    torch.cuda.synchronize()
+    y = o.swiglu_fwd(g, h13[:, h:])
+    q, s = o.quantize_rows(y)
+    assert np.array_equal(u8(res["q_row"]), q)
+    assert np.array_equal(u8(res["s_row"]), o.scales_to_mma(s))
+    if axis == "both":
+        qc, sc = o.quantize_cols(y)
+        assert np.array_equal(u8(res["q_col"]), qc)
+        assert np.array_equal(u8(res["s_col"]), o.scales_to_mma(sc))
+
+
 @pytest.mark.parametrize("M,h", [(256, 512), (384, 192), (128, 64)])
 def test_swiglu_fwd_dual_matches_oracle(M, h):
     h13 = _h13(M, h, seed=M + h)
