@@ -149,6 +149,16 @@ def max_over_ranks(ms: float, world: int, dev) -> float:
     return float(t.item())
 
 
+def workload_config(name, w, world):
+    """The line's `config`: the workload and its sizes (both arms print it)."""
+    d, h = w["d"], w["h"]
+    E = 0 if w["kind"] == "dense" else int(w["E"])
+    return {"workload": name, "M_total": int(w["M_total"]), "tokens": int(w["tokens"]), "d": d, "h": h,
+            "E": E or None, "recipe": w["recipe"], "flops_per_step": w["flops"],
+            "l2": f"inputs larger than L2 (weights {3 * d * h * 2 * max(E, 1) / 1e6:.0f} MB bf16)",
+            "parallelism": f"replicas x{world}"}
+
+
 def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
     return flops_per_rank * world / (ms_max * 1e-3) / 1e12
 
@@ -389,10 +399,7 @@ def run_gpu(args, rank, world, dev):
         "vs_baseline": None,
         "dtype": "mxfp8-e4m3 (fp32 accumulate)" + (" + bf16 wgrad" if recipe else ""),
         "data": "synthetic (seeded; bf16 N(0,1) activations, N(0,0.02) weights)",
-        "config": {"workload": args.workload, "M_total": M, "tokens": w["tokens"], "d": d, "h": h, "E": E or None,
-                   "recipe": w["recipe"], "flops_per_step": w["flops"],
-                   "l2": f"inputs larger than L2 (weights {3 * d * h * 2 * max(E, 1) / 1e6:.0f} MB bf16)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, w, world),
         "roofline": roofline,
         "quant_swiglu": {"achieved_gbs": round(mem_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                          "frac": round(mem_gbs / peaks["hbm_gbs"], 4),
@@ -699,7 +706,7 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def run_reference(args):
+def run_reference(args, world=1):
     w, inp = make_workload(args.workload)
     tokens, hidden = 64, 512
     for _ in range(args.warmup):
@@ -716,7 +723,7 @@ def run_reference(args):
         "metric": "MXFP8 MLP fwd+bwd TFLOP/s",
         "value": value,
         "unit": "TFLOP/s",
-        "n_gpus": 1,
+        "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": tot_t / args.steps * 1e3,
@@ -725,7 +732,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64 (exact MXFP8 oracle)",
         "data": "synthetic",
-        "config": {"workload": args.workload},
+        "config": workload_config(args.workload, w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -958,7 +965,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)))
+            print(json.dumps(run_reference(args, world)))
         return
 
     dev = torch.device("cuda", local)
