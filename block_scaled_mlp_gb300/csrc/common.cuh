@@ -423,11 +423,6 @@ MX_DEVINL uint32_t e8m0_from_amax_bits(uint32_t amax_bits, uint32_t rceil = 1u) 
   return s < 0 ? 0u : (uint32_t)s;
 }
 
-// 2^-(s-127) as an fp32 (exact; s <= 247 for finite blocks).
-MX_DEVINL float inv_scale_from_e8m0(uint32_t s) {
-  return __uint_as_float((uint32_t)(254 - (int)s) << 23);
-}
-
 // Two fp32 -> packed E4M3 pair (RNE, saturating), lo in the low byte.
 MX_DEVINL uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -436,7 +431,6 @@ MX_DEVINL uint32_t cvt_e4m3x2(float lo, float hi) {
 }
 
 MX_DEVINL float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
-MX_DEVINL float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
 
 MX_DEVINL uint32_t f32_to_bf16_bits(float f) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
