@@ -224,6 +224,8 @@ def run_gpu(args, rank, world, dev):
     recipe = mx.RECIPE_RCEIL_WGRAD_HP if w["recipe"] == "wgrad_hp" else mx.RECIPE_RCEIL
     t = {k: to_dev(inp[k], dev) for k in ("x", "w1", "w3", "w2", "dout")}
     offs = None if inp["offs"] is None else torch.from_numpy(inp["offs"]).to(dev)
+    if rank != 0 or args.no_cpu_baseline:
+        inp = None   # the host copies serve only rank 0's CPU-baseline sample
     M, d, h = w["M_total"], w["d"], w["h"]
     E = 0 if offs is None else offs.numel()
     cb, sb = mx.mlp_workspace_size(M, d, h, E, recipe)
