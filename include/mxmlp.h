@@ -31,9 +31,14 @@
  *   There is no fallback path: unsupported shapes return
  *   MX_ERR_UNSUPPORTED.
  * - Faults found on the device (non-monotone or unaligned group offsets, a
- *   pipeline wait that exceeded its bound) are OR-ed as mx_status bits into
- *   the caller's `err_word` (int32, device memory; may be NULL where noted)
- *   and the kernel skips the faulty work instead of trapping.
+ *   pipeline wait that exceeded its bound, a shared-memory base without the
+ *   1024-byte alignment the swizzled copies need) are OR-ed as mx_status
+ *   bits into the caller's `err_word` (int32, device memory; may be NULL
+ *   where noted) and the kernel skips the faulty work instead of trapping.
+ *   Calls without an `err_word` (mx_quantize, mx_swiglu_quant,
+ *   mx_swiglu_quant_bwd and their *_mode forms) have no device-side report:
+ *   such a fault leaves part of their outputs unwritten; the composite
+ *   mx_mlp_fwd / mx_mlp_bwd pass their `err_word` to every kernel they run.
  * - Scale layout MX_SCALE_MMA is the block-scaled tensor-core layout: the
  *   [R, S] scale matrix (R rows, S = cols/32 scale columns) is cut into
  *   128-row x 4-column tiles of 512 bytes; tile (rb, cb) sits at byte
